@@ -1,0 +1,402 @@
+"""Benchmark of the block-FP8 MoE layer forward on GB300.
+
+One step = one forward at each batch size of the decode workload with small
+fine-grained experts (E=128, H=2048, I=512, top_k=8, T in {1,2,4,8,16}, down
+scales padded to stride 8), on seeded synthetic inputs resident in HBM, L2
+flushed (256 MiB write) before every forward.  The metric is the decode
+routed-weight HBM bandwidth: bytes of the distinct routed experts' e4m3
+weights and valid bf16 block scales, divided by the device time of the
+forwards (CUDA events on the launching stream).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle (the only baseline the pages
+allow here) on a bounded sample of the same workload.  Under torchrun
+(N > 1) every rank runs an independent replica (the layer has no exchange
+step on one GPU per token batch); value = bytes of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_fp8_mixture_route_gb300 import api, synthetic as syn  # noqa: E402
+
+DECODE_TS = [1, 2, 4, 8, 16]
+SHAPE = syn.DECODE_SMALL
+WORKLOAD = "decode E=128 H=2048 I=512 top_k=8 T={1,2,4,8,16} w2-scale stride 8"
+METRIC = "decode routed-weight HBM GB/s"
+
+
+def routed_bytes(shape: syn.MoeShape, ids: torch.Tensor) -> tuple[int, int]:
+    """(distinct routed experts, bytes of their weights + valid block scales)."""
+    E, H, I = shape.E, shape.H, shape.I
+    v = ids[(ids >= 0) & (ids < E)]
+    D = int(torch.unique(v).numel())
+    per = 2 * I * H + H * I + 2 * ((2 * I // 128) * (H // 128)) + 2 * ((H // 128) * (I // 128))
+    return D, D * per
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.dev = dev_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if not self.p:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    the kernel source has not changed since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "block_fp8_mixture_route_gb300", "csrc", "decode.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[3] == sha:
+            return float(f[2])
+    return None
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle
+def oracle_sample(problems, budget_s: float = 12.0):
+    """Time the float64 oracle (gathered mode) on whole forwards of the
+    workload, smallest T first, until ~budget_s of CPU work; returns
+    (routed bytes processed, seconds, description)."""
+    from oracle import moe_oracle as mo
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import oracle_args
+    done_bytes, secs, parts = 0, 0.0, []
+    for T in DECODE_TS:
+        prob = problems[T]
+        args, _ = oracle_args(prob)
+        _, nbytes = routed_bytes(SHAPE, prob["topk_ids"])
+        t0 = time.perf_counter()
+        mo.forward(*args, mode="gathered", act="bf16")
+        dt = time.perf_counter() - t0
+        done_bytes += nbytes
+        secs += dt
+        parts.append(f"T={T}")
+        if secs > budget_s:
+            break
+    return done_bytes, secs, "full forwards of the workload at " + ",".join(parts)
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+def make_problems(device):
+    w13, w13s, w2, w2s = syn.make_weights(SHAPE, 0, device)
+    probs = {}
+    for T in DECODE_TS:
+        ids, w = syn.make_routing(T, SHAPE.E, SHAPE.k, 0, device, "softmax", step=T)
+        probs[T] = dict(hidden=syn.make_hidden(T, SHAPE.H, 0, device, step=T), topk_ids=ids, topk_weights=w,
+                        w13=w13, w13_scale=w13s, w2=w2, w2_scale=w2s)
+    return probs
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    probs = make_problems("cuda" if torch.cuda.is_available() else "cpu")
+    for _ in range(args.warmup):
+        oracle_sample(probs, budget_s=0.5)
+    tb, ts = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        b, s, desc = oracle_sample(probs, budget_s=8.0)
+        tb += b
+        ts += s
+    v = tb / ts / 1e9
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * ts / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "n/a (host)"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    probs = make_problems(dev)
+    s = torch.cuda.Stream(device=dev)
+    api.moe_fp8_block_reserve(max(DECODE_TS), SHAPE.k, SHAPE.H, SHAPE.I, SHAPE.E, stream=s)
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(max(256 << 20, 2 * getattr(props, "L2_cache_size", 128 << 20)), dtype=torch.uint8,
+                        device=dev)
+    outs = {T: torch.empty(T, SHAPE.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
+    info = {T: routed_bytes(SHAPE, probs[T]["topk_ids"]) for T in DECODE_TS}
+    step_bytes = sum(b for _, b in info.values())
+    step_tokens = sum(DECODE_TS)
+
+    def fwd(T):
+        api.forward_problem(probs[T], out=outs[T], stream=s, force_path="decode")
+
+    # warm-up (also compiles nothing: the library is prebuilt)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            for T in DECODE_TS:
+                flush.zero_()
+                fwd(T)
+    s.synchronize()
+    launches_per_step = 0
+    for T in DECODE_TS:
+        with torch.cuda.stream(s):
+            fwd(T)
+        launches_per_step += api.moe_fp8_block_last_launches()
+    s.synchronize()
+
+    clocks = Clocks(local)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            for i, T in enumerate(DECODE_TS):
+                flush.zero_()
+                ev[k][i][0].record(s)
+                fwd(T)
+                ev[k][i][1].record(s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    ck = clocks.stop()
+    per_T = {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i, T in enumerate(DECODE_TS)}
+    dev_ms = sum(sum(v) for v in per_T.values())
+    dev_ms_max = allreduce_max(dev_ms, world)
+    total_bytes = allreduce_sum(step_bytes * args.steps, world)
+    value = total_bytes / (dev_ms_max / 1e3) / 1e9
+    tok_s = allreduce_sum(step_tokens * args.steps, world) / (dev_ms_max / 1e3)
+
+    # dominant kernel (decode GEMM1) timed with CUDA events between the stages
+    g1_ms = gemm1_durations(probs, s, flush, args.steps)
+    D16, _ = info[16]
+    g1_bytes = {T: info[T][0] * (2 * SHAPE.I * SHAPE.H + 2 * (2 * SHAPE.I // 128) * (SHAPE.H // 128))
+                + T * SHAPE.H * 2 + T * SHAPE.k * SHAPE.I * 4 for T in DECODE_TS}
+    g1_achieved = sum(g1_bytes.values()) / (sum(g1_ms.values()) / 1e3) / 1e9
+    hbm, _, src = peaks()
+
+    # end to end through the host-buffer entry point (pinned host inputs/outputs)
+    e2e_v, h2d, d2h = e2e_hostio(probs, s, flush, args.steps, args.warmup)
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1:
+        b, secs, desc = oracle_sample(probs)
+        cpu = {"value": b / secs / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xbf16->f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every forward",
+                   "path": "decode (forced)", "replicas": world},
+        "frac_of_hbm_peak": value / hbm, "peak_source": src,
+        "tok_per_s": tok_s,
+        "per_T": {str(T): {"distinct_experts": info[T][0], "routed_MB": info[T][1] / 1e6,
+                           "us": 1e3 * statistics.median(per_T[T]),
+                           "GB_s": info[T][1] / (statistics.median(per_T[T]) / 1e3) / 1e9}
+                  for T in DECODE_TS},
+        "roofline": {"kernel": "decode_gemm1", "bound": "hbm", "achieved": g1_achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": g1_achieved / hbm,
+                     "traffic": profile_traffic("decode_gemm1_kernel", "decode_small_T16"),
+                     "peak_source": f"{src} hbm_gbs (copy, burst)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": ck,
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def gemm1_durations(probs, s, flush, steps):
+    """Median device time of the decode GEMM1 kernel per T, from CUDA events
+    the library records between its kernels (stage-timing mode)."""
+    from block_fp8_mixture_route_gb300 import _lib
+    lib = _lib.load()
+    res = {}
+    for T in DECODE_TS:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        times = []
+        for _ in range(max(steps, 3)):
+            with torch.cuda.stream(s):
+                flush.zero_()
+                import ctypes
+                arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
+                lib.moe_fp8_block_set_stage_events(arr, 5)
+                api.forward_problem(probs[T], stream=s, force_path="decode")
+            s.synchronize()
+            times.append(evs[1].elapsed_time(evs[2]))
+        res[T] = statistics.median(times)
+    return res
+
+
+def e2e_hostio(probs, s, flush, steps, warmup):
+    host = {T: (probs[T]["hidden"].cpu().pin_memory(), probs[T]["topk_ids"].cpu().pin_memory(),
+                probs[T]["topk_weights"].cpu().pin_memory(),
+                torch.empty(T, SHAPE.H, dtype=torch.bfloat16).pin_memory()) for T in DECODE_TS}
+    w = probs[1]
+    total_b, total_s = 0, 0.0
+    h2d = sum(T * SHAPE.H * 2 + T * SHAPE.k * 8 for T in DECODE_TS)
+    d2h = sum(T * SHAPE.H * 2 for T in DECODE_TS)
+    for k in range(warmup + steps):
+        for T in DECODE_TS:
+            hx, hi, hw, ho = host[T]
+            with torch.cuda.stream(s):
+                flush.zero_()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            api.moe_fp8_block_forward_hostio(hx, hi, hw, w["w13"], w["w13_scale"], w["w13_scale"].stride(1),
+                                             w["w2"], w["w2_scale"], w["w2_scale"].stride(1), out=ho, stream=s,
+                                             force_path="decode")
+            e1.record(s)
+            s.synchronize()
+            if k >= warmup:
+                total_s += e0.elapsed_time(e1) / 1e3
+                total_b += routed_bytes(SHAPE, probs[T]["topk_ids"])[1]
+    return total_b / total_s / 1e9, h2d, d2h
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

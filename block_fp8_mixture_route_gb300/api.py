@@ -1,0 +1,170 @@
+"""Python entry points with the names of the C ABI, taking torch tensors.
+
+torch supplies device memory and streams only; each function builds the C
+descriptors and calls the CUDA library (include/moe_fp8_block.h).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import MoeOptions, MoeTensor, check
+
+_DTYPES = {
+    torch.bfloat16: _lib.MOE_BF16,
+    torch.float32: _lib.MOE_F32,
+    torch.uint8: _lib.MOE_E4M3,
+    torch.float8_e4m3fn: _lib.MOE_E4M3,
+    torch.int32: _lib.MOE_I32,
+}
+
+
+def desc(t: torch.Tensor) -> MoeTensor:
+    """C descriptor of a tensor (pointer, dtype, shape, strides in elements)."""
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError("tensors must have 1..4 dimensions")
+    d = MoeTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+    d.ndim = t.dim()
+    d.dtype = _DTYPES[t.dtype]
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _options(gate_ratio, force_path) -> Optional[MoeOptions]:
+    if gate_ratio is None and force_path is None:
+        return None
+    o = MoeOptions()
+    o.gate_ratio = float(gate_ratio) if gate_ratio is not None else 0.0
+    fp = {None: 0, "auto": 0, "decode": 1, "prefill": 2}
+    o.force_path = fp[force_path] if not isinstance(force_path, int) else force_path
+    return o
+
+
+def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                          w2_scale_stride, out=None, stream=None, gate_ratio=None, force_path=None):
+    """Layer forward on device tensors; returns `out` (bf16 [T, H])."""
+    lib = _lib.load()
+    if out is None:
+        out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    o = desc(out)
+    P = ctypes.byref
+    opt = _options(gate_ratio, force_path)
+    if opt is None:
+        rc = lib.moe_fp8_block_forward(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                       int(w2_scale_stride), P(o), _stream(stream))
+    else:
+        rc = lib.moe_fp8_block_forward_ex(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                          int(w2_scale_stride), P(o), _stream(stream), P(opt))
+    check(rc, "moe_fp8_block_forward")
+    return out
+
+
+def moe_fp8_block_forward_hostio(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
+                                 w2_scale, w2_scale_stride, out=None, stream=None, gate_ratio=None,
+                                 force_path=None):
+    """Layer forward with HOST hidden/ids/weights/out (pinned for async
+    copies) and device weight banks; returns `out` once it is filled."""
+    lib = _lib.load()
+    if out is None:
+        out = torch.empty(hidden.shape, dtype=torch.bfloat16, pin_memory=True)
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    o = desc(out)
+    P = ctypes.byref
+    opt = _options(gate_ratio, force_path)
+    rc = lib.moe_fp8_block_forward_hostio(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                          int(w2_scale_stride), P(o), _stream(stream),
+                                          P(opt) if opt is not None else None)
+    check(rc, "moe_fp8_block_forward_hostio")
+    return out
+
+
+def moe_fp8_block_route(topk_ids: torch.Tensor, E: int, stream=None):
+    """Routing lists (see the header): dict of int32 device tensors."""
+    lib = _lib.load()
+    S = topk_ids.numel()
+    dev = topk_ids.device
+    r = dict(
+        counts=torch.empty(E, dtype=torch.int32, device=dev),
+        offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        perm=torch.empty(max(S, 1), dtype=torch.int32, device=dev),
+        inv=torch.empty(max(S, 1), dtype=torch.int32, device=dev),
+        glist=torch.empty(max(min(E, S), 1), dtype=torch.int32, device=dev),
+        n_distinct=torch.empty(1, dtype=torch.int32, device=dev),
+    )
+    rc = lib.moe_fp8_block_route(ctypes.byref(desc(topk_ids)), int(E), *[r[n].data_ptr() for n in
+                                 ("counts", "offsets", "perm", "inv", "glist", "n_distinct")], _stream(stream))
+    check(rc, "moe_fp8_block_route")
+    r["perm"], r["inv"], r["glist"] = r["perm"][:S], r["inv"][:S], r["glist"][:min(E, S)]
+    return r
+
+
+def moe_fp8_block_act_quant(x: torch.Tensor, stream=None):
+    """Per-row, per-128-column e4m3 quantisation: (codes uint8 [R,K], scales fp32 [R,K/128])."""
+    lib = _lib.load()
+    R, K = x.shape
+    codes = torch.empty((R, K), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((R, max(K // 128, 1)), dtype=torch.float32, device=x.device)
+    rc = lib.moe_fp8_block_act_quant(ctypes.byref(desc(x)), codes.data_ptr(), scales.data_ptr(), _stream(stream))
+    check(rc, "moe_fp8_block_act_quant")
+    return codes, scales[:, :K // 128]
+
+
+def moe_fp8_block_widen_e4m3(codes: torch.Tensor, stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    out = torch.empty(codes.shape, dtype=torch.float32, device=codes.device)
+    rc = lib.moe_fp8_block_widen_e4m3(codes.data_ptr(), codes.numel(), out.data_ptr(), _stream(stream))
+    check(rc, "moe_fp8_block_widen_e4m3")
+    return out
+
+
+def moe_fp8_block_reserve(max_T: int, k: int, H: int, I: int, E: int, stream=None):
+    check(_lib.load().moe_fp8_block_reserve(max_T, k, H, I, E, _stream(stream)), "moe_fp8_block_reserve")
+
+
+def moe_fp8_block_device_status(stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    check(_lib.load().moe_fp8_block_device_status(_stream(stream), ctypes.byref(v)), "moe_fp8_block_device_status")
+    return v.value
+
+
+def moe_fp8_block_last_path() -> int:
+    return _lib.load().moe_fp8_block_last_path()
+
+
+def moe_fp8_block_last_launches() -> int:
+    return _lib.load().moe_fp8_block_last_launches()
+
+
+def moe_fp8_block_abi_version() -> int:
+    return _lib.load().moe_fp8_block_abi_version()
+
+
+def moe_fp8_block_release():
+    _lib.load().moe_fp8_block_release()
+
+
+def forward_problem(prob: dict, out=None, stream=None, **kw):
+    """Convenience: forward on a dict of tensors (the synthetic generator's
+    layout); scale strides are read from the scale tensors."""
+    return moe_fp8_block_forward(prob["hidden"], prob["topk_ids"], prob["topk_weights"], prob["w13"],
+                                 prob["w13_scale"], prob["w13_scale"].stride(1), prob["w2"], prob["w2_scale"],
+                                 prob["w2_scale"].stride(1), out=out, stream=stream, **kw)

@@ -1,0 +1,566 @@
+// host.cu -- the C ABI of include/moe_fp8_block.h: argument checks, the
+// path gate, per-(device, stream) workspaces and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "kernels.h"
+#include "moe_fp8_block.h"
+
+namespace moe {
+
+namespace {
+
+thread_local int g_last_path = MOE_PATH_NONE;
+thread_local int g_last_launches = 0;
+
+std::mutex g_mu;
+
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::map<int, int> g_sms;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Byte layout of one workspace.
+struct Layout {
+  size_t status, counts, offsets, perm, inv, glist, nd;
+  size_t xh, xexp, h, ybuf;                       // decode
+  size_t xq, xs, hq, hs, slots, tiles, ntiles;    // prefill
+  size_t hid, tids, twts, outb;                   // host-io staging
+  size_t total;
+};
+
+Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool hostio) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const int64_t S = T * k;
+  const int64_t g = S < E ? S : E;
+  L.status = take(16);
+  L.counts = take(4 * (size_t)E);
+  L.offsets = take(4 * (size_t)(E + 1));
+  L.perm = take(4 * (size_t)S);
+  L.inv = take(4 * (size_t)S);
+  L.glist = take(4 * (size_t)(g > 0 ? g : 1));
+  L.nd = take(16);
+  if (path == MOE_PATH_DECODE) {
+    L.xh = take(2 * (size_t)(T * H));
+    L.xexp = take(4 * (size_t)T);
+    L.h = take(4 * (size_t)(S * I));
+    L.ybuf = take(4 * (size_t)(S * H));
+  } else if (path == MOE_PATH_PREFILL) {
+    L.xq = take((size_t)(T * H));
+    L.xs = take(4 * (size_t)(T * (H / 128)));
+    L.hq = take((size_t)(S * I));
+    L.hs = take(4 * (size_t)(S * (I / 128)));
+    L.slots = take(2 * (size_t)(S * H));
+    // tile list: at most ceil(S/128) + E tiles of 128 rows, 2 ints each
+    L.tiles = take(8 * (size_t)((S + 127) / 128 + E + 1));
+    L.ntiles = take(16);
+  }
+  if (hostio) {
+    L.hid = take(2 * (size_t)(T * H));
+    L.tids = take(4 * (size_t)S);
+    L.twts = take(4 * (size_t)S);
+    L.outb = take(2 * (size_t)(T * H));
+  }
+  L.total = o;
+  return L;
+}
+
+size_t layout_max(int64_t T, int k, int64_t H, int64_t I, int E, bool hostio) {
+  size_t a = make_layout(T, k, H, I, E, MOE_PATH_DECODE, hostio).total;
+  size_t b = make_layout(T, k, H, I, E, MOE_PATH_PREFILL, hostio).total;
+  return a > b ? a : b;
+}
+
+// Return the workspace of (current device, stream) with at least `bytes`.
+int get_workspace(cudaStream_t st, size_t bytes, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& ws = g_ws[std::make_pair(dev, st)];
+  if (ws.bytes >= bytes && ws.base) {
+    *out = ws.base;
+    return MOE_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_CAPTURE_GROW;
+  if (ws.base) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaFree(ws.base);
+    ws.base = nullptr;
+    ws.bytes = 0;
+  }
+  size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
+  if (cudaMalloc(&ws.base, want) != cudaSuccess) {
+    ws.base = nullptr;
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  // the status word must start cleared
+  if (cudaMemsetAsync(ws.base, 0, 16, st) != cudaSuccess) return MOE_ERR_CUDA;
+  ws.bytes = want;
+  *out = ws.base;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------- descriptor checks
+int elem_size(int dtype) {
+  switch (dtype) {
+    case MOE_BF16: return 2;
+    case MOE_F32: return 4;
+    case MOE_E4M3: return 1;
+    case MOE_I32: return 4;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_tensor(const moe_tensor* t, int ndim, int dtype) {
+  if (!t) return MOE_ERR_NULL;
+  if (t->ndim != ndim) return MOE_ERR_SHAPE;
+  if (t->dtype != dtype) return MOE_ERR_DTYPE;
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+bool contiguous(const moe_tensor* t) {
+  int64_t s = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->stride[i] != s) return false;
+    s *= t->shape[i];
+  }
+  return true;
+}
+
+// Byte extent [lo, hi) covered by a strided tensor (empty tensors: lo == hi).
+std::pair<uintptr_t, uintptr_t> extent(const moe_tensor* t) {
+  uintptr_t lo = reinterpret_cast<uintptr_t>(t->data);
+  int64_t last = 0;
+  for (int i = 0; i < t->ndim; ++i) {
+    if (t->shape[i] == 0) return {lo, lo};
+    last += (t->shape[i] - 1) * t->stride[i];
+  }
+  return {lo, lo + (uintptr_t)((last + 1) * elem_size(t->dtype))};
+}
+
+bool overlap(const moe_tensor* a, const moe_tensor* b) {
+  auto x = extent(a), y = extent(b);
+  if (x.first == x.second || y.first == y.second) return false;
+  return x.first < y.second && y.first < x.second;
+}
+
+int check_scale_bank(const moe_tensor* s, int64_t E, int64_t rows, int64_t cols, int64_t row_stride) {
+  int rc = check_tensor(s, 3, MOE_BF16);
+  if (rc) return rc;
+  if (s->shape[0] != E || s->shape[1] != rows || s->shape[2] < cols) return MOE_ERR_SHAPE;
+  if (row_stride < cols || s->stride[2] != 1 || (rows > 1 && s->stride[1] != row_stride)) return MOE_ERR_STRIDE;
+  if (E > 1 && s->stride[0] < rows * row_stride) return MOE_ERR_STRIDE;
+  if (!s->data) return MOE_ERR_NULL;
+  return MOE_OK;
+}
+
+struct Checked {
+  LayerArgs a;
+  int64_t T;
+};
+
+int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
+                  const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                  const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride,
+                  const moe_tensor* out, bool host_io, Checked* c) {
+  int rc;
+  if ((rc = check_tensor(hidden, 2, MOE_BF16))) return rc;
+  if ((rc = check_tensor(topk_ids, 2, MOE_I32))) return rc;
+  if ((rc = check_tensor(topk_weights, 2, MOE_F32))) return rc;
+  if ((rc = check_tensor(w13, 3, MOE_E4M3))) return rc;
+  if ((rc = check_tensor(w2, 3, MOE_E4M3))) return rc;
+  if ((rc = check_tensor(out, 2, MOE_BF16))) return rc;
+  const int64_t T = hidden->shape[0], H = hidden->shape[1];
+  const int64_t k = topk_ids->shape[1];
+  const int64_t E = w13->shape[0];
+  const int64_t I2 = w13->shape[1];
+  if (topk_ids->shape[0] != T || topk_weights->shape[0] != T || topk_weights->shape[1] != k) return MOE_ERR_SHAPE;
+  if (out->shape[0] != T || out->shape[1] != H) return MOE_ERR_SHAPE;
+  if (k < 1 || k > 64 || E < 1 || E > 4096) return MOE_ERR_ARG;
+  if (w13->shape[2] != H || I2 % 2 != 0) return MOE_ERR_SHAPE;
+  const int64_t I = I2 / 2;
+  if (H <= 0 || I <= 0 || H % 128 != 0 || I % 128 != 0) return MOE_ERR_SHAPE;
+  if (w2->shape[0] != E || w2->shape[1] != H || w2->shape[2] != I) return MOE_ERR_SHAPE;
+  if (H > (1 << 20) || I > (1 << 20) || T > (1 << 24) / k) return MOE_ERR_ARG;
+  if ((rc = check_scale_bank(w13_scale, E, 2 * I / 128, H / 128, w13_scale_stride))) return rc;
+  if ((rc = check_scale_bank(w2_scale, E, H / 128, I / 128, w2_scale_stride))) return rc;
+  if (!contiguous(w13) || !contiguous(w2)) return MOE_ERR_STRIDE;
+  if (!contiguous(topk_ids) || !contiguous(topk_weights) || !contiguous(out)) return MOE_ERR_STRIDE;
+  if (hidden->stride[1] != 1 || (T > 1 && hidden->stride[0] < H)) return MOE_ERR_STRIDE;
+  if (host_io && T > 1 && hidden->stride[0] != H) return MOE_ERR_STRIDE;
+  if (T > 0) {
+    if (!hidden->data || !topk_ids->data || !topk_weights->data || !out->data) return MOE_ERR_NULL;
+    if (!aligned16(hidden->data) || !aligned16(out->data)) return MOE_ERR_ALIGN;
+    if (hidden->stride[0] % 8 != 0) return MOE_ERR_ALIGN;
+    if (!aligned16(topk_ids->data) && !host_io) return MOE_ERR_ALIGN;
+  }
+  if (!w13->data || !w2->data) return MOE_ERR_NULL;
+  if (!aligned16(w13->data) || !aligned16(w2->data)) return MOE_ERR_ALIGN;
+  if (!host_io) {
+    const moe_tensor* ins[] = {hidden, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale};
+    for (const moe_tensor* t : ins)
+      if (overlap(out, t)) return MOE_ERR_ALIAS;
+  }
+  LayerArgs& a = c->a;
+  a.hidden = static_cast<const uint16_t*>(hidden->data);
+  a.hidden_ld = T > 1 ? hidden->stride[0] : H;
+  a.ids = static_cast<const int32_t*>(topk_ids->data);
+  a.wts = static_cast<const float*>(topk_weights->data);
+  a.w13 = static_cast<const uint8_t*>(w13->data);
+  a.w13s = static_cast<const uint16_t*>(w13_scale->data);
+  a.s13_row = w13_scale_stride;
+  a.s13_exp = E > 1 ? w13_scale->stride[0] : (2 * I / 128) * w13_scale_stride;
+  a.w2 = static_cast<const uint8_t*>(w2->data);
+  a.w2s = static_cast<const uint16_t*>(w2_scale->data);
+  a.s2_row = w2_scale_stride;
+  a.s2_exp = E > 1 ? w2_scale->stride[0] : (H / 128) * w2_scale_stride;
+  a.out = static_cast<uint16_t*>(out->data);
+  a.T = (int)T;
+  a.k = (int)k;
+  a.H = (int)H;
+  a.I = (int)I;
+  a.E = (int)E;
+  a.S = (int)(T * k);
+  c->T = T;
+  return MOE_OK;
+}
+
+int check_options(const moe_options* opt, float* ratio, int* force) {
+  *ratio = 0.4f;
+  *force = MOE_PATH_NONE;
+  if (!opt) return MOE_OK;
+  for (int i = 0; i < 6; ++i)
+    if (opt->reserved[i] != 0) return MOE_ERR_ARG;
+  if (opt->force_path < MOE_PATH_NONE || opt->force_path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (opt->gate_ratio > 0.f) *ratio = opt->gate_ratio;
+  *force = opt->force_path;
+  return MOE_OK;
+}
+
+int device_ok(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int maj = 0, min = 0;
+  if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (maj != 10 || min != 3) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+// Run the forward on device buffers already described by `a`.
+int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, bool hostio, void* ws_base,
+                const Layout& L, int dev) {
+  char* w = static_cast<char*>(ws_base);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+  RouteBufs rb;
+  rb.counts = reinterpret_cast<int32_t*>(w + L.counts);
+  rb.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  rb.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  rb.inv = reinterpret_cast<int32_t*>(w + L.inv);
+  rb.glist = reinterpret_cast<int32_t*>(w + L.glist);
+  rb.nd = reinterpret_cast<int32_t*>(w + L.nd);
+  (void)hostio;
+  int path = force;
+  if (path == MOE_PATH_NONE)
+    path = ((double)a.T * a.k <= (double)a.E * ratio) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  int launches = 0;
+  cudaError_t err;
+  if (path == MOE_PATH_DECODE) {
+    DecodeBufs db;
+    db.xh = reinterpret_cast<uint16_t*>(w + L.xh);
+    db.xexp = reinterpret_cast<int32_t*>(w + L.xexp);
+    db.h = reinterpret_cast<float*>(w + L.h);
+    db.ybuf = reinterpret_cast<float*>(w + L.ybuf);
+    err = launch_decode(a, rb, db, status, dev, st, &launches);
+  } else {
+    PrefillBufs pb;
+    pb.xq = reinterpret_cast<uint8_t*>(w + L.xq);
+    pb.xs = reinterpret_cast<float*>(w + L.xs);
+    pb.hq = reinterpret_cast<uint8_t*>(w + L.hq);
+    pb.hs = reinterpret_cast<float*>(w + L.hs);
+    pb.slots = reinterpret_cast<uint16_t*>(w + L.slots);
+    pb.tiles = reinterpret_cast<int32_t*>(w + L.tiles);
+    pb.ntiles = reinterpret_cast<int32_t*>(w + L.ntiles);
+    err = launch_prefill(a, rb, pb, status, dev, st, &launches);
+  }
+  if (err == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return MOE_ERR_ARG;
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  stage_events().n = 0;
+  g_last_path = path;
+  g_last_launches = launches;
+  return MOE_OK;
+}
+
+int choose_path(const LayerArgs& a, float ratio, int force) {
+  if (force != MOE_PATH_NONE) return force;
+  return ((double)a.T * a.k <= (double)a.E * ratio) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+}
+
+int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
+                 const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                 const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
+                 void* stream, const moe_options* opt, bool hostio) {
+  Checked c{};
+  int rc = check_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                         w2_scale_stride, out, hostio, &c);
+  if (rc) return rc;
+  float ratio;
+  int force;
+  if ((rc = check_options(opt, &ratio, &force))) return rc;
+  if (c.T == 0) {
+    g_last_launches = 0;
+    return MOE_OK;
+  }
+  int dev;
+  if ((rc = device_ok(&dev))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LayerArgs a = c.a;
+  const int path = choose_path(a, ratio, force);
+  const Layout L = make_layout(c.T, a.k, a.H, a.I, a.E, path, hostio);
+  void* ws = nullptr;
+  if ((rc = get_workspace(st, L.total, &ws))) return rc;
+  char* w = static_cast<char*>(ws);
+  if (hostio) {
+    const size_t xb = 2 * (size_t)a.T * a.H, sb = 4 * (size_t)a.S;
+    if (cudaMemcpyAsync(w + L.hid, hidden->data, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(w + L.tids, topk_ids->data, sb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(w + L.twts, topk_weights->data, sb, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    a.hidden = reinterpret_cast<const uint16_t*>(w + L.hid);
+    a.hidden_ld = a.H;
+    a.ids = reinterpret_cast<const int32_t*>(w + L.tids);
+    a.wts = reinterpret_cast<const float*>(w + L.twts);
+    a.out = reinterpret_cast<uint16_t*>(w + L.outb);
+  }
+  rc = run_forward(a, ratio, path, st, hostio, ws, L, dev);
+  if (rc) return rc;
+  if (hostio) {
+    if (cudaMemcpyAsync(out->data, w + L.outb, 2 * (size_t)a.T * a.H, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+StageEvents& stage_events() {
+  static thread_local StageEvents se;
+  return se;
+}
+
+bool stage_mark(cudaStream_t st, int i) {
+  StageEvents& se = stage_events();
+  if (se.n == 0) return false;
+  if (i < se.n) cudaEventRecord(se.ev[i], st);
+  return true;
+}
+
+int num_sms(int device) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sms.find(device);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+  if (n <= 0) n = 1;
+  g_sms[device] = n;
+  return n;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_fp8_block_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
+                          const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                          const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride,
+                          moe_tensor* out, void* stream) {
+  return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                      w2_scale_stride, out, stream, nullptr, false);
+}
+
+int moe_fp8_block_forward_ex(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                             const moe_tensor* topk_weights, const moe_tensor* w13,
+                             const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,
+                             const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
+                             void* stream, const moe_options* opt) {
+  return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                      w2_scale_stride, out, stream, opt, false);
+}
+
+int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                 const moe_tensor* topk_weights, const moe_tensor* w13,
+                                 const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,
+                                 const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
+                                 void* stream, const moe_options* opt) {
+  return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                      w2_scale_stride, out, stream, opt, true);
+}
+
+int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                        int32_t* inv, int32_t* glist, int32_t* n_distinct, void* stream) {
+  int rc = check_tensor(topk_ids, 2, MOE_I32);
+  if (rc) return rc;
+  if (!contiguous(topk_ids)) return MOE_ERR_STRIDE;
+  if (E < 1 || E > 4096) return MOE_ERR_ARG;
+  const int64_t S = topk_ids->shape[0] * topk_ids->shape[1];
+  if (S > (1 << 24)) return MOE_ERR_ARG;
+  if (!counts || !offsets || !n_distinct || (S > 0 && (!perm || !inv || !glist || !topk_ids->data)))
+    return MOE_ERR_NULL;
+  int dev;
+  if ((rc = device_ok(&dev))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = get_workspace(st, 16, &ws))) return rc;
+  RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct};
+  if (launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb, static_cast<uint32_t*>(ws), st) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_fp8_block_act_quant(const moe_tensor* x, uint8_t* codes, float* scales, void* stream) {
+  int rc = check_tensor(x, 2, MOE_BF16);
+  if (rc) return rc;
+  const int64_t R = x->shape[0], K = x->shape[1];
+  if (K % 128 != 0 || R > (1 << 24) || K > (1 << 20)) return MOE_ERR_SHAPE;
+  if (x->stride[1] != 1 || (R > 1 && x->stride[0] < K)) return MOE_ERR_STRIDE;
+  if (R == 0 || K == 0) return MOE_OK;
+  if (!x->data || !codes || !scales) return MOE_ERR_NULL;
+  if (!aligned16(x->data) || !aligned16(codes) || (R > 1 && x->stride[0] % 8 != 0)) return MOE_ERR_ALIGN;
+  int dev;
+  if ((rc = device_ok(&dev))) return rc;
+  if (launch_act_quant(static_cast<const uint16_t*>(x->data), R > 1 ? x->stride[0] : K, (int)R, (int)K, codes,
+                       scales, static_cast<cudaStream_t>(stream), false) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_fp8_block_widen_e4m3(const uint8_t* codes, int64_t n, float* out, void* stream) {
+  if (n < 0) return MOE_ERR_ARG;
+  if (n == 0) return MOE_OK;
+  if (!codes || !out) return MOE_ERR_NULL;
+  int dev, rc;
+  if ((rc = device_ok(&dev))) return rc;
+  if (launch_widen(codes, n, out, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_fp8_block_reserve(int64_t max_T, int32_t k, int64_t H, int64_t I, int32_t E, void* stream) {
+  if (max_T < 0 || k < 1 || k > 64 || E < 1 || E > 4096 || H <= 0 || I <= 0 || H % 128 || I % 128)
+    return MOE_ERR_ARG;
+  int dev, rc;
+  if ((rc = device_ok(&dev))) return rc;
+  void* ws = nullptr;
+  rc = get_workspace(static_cast<cudaStream_t>(stream), layout_max(max_T, k, H, I, E, true), &ws);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_fp8_block_device_status(void* stream, uint32_t* status) {
+  if (!status) return MOE_ERR_NULL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_ws.find(std::make_pair(dev, st));
+    if (it != g_ws.end()) base = it->second.base;
+  }
+  *status = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!base) return MOE_OK;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, base, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+int moe_fp8_block_last_path(void) { return g_last_path; }
+
+int moe_fp8_block_last_launches(void) { return g_last_launches; }
+
+int moe_fp8_block_set_stage_events(void* const* events, int n) {
+  if (n < 0 || n > 16 || (n > 0 && !events)) return MOE_ERR_ARG;
+  StageEvents& se = stage_events();
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return MOE_ERR_NULL;
+    se.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  se.n = n;
+  return MOE_OK;
+}
+
+int moe_fp8_block_abi_version(void) { return MOE_FP8_BLOCK_ABI_VERSION; }
+
+const char* moe_fp8_block_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer or descriptor is NULL";
+    case MOE_ERR_DTYPE: return "wrong element type";
+    case MOE_ERR_SHAPE: return "inconsistent shapes, or H / I not a multiple of 128";
+    case MOE_ERR_ALIGN: return "a base pointer or row stride is not 16-byte aligned";
+    case MOE_ERR_STRIDE: return "unsupported stride";
+    case MOE_ERR_ALIAS: return "out overlaps an input";
+    case MOE_ERR_CAPTURE_GROW: return "workspace must grow while the stream is being captured; reserve first";
+    case MOE_ERR_CUDA: return "a CUDA call failed";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
+    default: return "unknown error code";
+  }
+}
+
+void moe_fp8_block_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& kv : g_ws)
+    if (kv.second.base) cudaFree(kv.second.base);
+  g_ws.clear();
+}
+
+}  // extern "C"

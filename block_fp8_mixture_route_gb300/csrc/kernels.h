@@ -1,0 +1,87 @@
+// kernels.h -- host-side launchers of the CUDA kernels (internal to the
+// library; the public interface is include/moe_fp8_block.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Arguments shared by the kernels of one forward call.  All pointers are
+// device memory.  Scale banks are bf16 bit patterns.
+struct LayerArgs {
+  const uint16_t* hidden;      // bf16 [T, H], row stride hidden_ld
+  int64_t hidden_ld;
+  const int32_t* ids;          // [T, k]
+  const float* wts;            // [T, k]
+  const uint8_t* w13;          // e4m3 [E, 2I, H]
+  const uint16_t* w13s;        // bf16 [E, 2I/128, s13_row], expert stride s13_exp
+  int64_t s13_row, s13_exp;
+  const uint8_t* w2;           // e4m3 [E, H, I]
+  const uint16_t* w2s;         // bf16 [E, H/128, s2_row], expert stride s2_exp
+  int64_t s2_row, s2_exp;
+  uint16_t* out;               // bf16 [T, H]
+  int T, k, H, I, E, S;        // S = T*k
+};
+
+// Routing lists produced by the route kernel (device int32 buffers).
+struct RouteBufs {
+  int32_t* counts;    // [E]
+  int32_t* offsets;   // [E+1]
+  int32_t* perm;      // [S]
+  int32_t* inv;       // [S]
+  int32_t* glist;     // [min(E,S)]
+  int32_t* nd;        // [1]
+};
+
+// Scratch of the decode path.
+struct DecodeBufs {
+  uint16_t* xh;       // f16 [T, H]: activations scaled by 2^-xexp[t]
+  int32_t* xexp;      // [T]
+  float* h;           // [S, I] in routed (perm) order
+  float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
+};
+
+// Scratch of the prefill path.
+struct PrefillBufs {
+  uint8_t* xq;        // e4m3 [T, H] activation codes
+  float* xs;          // [T, H/128] activation scales
+  uint8_t* hq;        // e4m3 [S, I] h codes, routed order
+  float* hs;          // [S, I/128] h scales
+  uint16_t* slots;    // bf16 [S, H] per-slot outputs times top-k weight, slot order
+  int32_t* tiles;     // tile work list
+  int32_t* ntiles;    // [1]
+};
+
+int num_sms(int device);
+
+// Stage events of moe_fp8_block_set_stage_events (per host thread).
+struct StageEvents {
+  cudaEvent_t ev[16];
+  int n = 0;
+};
+StageEvents& stage_events();
+// Record stage event i on st if one was requested; returns true while stage
+// events are active (the launchers then drop programmatic dependent launch).
+bool stage_mark(cudaStream_t st, int i);
+
+cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, uint32_t* status,
+                         cudaStream_t st);
+cudaError_t launch_widen(const uint8_t* codes, int64_t n, float* out, cudaStream_t st);
+
+// Decode (W8A16) path: prep (route + f16 activations), GEMM1+silu*up,
+// GEMM2, combine.  Adds the number of launches to *launches.
+cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeBufs& db, uint32_t* status,
+                          int device, cudaStream_t st, int* launches);
+
+// Prefill (W8A8) path.
+cudaError_t launch_act_quant(const uint16_t* x, int64_t ld, int R, int K, uint8_t* codes, float* scales,
+                             cudaStream_t st, bool pdl);
+cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, uint32_t* status,
+                           int device, cudaStream_t st, int* launches);
+
+// Shared-memory bytes the route kernel needs for E experts with nthreads.
+size_t route_smem_bytes(int E, int nthreads);
+int route_threads(int E);
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+/*
+ * moe_fp8_block.h -- C ABI of the block-FP8 mixture-of-experts layer forward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (one call of moe_fp8_block_forward):
+ *   for every token t and routed slot j (expert e = topk_ids[t,j]):
+ *     [gate; up] = dequant(w13[e]) . x_t           (one fused projection)
+ *     h          = silu(gate) * up
+ *     y_{t,j}    = dequant(w2[e]) . h              (fp32 accumulation)
+ *   out_t = sum_j topk_weights[t,j] * y_{t,j}      (fixed order, no atomics)
+ * Only the g = min(E, T*k) routed experts are read ("gathered-expert FP8 MoE
+ * combine", fp8-moe-gather page, sections Problem and The fix).
+ *
+ * Weight format (FreeToken PR #662, PR body): every expert bank is e4m3
+ * (float8 e4m3fn bytes) row-major [rows, K], K contiguous per output row,
+ * with one bf16 scale per 128x128 block.  The scale bank's row stride may be
+ * padded (same PR, commit "honor padded fp8 scale strides"), so it is passed
+ * explicitly and never recomputed from K.  w13 stacks the gate and up
+ * projections along the output rows: rows [0, I) gate, rows [I, 2I) up
+ * (tpu-inference PR #3040, review of the bias DMA: gate half at
+ * n_id*tile_n1, up half at out_n1 + n_id*tile_n1).
+ *
+ * Paths (chosen per call; the choice is readable through
+ * moe_fp8_block_last_path):
+ *   decode  (W8A16): taken while T*k <= E*ratio, ratio 0.4 by default
+ *     (fp8-moe-gather page, environment-variable table).  bf16 activations,
+ *     e4m3 weights widened in registers, fp32 accumulation and fp32 h.
+ *   prefill (W8A8): activations quantised per token per 128 columns with a
+ *     dynamic scale amax/448 (fp8-moe-gather page, "Affects": dynamic
+ *     activation scales), grouped FP8 tensor-core GEMMs, h quantised the same
+ *     way, fp32 accumulation.
+ *
+ * Conventions common to all entry points:
+ *   - Every pointer is DEVICE memory unless the entry point says otherwise.
+ *     The caller owns every buffer it passes; the library never frees them.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous unless stated otherwise.  No entry point
+ *     that takes a stream synchronises it, except moe_fp8_block_device_status
+ *     and moe_fp8_block_forward_hostio.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  All argument
+ *     checks run on the host before anything is enqueued; on error nothing is
+ *     enqueued and the output is untouched.  No C++ exception crosses the ABI.
+ *   - Inputs are never modified.  `out` is fully overwritten.
+ *   - The library keeps a workspace per (device, stream), grown on demand.
+ *     Growth calls cudaMalloc, which is not allowed while the stream is being
+ *     captured into a CUDA graph: call moe_fp8_block_reserve first with the
+ *     largest sizes, then capture (growth during capture returns
+ *     MOE_ERR_CAPTURE_GROW).  Calls on one stream are ordered by the stream;
+ *     calls on different streams use different workspaces.
+ */
+#ifndef MOE_FP8_BLOCK_H
+#define MOE_FP8_BLOCK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight-format / ABI identifier.  The Python binding refuses a library whose
+ * moe_fp8_block_abi_version() differs, so a stale build fails loudly instead
+ * of reading the banks with the wrong layout (FreeToken PR #662, PR body: the
+ * weight-format ABI probe max_weight_format_id). */
+#define MOE_FP8_BLOCK_ABI_VERSION 1
+
+/* Element types of moe_tensor.dtype. */
+typedef enum {
+  MOE_BF16 = 1,  /* bfloat16 (2 bytes)                                   */
+  MOE_F32 = 2,   /* IEEE binary32                                        */
+  MOE_E4M3 = 3,  /* float8 e4m3fn byte (codes 0x7F/0xFF are NaN)         */
+  MOE_I32 = 4    /* int32                                                */
+} moe_dtype;
+
+/* A strided view of a buffer.  Strides are in ELEMENTS, shape[i] >= 0. */
+typedef struct {
+  void* data;         /* device pointer (host pointer where stated)       */
+  int32_t ndim;       /* 1..4                                             */
+  int32_t dtype;      /* moe_dtype                                        */
+  int64_t shape[4];
+  int64_t stride[4];
+} moe_tensor;
+
+/* Return codes. */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,          /* a required pointer or descriptor is NULL         */
+  MOE_ERR_DTYPE = -2,         /* wrong element type                               */
+  MOE_ERR_SHAPE = -3,         /* inconsistent shapes; H or I not a multiple of 128 */
+  MOE_ERR_ALIGN = -4,         /* a base pointer is not 16-byte aligned            */
+  MOE_ERR_STRIDE = -5,        /* unsupported stride (see each argument)           */
+  MOE_ERR_ALIAS = -6,         /* out overlaps an input                            */
+  MOE_ERR_CAPTURE_GROW = -7,  /* workspace must grow while the stream is captured */
+  MOE_ERR_CUDA = -8,          /* a CUDA runtime/driver call failed                */
+  MOE_ERR_ARG = -9,           /* another invalid argument (sizes, options)        */
+  MOE_ERR_DEVICE = -10        /* unsupported device (not compute capability 10.3) */
+};
+
+/* Paths, as reported by moe_fp8_block_last_path and forced by options. */
+enum { MOE_PATH_NONE = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 };
+
+/* Bits of the device status word (moe_fp8_block_device_status). */
+enum {
+  MOE_STATUS_BAD_ID = 1u,    /* a topk id >= E was seen; its slot was skipped   */
+  MOE_STATUS_TIMEOUT = 2u    /* a bounded pipeline wait gave up; output invalid */
+};
+
+/* Options of moe_fp8_block_forward_ex.  Zero-initialise, then set fields. */
+typedef struct {
+  float gate_ratio;   /* decode while T*k <= E*gate_ratio; <= 0 -> 0.4          */
+  int32_t force_path; /* MOE_PATH_NONE (gate decides), _DECODE or _PREFILL     */
+  int32_t reserved[6];/* must be zero                                          */
+} moe_options;
+
+/*
+ * moe_fp8_block_forward -- the layer forward.
+ *
+ *  hidden        bf16 [T, H], stride[1] == 1, stride[0] >= H.  T >= 0.
+ *  topk_ids      int32 [T, k], contiguous.  An id < 0 skips its slot (it adds
+ *                nothing); an id >= E skips its slot and sets
+ *                MOE_STATUS_BAD_ID.  A token may name one expert twice: each
+ *                slot counts.
+ *  topk_weights  fp32 [T, k], contiguous; used as given (no renormalisation).
+ *  w13           e4m3 [E, 2I, H], contiguous; rows [0,I) gate, [I,2I) up.
+ *  w13_scale     bf16 [E, 2I/128, >= H/128]; stride[2] == 1,
+ *                stride[1] == w13_scale_stride >= H/128,
+ *                stride[0] >= (2I/128) * w13_scale_stride.
+ *  w13_scale_stride  row stride of w13_scale in elements (read from the tensor
+ *                by the caller; it may be padded).
+ *  w2            e4m3 [E, H, I], contiguous.
+ *  w2_scale      bf16 [E, H/128, >= I/128]; stride rules as for w13_scale
+ *                with w2_scale_stride >= I/128.
+ *  out           bf16 [T, H], contiguous; must not overlap any input.
+ *  stream        cudaStream_t.
+ * H and I must be multiples of 128; k in [1, 64]; E in [1, 4096].  Every
+ * base pointer must be 16-byte aligned.  T == 0 is a no-op returning MOE_OK.
+ */
+int moe_fp8_block_forward(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                          const moe_tensor* topk_weights, const moe_tensor* w13,
+                          const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                          const moe_tensor* w2, const moe_tensor* w2_scale,
+                          int64_t w2_scale_stride, moe_tensor* out, void* stream);
+
+/* As moe_fp8_block_forward, with options (NULL = defaults). */
+int moe_fp8_block_forward_ex(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                             const moe_tensor* topk_weights, const moe_tensor* w13,
+                             const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                             const moe_tensor* w2, const moe_tensor* w2_scale,
+                             int64_t w2_scale_stride, moe_tensor* out, void* stream,
+                             const moe_options* opt);
+
+/* As moe_fp8_block_forward_ex, but hidden, topk_ids, topk_weights and out
+ * are HOST buffers (page-locked memory gives asynchronous copies; pageable
+ * memory works but copies synchronously).  The weight banks stay device
+ * memory.  The inputs are copied to the workspace, the forward runs and the
+ * output is copied back, all on `stream`; the call returns after
+ * synchronising `stream`, with `out` filled. */
+int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                 const moe_tensor* topk_weights, const moe_tensor* w13,
+                                 const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                                 const moe_tensor* w2, const moe_tensor* w2_scale,
+                                 int64_t w2_scale_stride, moe_tensor* out, void* stream,
+                                 const moe_options* opt);
+
+/*
+ * moe_fp8_block_route -- the routing lists of the gathered path, on their
+ * own (the same kernel the forward runs).  For S = T*k slots s = t*k + j:
+ *  counts   int32 [E]     slots per expert (valid ids only)
+ *  offsets  int32 [E+1]   exclusive prefix sum of counts
+ *  perm     int32 [S]     slot indices grouped by expert ascending, stable in
+ *                         s; entries past offsets[E] are -1
+ *  inv      int32 [S]     position of slot s in perm, or -1 when skipped
+ *  glist    int32 [min(E,S)] distinct routed experts ascending, padded with -1
+ *  n_distinct int32 [1]   number of distinct routed experts
+ * ("the g = min(local_experts, tokens * top_k) routed experts are gathered",
+ * fp8-moe-gather page, The fix.)  All outputs are device int32 buffers of the
+ * sizes above, contiguous.  Requires S <= 2^24.
+ */
+int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* glist,
+                        int32_t* n_distinct, void* stream);
+
+/*
+ * moe_fp8_block_act_quant -- the dynamic activation quantisation of the
+ * prefill path, on its own (the same kernel the forward runs): for each row r
+ * of x (bf16 [R, K], stride[1] == 1, K a multiple of 128) and each 128-column
+ * group c: amax = max |x|, scale = amax / 448 in IEEE fp32,
+ * code = e4m3(x / scale) rounded to nearest even and saturated to +-448
+ * (amax == 0 gives scale 0 and codes 0).
+ *  codes   uint8 [R, K] contiguous (e4m3 bytes)
+ *  scales  fp32 [R, K/128] contiguous
+ */
+int moe_fp8_block_act_quant(const moe_tensor* x, uint8_t* codes, float* scales, void* stream);
+
+/*
+ * moe_fp8_block_widen_e4m3 -- the in-register e4m3 widening used by the
+ * decode kernels, applied to n bytes: out[i] = value of codes[i] as fp32
+ * (exact for every finite code; FreeToken PR #662, PR body: e4m3 -> bf16 is
+ * exact).  codes: device uint8 [n]; out: device fp32 [n].
+ */
+int moe_fp8_block_widen_e4m3(const uint8_t* codes, int64_t n, float* out, void* stream);
+
+/* Pre-size the workspace of (current device, stream) for calls with up to
+ * max_T tokens of the given layer shape, so that a later call can be
+ * captured into a CUDA graph.  Synchronous with respect to the host. */
+int moe_fp8_block_reserve(int64_t max_T, int32_t k, int64_t H, int64_t I, int32_t E,
+                          void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word of the
+ * (current device, stream) workspace into *status (MOE_STATUS_* bits). */
+int moe_fp8_block_device_status(void* stream, uint32_t* status);
+
+/* Path taken by the last successful forward call on this host thread:
+ * MOE_PATH_DECODE, MOE_PATH_PREFILL, or MOE_PATH_NONE before any call. */
+int moe_fp8_block_last_path(void);
+
+/* Number of kernel launches the last successful forward call on this host
+ * thread enqueued. */
+int moe_fp8_block_last_launches(void);
+
+/* Profiling aid.  The next forward call on this host thread records
+ * events[i] (cudaEvent_t, created by the caller) on its stream before its
+ * i-th kernel launch and one more event after its last launch, for as many
+ * events as given (n <= 16), then forgets them.  While events are recorded
+ * the kernels are launched without programmatic dependent launch, so each
+ * interval is one kernel's device time.  n == 0 clears. */
+int moe_fp8_block_set_stage_events(void* const* events, int n);
+
+/* MOE_FP8_BLOCK_ABI_VERSION of the built library. */
+int moe_fp8_block_abi_version(void);
+
+/* Static description of a return code (never NULL). */
+const char* moe_fp8_block_error_string(int code);
+
+/* Free every workspace (all devices, all streams).  No call may be in flight. */
+void moe_fp8_block_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_BLOCK_H */

@@ -1,0 +1,166 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every
+symbol the header declares, and rejects bad arguments on the host before
+touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from block_fp8_mixture_route_gb300 import _lib, api, synthetic as syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_fp8_block.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_fp8_block_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    assert sorted(names) == sorted(_lib.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.moe_fp8_block_abi_version() == _lib.ABI_VERSION
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, 12345]:
+        assert len(_lib.error_string(code)) > 0
+    assert lib.moe_fp8_block_last_path() == _lib.MOE_PATH_NONE
+
+
+def _descs(prob):
+    return [api.desc(prob[n]) for n in ("hidden", "topk_ids", "topk_weights", "w13", "w13_scale", "w2", "w2_scale")]
+
+
+def _call(lib, prob, out=None, s13=None, s2=None, opt=None, mutate=None):
+    d = _descs(prob)
+    o = api.desc(out if out is not None else torch.empty(prob["hidden"].shape, dtype=torch.bfloat16))
+    if mutate:
+        mutate(d, o)
+    s13 = prob["w13_scale"].stride(1) if s13 is None else s13
+    s2 = prob["w2_scale"].stride(1) if s2 is None else s2
+    P = ctypes.byref
+    if opt is None:
+        return lib.moe_fp8_block_forward(P(d[0]), P(d[1]), P(d[2]), P(d[3]), P(d[4]), s13, P(d[5]), P(d[6]), s2,
+                                         P(o), None)
+    return lib.moe_fp8_block_forward_ex(P(d[0]), P(d[1]), P(d[2]), P(d[3]), P(d[4]), s13, P(d[5]), P(d[6]), s2,
+                                        P(o), None, P(opt))
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return syn.make_problem(syn.TINY, T=4, seed=0)
+
+
+def test_null_descriptor(lib):
+    P = ctypes.byref
+    t = api.desc(torch.zeros(4, 256, dtype=torch.bfloat16))
+    assert lib.moe_fp8_block_forward(None, P(t), P(t), P(t), P(t), 2, P(t), P(t), 1, P(t), None) == -1
+
+
+@pytest.mark.parametrize("case,code", [
+    ("hidden_dtype", -2), ("ids_dtype", -2), ("w13_dtype", -2),
+    ("H_not_128", -3), ("out_shape", -3), ("scale_rows", -3),
+    ("s13_small", -5), ("s2_mismatch", -5), ("w13_noncontig", -5),
+    ("unaligned_hidden", -4), ("alias", -6), ("k_zero", -3), ("null_data", -1),
+])
+def test_argument_errors(lib, tiny, case, code):
+    prob = dict(tiny)
+    out = None
+    s13 = s2 = None
+    mutate = None
+    if case == "hidden_dtype":
+        prob["hidden"] = tiny["hidden"].float()
+    elif case == "ids_dtype":
+        prob["topk_ids"] = tiny["topk_ids"].long() if False else tiny["topk_ids"].float()
+    elif case == "w13_dtype":
+        prob["w13"] = tiny["w13"].to(torch.int32)
+    elif case == "H_not_128":
+        def mutate(d, o):
+            d[0].shape[1] = 200
+            o.shape[1] = 200
+    elif case == "out_shape":
+        out = torch.empty(3, 256, dtype=torch.bfloat16)
+    elif case == "scale_rows":
+        prob["w2_scale"] = tiny["w2_scale"][:, :1]
+    elif case == "s13_small":
+        s13 = 1
+    elif case == "s2_mismatch":
+        s2 = 3
+    elif case == "w13_noncontig":
+        prob["w13"] = tiny["w13"].transpose(1, 2)
+    elif case == "unaligned_hidden":
+        big = torch.zeros(4 * 256 + 8, dtype=torch.bfloat16)
+        prob["hidden"] = big[1:1 + 4 * 256].view(4, 256)
+    elif case == "alias":
+        out = tiny["hidden"]
+    elif case == "k_zero":
+        prob["topk_ids"] = tiny["topk_ids"][:, :0]
+        prob["topk_weights"] = tiny["topk_weights"][:, :0]
+    elif case == "null_data":
+        def mutate(d, o):
+            d[3].data = None
+    if case == "k_zero":
+        rc = _call(lib, prob, out, s13, s2, mutate=mutate)
+        assert rc in (-3, -9)
+        return
+    assert _call(lib, prob, out, s13, s2, mutate=mutate) == code
+
+
+def test_bad_options(lib, tiny):
+    o = _lib.MoeOptions()
+    o.force_path = 7
+    assert _call(lib, tiny, opt=o) == -9
+    o = _lib.MoeOptions()
+    o.reserved[2] = 1
+    assert _call(lib, tiny, opt=o) == -9
+
+
+def test_empty_batch_is_noop(lib):
+    prob = syn.make_problem(syn.TINY, T=0, seed=0)
+    assert _call(lib, prob) == 0
+
+
+def test_no_device_is_reported(lib, tiny):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _call(lib, tiny)
+    assert rc in (-8, -10)
+    assert lib.moe_fp8_block_route(ctypes.byref(api.desc(tiny["topk_ids"])), 8, 1, 1, 1, 1, 1, 1, None) in (-8, -10)
+
+
+def test_route_argument_errors(lib, tiny):
+    d = api.desc(tiny["topk_ids"])
+    P = ctypes.byref
+    assert lib.moe_fp8_block_route(P(d), 0, 1, 1, 1, 1, 1, 1, None) == -9
+    assert lib.moe_fp8_block_route(P(d), 8, None, 1, 1, 1, 1, 1, None) == -1
+    f = api.desc(tiny["topk_weights"])
+    assert lib.moe_fp8_block_route(P(f), 8, 1, 1, 1, 1, 1, 1, None) == -2
+
+
+def test_act_quant_argument_errors(lib):
+    P = ctypes.byref
+    x = api.desc(torch.zeros(2, 200, dtype=torch.bfloat16))
+    assert lib.moe_fp8_block_act_quant(P(x), 16, 16, None) == -3
+    x = api.desc(torch.zeros(2, 256, dtype=torch.float32))
+    assert lib.moe_fp8_block_act_quant(P(x), 16, 16, None) == -2
+
+
+def test_reserve_argument_errors(lib):
+    assert lib.moe_fp8_block_reserve(16, 0, 2048, 512, 128, None) == -9
+    assert lib.moe_fp8_block_reserve(16, 8, 2000, 512, 128, None) == -9
