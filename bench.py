@@ -72,7 +72,7 @@ class Clocks:
     def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
@@ -247,7 +247,10 @@ def run_ours(args, world, rank, local):
     def fwd(T):
         api.forward_problem(probs[T], out=outs[T], stream=s, force_path="decode")
 
-    # warm-up (also compiles nothing: the library is prebuilt)
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    # warm-up
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
             for T in DECODE_TS:
@@ -261,12 +264,10 @@ def run_ours(args, world, rank, local):
         launches_per_step += api.moe_fp8_block_last_launches()
     s.synchronize()
 
-    clocks = Clocks(local)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t_wall = time.perf_counter()
     with torch.cuda.stream(s):
         for k in range(args.steps):
@@ -288,8 +289,8 @@ def run_ours(args, world, rank, local):
     tok_s = allreduce_sum(step_tokens * args.steps, world) / (dev_ms_max / 1e3)
 
     # dominant kernel (decode GEMM1) timed with CUDA events between the stages
-    g1_ms = gemm1_durations(probs, s, flush, args.steps)
-    D16, _ = info[16]
+    st_ms = stage_durations(probs, s, flush, args.steps)
+    g1_ms = {T: st_ms[T][1] for T in DECODE_TS}
     g1_bytes = {T: info[T][0] * (2 * SHAPE.I * SHAPE.H + 2 * (2 * SHAPE.I // 128) * (SHAPE.H // 128))
                 + T * SHAPE.H * 2 + T * SHAPE.k * SHAPE.I * 4 for T in DECODE_TS}
     g1_achieved = sum(g1_bytes.values()) / (sum(g1_ms.values()) / 1e3) / 1e9
@@ -317,6 +318,8 @@ def run_ours(args, world, rank, local):
                            "us": 1e3 * statistics.median(per_T[T]),
                            "GB_s": info[T][1] / (statistics.median(per_T[T]) / 1e3) / 1e9}
                   for T in DECODE_TS},
+        "stage_us": {str(T): {n: round(1e3 * v, 2) for n, v in zip(("prep", "gemm1", "gemm2", "combine"), st_ms[T])}
+                     for T in DECODE_TS},
         "roofline": {"kernel": "decode_gemm1", "bound": "hbm", "achieved": g1_achieved, "peak": hbm,
                      "unit": "GB/s", "frac": g1_achieved / hbm,
                      "traffic": profile_traffic("decode_gemm1_kernel", "decode_small_T16"),
@@ -330,25 +333,29 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def gemm1_durations(probs, s, flush, steps):
-    """Median device time of the decode GEMM1 kernel per T, from CUDA events
-    the library records between its kernels (stage-timing mode)."""
+def stage_durations(probs, s, flush, steps):
+    """Median device time of each kernel of the decode path per T, from CUDA
+    events the library records between its kernels (stage-timing mode:
+    moe_fp8_block_set_stage_events).  Returns {T: [prep, gemm1, gemm2, combine]} in ms."""
+    import ctypes
     from block_fp8_mixture_route_gb300 import _lib
     lib = _lib.load()
     res = {}
     for T in DECODE_TS:
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in evs:          # torch creates the event handle on first record
+            e.record(s)
+        s.synchronize()
+        arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
         times = []
         for _ in range(max(steps, 3)):
             with torch.cuda.stream(s):
                 flush.zero_()
-                import ctypes
-                arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
-                lib.moe_fp8_block_set_stage_events(arr, 5)
+                _lib.check(lib.moe_fp8_block_set_stage_events(arr, 5), "set_stage_events")
                 api.forward_problem(probs[T], stream=s, force_path="decode")
             s.synchronize()
-            times.append(evs[1].elapsed_time(evs[2]))
-        res[T] = statistics.median(times)
+            times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
+        res[T] = [statistics.median(t[i] for t in times) for i in range(4)]
     return res
 
 

@@ -3,23 +3,38 @@
 // At small token counts each token routes to only top_k experts, so the
 // layer is bound by reading the routed experts' weights (fp8-moe-gather
 // page, Problem).  This path reads only those experts (the gathered-expert
-// combine, same page, The fix), streams their e4m3 rows from HBM into
-// shared memory with bulk (TMA) copies through per-warp mbarrier rings,
-// widens e4m3 in registers (exact: FreeToken PR #662, PR body), applies each
-// bf16 block scale once per 128-wide K block to an fp32 partial sum, and
-// keeps h = silu(gate) * up in fp32 for the down projection ("the down
-// projection in fp32", fp8-moe-gather page, The fix).
+// combine, same page, The fix).  Their e4m3 rows are streamed from HBM into
+// shared memory with large bulk (TMA) copies of whole rows, widened in
+// registers (exact: FreeToken PR #662, PR body), and each bf16 block scale
+// is applied once per 128-wide K block to an fp32 partial sum; h =
+// silu(gate) * up stays fp32 for the down projection ("the down projection
+// in fp32", fp8-moe-gather page, The fix).
 //
 // Kernels, in stream order (chained with programmatic dependent launch):
 //   decode_prep    CTA 0: routing lists; CTAs 1..T: f16 copy of each token
 //                  scaled by a power of two 2^-s_t (max |x_t| in [2^14, 2^15))
-//   decode_gemm1   gate/up projection of every routed (expert, 8-row-pair)
-//                  unit with mma.sync m16n8k16 (f16 x f16 -> fp32), fused
-//                  silu(gate)*up epilogue -> h fp32 [S, I]
-//   decode_gemm2   down projection of every routed (expert, 16-row) unit on
-//                  CUDA cores (fp32 h, fp32 FMA), times the slot's top-k
-//                  weight -> ybuf fp32 [S, H]
+//   decode_gemm1   gate/up projection of every routed (expert, R-row-pair)
+//                  unit with mma.sync m16n8k16 (f16 x f16 -> fp32), the four
+//                  consumer warps splitting K; fused silu(gate)*up epilogue
+//                  -> h fp32 [S, I] in routed order
+//   decode_gemm2   down projection of every routed (expert, R2-row) unit
+//                  with mma.sync on a two-term f16 split of the fp32 h
+//                  (about 22 significant bits), times the slot's top-k
+//                  weight -> ybuf fp32 [S, H] in slot order
 //   decode_combine out[t] = sum_j ybuf[t*k + j] in j order -> bf16
+//
+// Work split: the units of all routed experts form one list; CTA c of G
+// takes the contiguous range [c*U/G, (c+1)*U/G), so every SM streams the
+// same number of weight bytes whatever the routing.  Within a CTA, units of
+// one expert share that expert's activation rows (x or h), loaded once per
+// (expert, pass of up to SPP slots).  Two groups of four consumer warps take
+// alternate units (one group's latency hides behind the other's work); the
+// four warps of a group split the unit's K blocks and one of them sums the
+// partials.
+//
+// Copy sizes: one SM's bulk-copy engine needs copies of several KiB to move
+// data near the HBM rate (small copies are dominated by a fixed cost per
+// copy), so every weight copy here is a block of whole rows of 8-32 KiB.
 #include "common.cuh"
 #include "kernels.h"
 #include "route_dev.cuh"
@@ -28,13 +43,34 @@
 
 namespace moe {
 
+// Launch-time configuration of the two streaming kernels (host computed).
+struct StreamCfg {
+  int R;        // rows (GEMM1: row pairs) per unit before halving for balance
+  int NS;       // ring stages
+  int SB;       // bytes per ring stage
+  int SPP;      // slots per pass
+  int XB;       // bytes of one activation buffer
+  int XP;       // activation row pitch in the buffer (bytes)
+  int HBB;      // bytes of one converted-h buffer (GEMM2)
+  int HP;       // converted-h row pitch (bytes)
+  int V;        // floats per lane in the cross-warp reduction
+  int red_off, abuf_off, hb_off, ring_off, smem;
+};
 
 struct DecodeArgs {
   LayerArgs a;
   RouteBufs rb;
   DecodeBufs db;
   uint32_t* status;
+  StreamCfg c1, c2;
 };
+
+constexpr int kMaxNS = 8;
+constexpr int kGroups = 2;             // consumer groups taking alternate units
+constexpr int kGW = 4;                 // warps per group (they split K)
+constexpr int kNWC = kGroups * kGW;    // consumer warps
+constexpr int kThreads = 32 * (kNWC + 1);
+constexpr int kSmemLimit = 232448;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
@@ -72,19 +108,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
   if (threadIdx.x == 0) p.db.xexp[t] = s;
 }
 
-// ------------------------------------------------------------ GEMM1 ----
-namespace g1 {
-constexpr int NWC = 4;           // consumer warps
-constexpr int NSW = 4;           // ring slots per consumer warp
-constexpr int KC = 512;          // K bytes per stage
-constexpr int PITCH = 576;       // smem row pitch (== 64 mod 128: conflict-free fragment loads)
-constexpr int ROWS = 16;         // 8 gate rows + the 8 matching up rows
-constexpr int STAGE = ROWS * PITCH;
-constexpr int SPP = 16;          // slots per pass (two n=8 groups)
-constexpr int THREADS = 32 * (NWC + 1);
-constexpr int SMEM = 1024 + NWC * NSW * STAGE;
-}  // namespace g1
-
+// ----------------------------------------------------- shared helpers ----
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -101,37 +125,147 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint4 ldg128(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+__device__ __forceinline__ float4 lds_f4(const void* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
   return v;
 }
 
-__device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ int4 ld_meta(const DecodeArgs& p, int d) { return __ldg(p.rb.meta + d); }
 
-// Unit u of GEMM1: routed expert d = u / (I/8), row pairs [i0, i0+8).
-struct G1Unit {
-  int e, i0, off, ne, passes;
-};
-
-__device__ __forceinline__ G1Unit g1_unit(const DecodeArgs& p, long u) {
-  const int tpe = p.a.I / 8;
-  G1Unit r;
-  const int d = (int)(u / tpe);
-  r.i0 = (int)(u % tpe) * 8;
-  r.e = p.rb.glist[d];
-  r.off = p.rb.offsets[r.e];
-  r.ne = p.rb.offsets[r.e + 1] - r.off;
-  r.passes = (r.ne + g1::SPP - 1) / g1::SPP;
-  return r;
+// Bounded wait by lane 0 of a warp; the verdict is returned on all lanes.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// The A fragment words of one 64-wide K chunk (rows g and g+8) for the four
-// k16 MMAs.  Physical byte 16c + 4m + v of the chunk plays logical k
-// {2c, 2c+1, 2c+8, 2c+9}[v] of MMA m; the B fragment uses the same map.
-__device__ __forceinline__ void g1_afrag(const uint4& wa, const uint4& wb, uint32_t (&A)[4][4]) {
+// Shared-memory layout common to both streaming kernels.
+struct Smem {
+  uint64_t* full;     // [kMaxNS] ring stage landed (tx)
+  uint64_t* empty;    // [kMaxNS] ring stage consumed (kGW arrivals: the consuming group)
+  uint64_t* afull;    // [2] activation buffer landed (tx)
+  uint64_t* aempty;   // [2] activation buffer released (kNWC arrivals)
+  uint64_t* hbfull;   // [2] converted h written (kNWC arrivals)
+  uint64_t* hbfree;   // [2] converted h released (kNWC arrivals)
+  uint64_t* rfull;    // [kGroups][2] cross-warp partials written (kGW arrivals)
+  uint64_t* rempty;   // [kGroups][2] cross-warp partials read (1 arrival)
+  float* red;         // [kGroups][2][kGW][32][V]
+  uint8_t* abuf;
+  uint8_t* hb;
+  uint8_t* ring;      // [NS][SB]
+};
+
+__device__ __forceinline__ Smem smem_layout(uint8_t* base, const StreamCfg& c) {
+  Smem s;
+  uint64_t* b = reinterpret_cast<uint64_t*>(base);
+  s.full = b;
+  s.empty = b + kMaxNS;
+  s.afull = b + 2 * kMaxNS;
+  s.aempty = s.afull + 2;
+  s.hbfull = s.aempty + 2;
+  s.hbfree = s.hbfull + 2;
+  s.rfull = s.hbfree + 2;
+  s.rempty = s.rfull + 2 * kGroups;
+  s.red = reinterpret_cast<float*>(base + c.red_off);
+  s.abuf = base + c.abuf_off;
+  s.hb = base + c.hb_off;
+  s.ring = base + c.ring_off;
+  return s;
+}
+
+__device__ __forceinline__ void smem_init(const Smem& s, int NS) {
+  for (int i = 0; i < NS; ++i) {
+    mbar_init(&s.full[i], 1);
+    mbar_init(&s.empty[i], kGW);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&s.afull[i], 1);
+    mbar_init(&s.aempty[i], kNWC);
+    mbar_init(&s.hbfull[i], kNWC);
+    mbar_init(&s.hbfree[i], kNWC);
+  }
+  for (int i = 0; i < 2 * kGroups; ++i) {
+    mbar_init(&s.rfull[i], kGW);
+    mbar_init(&s.rempty[i], 1);
+  }
+  fence_mbar_init();
+}
+
+// The CTA's units, walked expert segment by expert segment and, within a
+// segment, pass by pass (a pass covers up to SPP of the expert's slots), so
+// that each (expert, pass) activation load is shared by all units of the
+// segment.  Producer and consumers walk the same sequence; ring stage m goes
+// to consumer group m % 2.
+struct Walk {
+  long u, ue;          // next segment start, range end
+  int upe;             // units per expert
+  int d, e, off, ne;   // current expert
+  long seg_b, seg_e;   // current segment [seg_b, seg_e)
+  int passes;
+};
+
+__device__ __forceinline__ bool walk_next_segment(const DecodeArgs& p, Walk& w, int SPP) {
+  if (w.u >= w.ue) return false;
+  w.d = (int)(w.u / w.upe);
+  w.seg_b = w.u;
+  w.seg_e = min(w.ue, (long)(w.d + 1) * w.upe);
+  const int4 m = ld_meta(p, w.d);
+  w.e = m.x;
+  w.off = m.y;
+  w.ne = m.z;
+  w.passes = (w.ne + SPP - 1) / SPP;
+  w.u = w.seg_e;
+  return true;
+}
+
+// Rows per unit after halving until every SM gets enough units to balance
+// (the count of routed experts D is only known on the device).
+__device__ __forceinline__ int balanced_rows(int R, int min_rows, int rows_total, int D, int G) {
+  while (R > min_rows && (long)D * (rows_total / R) < 6L * G) R >>= 1;
+  return R;
+}
+
+// Cross-warp sum of a group's K-split partials through shared memory.
+// Every warp of the group deposits V floats per lane; the group's first
+// warp (the leader) waits for all of them and returns the totals in tot.
+// Double-buffered by the group's unit parity; every wait is bounded.
+// Returns false on a timeout.
+template <int V>
+__device__ __forceinline__ bool group_reduce(const Smem& S, int gr, int wq, int lane, int ml, const float (&part)[V],
+                                             float (&tot)[V]) {
+  const int rb = ml & 1;
+  uint64_t* rf = &S.rfull[gr * 2 + rb];
+  uint64_t* re = &S.rempty[gr * 2 + rb];
+  if (ml >= 2 && !warp_wait(re, ((ml >> 1) - 1) & 1, lane)) return false;
+  float* dst = S.red + (((gr * 2 + rb) * kGW + wq) * 32 + lane) * V;
+#pragma unroll
+  for (int i = 0; i < V; ++i) dst[i] = part[i];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(rf);
+  if (wq != 0) return true;
+  if (!warp_wait(rf, (ml >> 1) & 1, lane)) return false;
+#pragma unroll
+  for (int i = 0; i < V; ++i) tot[i] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kGW; ++w) {
+    const float* src = S.red + (((gr * 2 + rb) * kGW + w) * 32 + lane) * V;
+#pragma unroll
+    for (int i = 0; i < V; ++i) tot[i] += src[i];
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(re);
+  return true;
+}
+
+// Widen one 64-wide K chunk of two weight rows (tile rows g and g+8) into
+// the A fragments of four m16n8k16 MMAs.  Physical element 16c + 4m + v of
+// the chunk (c = lane % 4) plays logical k {2c, 2c+1, 2c+8, 2c+9}[v] of MMA
+// m; the B fragment uses the same map, so the four MMAs together sum over
+// exactly the chunk's 64 elements.
+__device__ __forceinline__ void afrag(const uint4& wa, const uint4& wb, uint32_t (&A)[4][4]) {
   const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w};
   const uint32_t wb_[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
@@ -141,20 +275,40 @@ __device__ __forceinline__ void g1_afrag(const uint4& wa, const uint4& wb, uint3
   }
 }
 
-__global__ void __launch_bounds__(g1::THREADS, 1) decode_gemm1_kernel(DecodeArgs p) {
-  using namespace g1;
+// One 64-wide K chunk: four MMAs on two independent accumulators (shorter
+// dependency chains).
+__device__ __forceinline__ void chunk_mma(float (&b0)[4], float (&b1)[4], const uint4& wa, const uint4& wb,
+                                          const uint4& x0, const uint4& x1) {
+  uint32_t A[4][4];
+  afrag(wa, wb, A);
+  mma_f16_16816(b0, A[0], x0.x, x0.y);
+  mma_f16_16816(b1, A[1], x0.z, x0.w);
+  mma_f16_16816(b0, A[2], x1.x, x1.y);
+  mma_f16_16816(b1, A[3], x1.z, x1.w);
+}
+
+#define MOE_FAIL()                              \
+  do {                                          \
+    abort_flag = 1;                             \
+    raise_status(p.status, MOE_STATUS_TIMEOUT); \
+    return;                                     \
+  } while (0)
+
+// ------------------------------------------------------------ GEMM1 ----
+// Unit: routed expert e, row pairs [i0, i0+R) (R <= 8).  A ring stage holds
+// the R gate rows and the R up rows, whole (two contiguous bulk copies of
+// R*H bytes).  The m16 MMA tile takes gate rows as tile rows 0..R-1 and up
+// rows as tile rows 8..8+R-1, so each lane ends with gate and up of the same
+// row pair.  The four warps of a group split the unit's K blocks; the
+// group's leader sums the partials and applies silu(gate)*up.
+__global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + NWC * NSW;
-  uint8_t* ring = smem + 1024;
+  const StreamCfg& cfg = p.c1;
+  const Smem S = smem_layout(smem, cfg);
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NWC * NSW; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    fence_mbar_init();
+    smem_init(S, cfg.NS);
     abort_flag = 0;
   }
   __syncthreads();
@@ -163,255 +317,328 @@ __global__ void __launch_bounds__(g1::THREADS, 1) decode_gemm1_kernel(DecodeArgs
 
   const LayerArgs& a = p.a;
   const int D = *p.rb.nd;
-  const long U = (long)D * (a.I / 8);
-  const long ub = U * blockIdx.x / gridDim.x, ue = U * (blockIdx.x + 1) / gridDim.x;
-  const int nk = (a.H + KC - 1) / KC;
+  const int R = balanced_rows(cfg.R, 1, a.I, D, gridDim.x);
+  const int upe = a.I / R;
+  const long U = (long)D * upe;
+  Walk wk;
+  wk.u = U * blockIdx.x / gridDim.x;
+  wk.ue = U * (blockIdx.x + 1) / gridDim.x;
+  wk.upe = upe;
+  const int NS = cfg.NS, SPP = cfg.SPP;
+  const int rowb = R * a.H;   // bytes of R whole rows
 
-  if (warp == NWC) {
-    // ------------------------------------------------ producer (1 thread)
-    if (lane != 0) return;
-    const uint64_t pol = l2_policy_evict_first();
-    long cu[NWC];
-    int cpass[NWC], ckc[NWC], cm[NWC];
-    G1Unit cun[NWC];
-    int active = 0;
-    for (int w = 0; w < NWC; ++w) {
-      cu[w] = ub + w;
-      cpass[w] = 0;
-      ckc[w] = 0;
-      cm[w] = 0;
-      if (cu[w] < ue) {
-        cun[w] = g1_unit(p, cu[w]);
-        ++active;
-      } else {
-        cu[w] = -1;
-      }
-    }
+  if (warp == kNWC) {
+    // ------------------------------------------------ producer warp
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    int m = 0, gen = 0;
     bool ok = true;
-    while (active > 0 && ok) {
-      for (int w = 0; w < NWC && ok; ++w) {
-        if (cu[w] < 0) continue;
-        const int slot = cm[w] % NSW;
-        uint64_t* fb = &full[w * NSW + slot];
-        if (cm[w] >= NSW && !mbar_wait(&empty[w * NSW + slot], ((cm[w] / NSW) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const G1Unit& un = cun[w];
-        const int kc0 = ckc[w] * KC;
-        const int kcb = min(KC, a.H - kc0);
-        mbar_arrive_expect_tx(fb, ROWS * kcb);
-        uint8_t* dst = ring + (w * NSW + slot) * STAGE;
-        const uint8_t* base = a.w13 + (int64_t)un.e * 2 * a.I * a.H + kc0;
-#pragma unroll 1
-        for (int r = 0; r < ROWS; ++r) {
-          const int row = r < 8 ? un.i0 + r : a.I + un.i0 + (r - 8);
-          bulk_g2s(dst + r * PITCH, base + (int64_t)row * a.H, kcb, fb, pol);
-        }
-        ++cm[w];
-        if (++ckc[w] == nk) {
-          ckc[w] = 0;
-          if (++cpass[w] == un.passes) {
-            cpass[w] = 0;
-            cu[w] += NWC;
-            if (cu[w] >= ue) {
-              cu[w] = -1;
-              --active;
-            } else {
-              cun[w] = g1_unit(p, cu[w]);
-            }
+    while (ok && walk_next_segment(p, wk, SPP)) {
+      for (int pass = 0; pass < wk.passes && ok; ++pass, ++gen) {
+        const int nx = min(SPP, wk.ne - pass * SPP);
+        const int b = gen & 1;
+        // activation rows of this pass: lane j holds the token of slot j
+        const int tok = lane < nx ? p.rb.perm[wk.off + pass * SPP + lane] / a.k : 0;
+        if (gen >= 2) ok = warp_wait(&S.aempty[b], ((gen >> 1) - 1) & 1, lane);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&S.afull[b], nx * 2 * a.H);
+        __syncwarp();
+        if (lane < nx)
+          bulk_g2s(S.abuf + b * cfg.XB + lane * cfg.XP, p.db.xh + (int64_t)tok * a.H, 2 * a.H, &S.afull[b], pol_x);
+        for (long u = wk.seg_b; u < wk.seg_e && ok; ++u, ++m) {
+          const int slot = m % NS;
+          if (m >= NS) ok = warp_wait(&S.empty[slot], ((m / NS) - 1) & 1, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            const int i0 = (int)(u % upe) * R;
+            const uint8_t* gsrc = a.w13 + ((int64_t)wk.e * 2 * a.I + i0) * a.H;
+            mbar_arrive_expect_tx(&S.full[slot], 2 * rowb);
+            bulk_g2s(S.ring + slot * cfg.SB, gsrc, rowb, &S.full[slot], pol_w);
+            bulk_g2s(S.ring + slot * cfg.SB + rowb, gsrc + (int64_t)a.I * a.H, rowb, &S.full[slot], pol_w);
           }
+          __syncwarp();
         }
+        if (*(volatile int*)&abort_flag) ok = false;
       }
-      if (*(volatile int*)&abort_flag) ok = false;
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       abort_flag = 1;
       raise_status(p.status, MOE_STATUS_TIMEOUT);
       // let the copies already issued land before the CTA exits
-      for (int w = 0; w < NWC; ++w)
-        for (int m = max(0, cm[w] - NSW); m < cm[w]; ++m) mbar_wait(&full[w * NSW + (m % NSW)], (m / NSW) & 1);
+      for (int mm = max(0, m - NS); mm < m; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
+      for (int gg = max(0, gen - 1); gg <= gen; ++gg) mbar_wait(&S.afull[gg & 1], (gg >> 1) & 1);
     }
     return;
   }
 
   // -------------------------------------------------- consumer warps
+  const int gr = warp / kGW, wq = warp % kGW;
   const int g = lane >> 2, c = lane & 3;
-  const __half* xh = reinterpret_cast<const __half*>(p.db.xh);
-  int m = 0;
-  for (long u = ub + warp; u < ue; u += NWC) {
-    const G1Unit un = g1_unit(p, u);
-    const uint16_t* sg_row = a.w13s + (int64_t)un.e * a.s13_exp + (int64_t)(un.i0 / 128) * a.s13_row;
-    const uint16_t* su_row = a.w13s + (int64_t)un.e * a.s13_exp + (int64_t)((a.I + un.i0) / 128) * a.s13_row;
-    for (int pass = 0; pass < un.passes; ++pass) {
-      const int nsl = min(SPP, un.ne - pass * SPP);
-      const int ngrp = (nsl + 7) >> 3;
-      // B operand rows: slot (grp*8 + g) of this pass
-      const __half* xrow[2];
+  const int nkb = a.H >> 7;
+  const int kb0 = wq * nkb / kGW, kb1 = (wq + 1) * nkb / kGW;
+  const bool has_w = g < R;
+  int m = 0, gen = 0;
+  while (walk_next_segment(p, wk, SPP)) {
+    for (int pass = 0; pass < wk.passes; ++pass, ++gen) {
+      const int nx = min(SPP, wk.ne - pass * SPP);
+      const int b = gen & 1;
+      const bool has_x = g < nx;
+      const uint8_t* xrow = S.abuf + b * cfg.XB + g * cfg.XP + c * 32;
+      // epilogue data (group leaders): routed positions and token scales of slots 2c, 2c+1
+      const int pos0 = wk.off + pass * SPP + 2 * c;
+      int sx[2] = {0, 0};
+      if (wq == 0) {
 #pragma unroll
-      for (int gr = 0; gr < 2; ++gr) {
-        const int q = gr * 8 + g;
-        xrow[gr] = nullptr;
-        if (q < nsl) {
-          const int s = p.rb.perm[un.off + pass * SPP + q];
-          xrow[gr] = xh + (int64_t)(s / a.k) * a.H + c * 16;
-        }
+        for (int j = 0; j < 2; ++j)
+          if (2 * c + j < nx) sx[j] = p.db.xexp[p.rb.perm[pos0 + j] / a.k];
       }
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float blk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int kc = 0; kc < nk; ++kc) {
-        const int slot = m % NSW;
-        if (!mbar_wait(&full[warp * NSW + slot], (m / NSW) & 1)) {
-          abort_flag = 1;
-          raise_status(p.status, MOE_STATUS_TIMEOUT);
-          return;
-        }
-        const uint8_t* stage = ring + (warp * NSW + slot) * STAGE;
-        const int kc0 = kc * KC;
-        const int kcb = min(KC, a.H - kc0);
-#pragma unroll 2
-        for (int ch = 0; ch < kcb / 64; ++ch) {
-          const uint4 wa = lds128(stage + g * PITCH + ch * 64 + c * 16);
-          const uint4 wb = lds128(stage + (g + 8) * PITCH + ch * 64 + c * 16);
-          uint32_t A[4][4];
-          g1_afrag(wa, wb, A);
+      if (!warp_wait(&S.afull[b], (gen >> 1) & 1, lane)) MOE_FAIL();
+      for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
+        if ((m & 1) != gr) continue;   // the other group's unit
+        const int i0 = (int)(u % upe) * R;
+        // this warp's block scales of the unit: lane j holds K block kb0 + j
+        const uint16_t* sg_row = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)(i0 / 128) * a.s13_row;
+        const uint16_t* su_row = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)((a.I + i0) / 128) * a.s13_row;
+        const float sgl = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(sg_row + kb0 + lane)) : 0.f;
+        const float sul = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(su_row + kb0 + lane)) : 0.f;
+        const int slot = m % NS;
+        if (!warp_wait(&S.full[slot], (m / NS) & 1, lane)) MOE_FAIL();
+        const uint8_t* st = S.ring + slot * cfg.SB;
+        const uint8_t* arow = st + g * a.H + c * 16;
+        const uint8_t* brow = arow + rowb;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int kb = kb0; kb < kb1; ++kb) {
+          float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int gr = 0; gr < 2; ++gr) {
-            if (gr < ngrp) {
-              uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
-              if (xrow[gr]) {
-                x0 = ldg128(xrow[gr] + kc0 + ch * 64);
-                x1 = ldg128(xrow[gr] + kc0 + ch * 64 + 8);
-              }
-              const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-              for (int mm = 0; mm < 4; ++mm) mma_f16_16816(blk[gr], A[mm], xb[2 * mm], xb[2 * mm + 1]);
+          for (int ch = 0; ch < 2; ++ch) {
+            const int kk = kb * 128 + ch * 64;
+            uint4 wa = make_uint4(0, 0, 0, 0), wb = wa, x0 = wa, x1 = wa;
+            if (has_w) {
+              wa = lds128(arow + kk);
+              wb = lds128(brow + kk);
             }
-          }
-          if (ch & 1) {  // a 128-wide K block is complete: apply its scales once
-            const int kb = (kc0 + ch * 64) >> 7;
-            const float sg = bf16_bits_to_f32(__ldg(sg_row + kb));
-            const float su = bf16_bits_to_f32(__ldg(su_row + kb));
-#pragma unroll
-            for (int gr = 0; gr < 2; ++gr) {
-              acc[gr][0] = fmaf(sg, blk[gr][0], acc[gr][0]);
-              acc[gr][1] = fmaf(sg, blk[gr][1], acc[gr][1]);
-              acc[gr][2] = fmaf(su, blk[gr][2], acc[gr][2]);
-              acc[gr][3] = fmaf(su, blk[gr][3], acc[gr][3]);
-              blk[gr][0] = blk[gr][1] = blk[gr][2] = blk[gr][3] = 0.f;
+            if (has_x) {
+              x0 = lds128(xrow + 2 * kk);
+              x1 = lds128(xrow + 2 * kk + 16);
             }
+            chunk_mma(b0, b1, wa, wb, x0, x1);
           }
+          // the 128-wide K block is complete: apply its scales once
+          const float sg = __shfl_sync(0xffffffffu, sgl, kb - kb0);
+          const float su = __shfl_sync(0xffffffffu, sul, kb - kb0);
+          acc[0] = fmaf(sg, b0[0] + b1[0], acc[0]);
+          acc[1] = fmaf(sg, b0[1] + b1[1], acc[1]);
+          acc[2] = fmaf(su, b0[2] + b1[2], acc[2]);
+          acc[3] = fmaf(su, b0[3] + b1[3], acc[3]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[warp * NSW + slot]);
-        ++m;
-        if (*(volatile int*)&abort_flag) return;
-      }
-      // epilogue: lane holds gate/up of row pair i0+g for slots 2c, 2c+1
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        float tot[4];
+        if (!group_reduce<4>(S, gr, wq, lane, m >> 1, acc, tot)) MOE_FAIL();
+        if (wq == 0 && has_w) {
+          // lane: gate/up of row pair i0+g for slots 2c, 2c+1
 #pragma unroll
-      for (int gr = 0; gr < 2; ++gr) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int q = gr * 8 + 2 * c + j;
-          if (q < nsl) {
-            const int pos = un.off + pass * SPP + q;
-            const int s = p.rb.perm[pos];
-            const int sx = p.db.xexp[s / a.k];
-            const float gv = ldexpf(acc[gr][j], sx);
-            const float uv = ldexpf(acc[gr][2 + j], sx);
-            p.db.h[(int64_t)pos * a.I + un.i0 + g] = gv / (1.0f + expf(-gv)) * uv;
+          for (int j = 0; j < 2; ++j) {
+            if (2 * c + j < nx) {
+              const float gv = ldexpf(tot[j], sx[j]);
+              const float uv = ldexpf(tot[2 + j], sx[j]);
+              p.db.h[(int64_t)(pos0 + j) * a.I + i0 + g] = gv / (1.0f + expf(-gv)) * uv;
+            }
           }
         }
+        if (*(volatile int*)&abort_flag) return;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.aempty[b]);
     }
   }
 }
 
 // ------------------------------------------------------------ GEMM2 ----
-namespace g2 {
-constexpr int NWC = 4;
-constexpr int NSW = 4;
-constexpr int KC = 512;
-constexpr int ROWS = 16;
-constexpr int STAGE = ROWS * KC;
-constexpr int SPP = 4;           // slots per pass
-constexpr int THREADS = 32 * (NWC + 1);
-constexpr int SMEM = 1024 + NWC * NSW * STAGE;
-}  // namespace g2
-
-struct G2Unit {
-  int e, n0, off, ne, passes;
-};
-
-__device__ __forceinline__ G2Unit g2_unit(const DecodeArgs& p, long u) {
-  const int tpe = p.a.H / 16;
-  G2Unit r;
-  const int d = (int)(u / tpe);
-  r.n0 = (int)(u % tpe) * 16;
-  r.e = p.rb.glist[d];
-  r.off = p.rb.offsets[r.e];
-  r.ne = p.rb.offsets[r.e + 1] - r.off;
-  r.passes = (r.ne + g2::SPP - 1) / g2::SPP;
-  return r;
-}
-
-// Sum each of the 64 per-lane values over the warp; afterwards lane L holds
-// the totals of values 2L and 2L+1 in v[0], v[1].
-__device__ __forceinline__ void warp_transpose_reduce64(float (&v)[64], int lane) {
+// Unit: routed expert e, output rows [n0, n0+R2) (R2 in {16, 32, 64}, so a
+// unit lies in one 128-row scale block); MT = R2/16 m16 tiles.  A ring stage
+// holds the R2 whole rows (one contiguous copy of R2*I bytes).
+//
+// The pass's fp32 h rows (up to 4 slots, consecutive in routed order) land
+// in a raw buffer; the consumers turn each slot's row into two f16 terms
+// with a per-slot power-of-two scale 2^-s (max |h| * 2^-s in [2^14, 2^15)):
+// hi = f16(h * 2^-s), lo = f16(h * 2^-s - hi), which together carry about
+// 22 significant bits.  They form the eight MMA columns [hi_0..hi_3,
+// lo_0..lo_3]; y_slot = (C[:, slot] + C[:, 4 + slot]) * 2^s.  The four warps
+// of a group split K; the leader sums the partials and writes y times the
+// slot's top-k weight.
+template <int MT>
+__device__ void gemm2_unit_compute(const uint8_t* st, const uint8_t* hbrow, int I, int kb0, int kb1, int lane,
+                                   bool has_b, float sl, float (&acc)[MT][4]) {
+  const int g = lane >> 2, c = lane & 3;
 #pragma unroll
-  for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
-    const bool up = (lane & o) != 0;
+  for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll 1
+  for (int kb = kb0; kb < kb1; ++kb) {
+    float b0[MT][4], b1[MT][4];
 #pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = up ? v[i] : v[i + n / 2];
-      const float keep = up ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-}
-
-template <int NS>
-__device__ __forceinline__ void g2_stage_rows(const uint8_t* stage, int kcb, int lane, const float (&hv)[4][16],
-                                              float sc, float (&acc)[64]) {
+    for (int t = 0; t < MT; ++t)
 #pragma unroll
-  for (int r = 0; r < g2::ROWS; ++r) {
-    const uint4 w = lds128(stage + r * kcb + lane * 16);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    float part[NS];
+      for (int i = 0; i < 4; ++i) b0[t][i] = b1[t][i] = 0.f;
 #pragma unroll
-    for (int j = 0; j < NS; ++j) part[j] = 0.f;
+    for (int ch = 0; ch < 2; ++ch) {
+      const int kk = kb * 128 + ch * 64;
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+      if (has_b) {
+        x0 = lds128(hbrow + 2 * kk);
+        x1 = lds128(hbrow + 2 * kk + 16);
+      }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t lo, hi;
-      e4m3x4_to_f16x4(ww[q], lo, hi);
-      const float2 f0 = f16x2_to_f32x2(lo), f1 = f16x2_to_f32x2(hi);
-#pragma unroll
-      for (int j = 0; j < NS; ++j) {
-        part[j] = fmaf(f0.x, hv[j][4 * q + 0], part[j]);
-        part[j] = fmaf(f0.y, hv[j][4 * q + 1], part[j]);
-        part[j] = fmaf(f1.x, hv[j][4 * q + 2], part[j]);
-        part[j] = fmaf(f1.y, hv[j][4 * q + 3], part[j]);
+      for (int t = 0; t < MT; ++t) {
+        const uint8_t* ra = st + (t * 16 + g) * I + kk + c * 16;
+        const uint4 wa = lds128(ra);
+        const uint4 wb = lds128(ra + 8 * I);
+        chunk_mma(b0[t], b1[t], wa, wb, x0, x1);
       }
     }
+    const float s = __shfl_sync(0xffffffffu, sl, kb - kb0);
 #pragma unroll
-    for (int j = 0; j < NS; ++j) acc[r * 4 + j] = fmaf(part[j], sc, acc[r * 4 + j]);
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[t][i] = fmaf(s, b0[t][i] + b1[t][i], acc[t][i]);
   }
 }
 
-__global__ void __launch_bounds__(g2::THREADS, 1) decode_gemm2_kernel(DecodeArgs p) {
-  using namespace g2;
+template <int MT>
+__device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, int R2, int upe, int warp, int lane,
+                                int* abort_flag) {
+  const LayerArgs& a = p.a;
+  const StreamCfg& cfg = p.c2;
+  const int NS = cfg.NS, SPP = cfg.SPP;
+  const int gr = warp / kGW, wq = warp % kGW;
+  const int g = lane >> 2, c = lane & 3;
+  const int nkb = a.I >> 7;
+  const int kb0 = wq * nkb / kGW, kb1 = (wq + 1) * nkb / kGW;
+  // this warp's share of the h conversion
+  const int ck0 = warp * a.I / kNWC, ck1 = (warp + 1) * a.I / kNWC;
+  int m = 0, gen = 0;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_status(p.status, MOE_STATUS_TIMEOUT);
+  };
+  while (walk_next_segment(p, wk, SPP)) {
+    for (int pass = 0; pass < wk.passes; ++pass, ++gen) {
+      const int nh = min(SPP, wk.ne - pass * SPP);
+      const int b = gen & 1;
+      uint8_t* hb = S.hb + b * cfg.HBB;
+      const uint8_t* hraw = S.abuf;
+      // epilogue data (group leaders): slots 2c, 2c+1 (lanes with c < 2)
+      int so[2] = {-1, -1};
+      float wo[2] = {0.f, 0.f};
+      if (wq == 0 && c < 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (2 * c + j < nh) {
+            so[j] = p.rb.perm[wk.off + pass * SPP + 2 * c + j];
+            wo[j] = a.wts[so[j]];
+          }
+        }
+      }
+      if (!warp_wait(&S.afull[0], gen & 1, lane)) return fail();
+      // per-slot scale exponents from the row maxima (every warp computes them)
+      int es[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if (s < nh) {
+          float mx = 0.f;
+          for (int k = lane * 4; k < a.I; k += 128) {
+            const float4 v = lds_f4(hraw + (s * a.I + k) * 4);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (mx > 0.f) {
+            int ex;
+            frexpf(mx, &ex);
+            es[s] = (ex - 1) - 14;
+          }
+        }
+      }
+      if (gen >= 2 && !warp_wait(&S.hbfree[b], ((gen >> 1) - 1) & 1, lane)) return fail();
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if (s >= nh) break;
+        for (int k = ck0 + 2 * lane; k < ck1; k += 64) {
+          const float2 v = *reinterpret_cast<const float2*>(hraw + (s * a.I + k) * 4);
+          const float v0 = ldexpf(v.x, -es[s]), v1 = ldexpf(v.y, -es[s]);
+          const __half2 hi = __floats2half2_rn(v0, v1);
+          const float2 hf = __half22float2(hi);
+          const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+          *reinterpret_cast<__half2*>(hb + s * cfg.HP + 2 * k) = hi;
+          *reinterpret_cast<__half2*>(hb + (4 + s) * cfg.HP + 2 * k) = lo;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.aempty[0]);
+        mbar_arrive(&S.hbfull[b]);
+      }
+      if (!warp_wait(&S.hbfull[b], (gen >> 1) & 1, lane)) return fail();
+      const bool has_b = (g & 3) < nh;
+      const uint8_t* hbrow = hb + g * cfg.HP + c * 32;
+      int esl[2] = {0, 0};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int s = (2 * c + j) & 3;
+        esl[j] = s == 0 ? es[0] : (s == 1 ? es[1] : (s == 2 ? es[2] : es[3]));
+      }
+      for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
+        if ((m & 1) != gr) continue;
+        const int n0 = (int)(u % upe) * R2;
+        const uint16_t* srow = a.w2s + (int64_t)wk.e * a.s2_exp + (int64_t)(n0 / 128) * a.s2_row;
+        const float sl = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(srow + kb0 + lane)) : 0.f;
+        const int slot = m % NS;
+        if (!warp_wait(&S.full[slot], (m / NS) & 1, lane)) return fail();
+        float acc[MT][4];
+        gemm2_unit_compute<MT>(S.ring + slot * cfg.SB, hbrow, a.I, kb0, kb1, lane, has_b, sl, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        float part[MT * 4], tot[MT * 4];
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) part[t * 4 + i] = acc[t][i];
+        if (!group_reduce<MT * 4>(S, gr, wq, lane, m >> 1, part, tot)) return fail();
+        if (wq == 0) {
+          // columns 2c, 2c+1: hi terms on lanes c < 2, lo terms on lanes c >= 2
+#pragma unroll
+          for (int i = 0; i < MT * 4; ++i) tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], 2);
+          if (c < 2) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                if (so[j] >= 0) {
+                  const int n = n0 + t * 16 + g;
+                  p.db.ybuf[(int64_t)so[j] * a.H + n] = ldexpf(tot[t * 4 + j], esl[j]) * wo[j];
+                  p.db.ybuf[(int64_t)so[j] * a.H + n + 8] = ldexpf(tot[t * 4 + 2 + j], esl[j]) * wo[j];
+                }
+              }
+            }
+          }
+        }
+        if (*(volatile int*)abort_flag) return;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.hbfree[b]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + NWC * NSW;
-  uint8_t* ring = smem + 1024;
+  const StreamCfg& cfg = p.c2;
+  const Smem S = smem_layout(smem, cfg);
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NWC * NSW; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    fence_mbar_init();
+    smem_init(S, cfg.NS);
     abort_flag = 0;
   }
   __syncthreads();
@@ -420,139 +647,59 @@ __global__ void __launch_bounds__(g2::THREADS, 1) decode_gemm2_kernel(DecodeArgs
 
   const LayerArgs& a = p.a;
   const int D = *p.rb.nd;
-  const long U = (long)D * (a.H / 16);
-  const long ub = U * blockIdx.x / gridDim.x, ue = U * (blockIdx.x + 1) / gridDim.x;
-  const int nk = (a.I + KC - 1) / KC;
+  const int R2 = balanced_rows(cfg.R, 16, a.H, D, gridDim.x);
+  const int upe = a.H / R2;
+  const long U = (long)D * upe;
+  Walk wk;
+  wk.u = U * blockIdx.x / gridDim.x;
+  wk.ue = U * (blockIdx.x + 1) / gridDim.x;
+  wk.upe = upe;
+  const int NS = cfg.NS, SPP = cfg.SPP;
+  const int tileb = R2 * a.I;
 
-  if (warp == NWC) {
-    if (lane != 0) return;
-    const uint64_t pol = l2_policy_evict_first();
-    long cu[NWC];
-    int cpass[NWC], ckc[NWC], cm[NWC];
-    G2Unit cun[NWC];
-    int active = 0;
-    for (int w = 0; w < NWC; ++w) {
-      cu[w] = ub + w;
-      cpass[w] = ckc[w] = cm[w] = 0;
-      if (cu[w] < ue) {
-        cun[w] = g2_unit(p, cu[w]);
-        ++active;
-      } else {
-        cu[w] = -1;
-      }
-    }
+  if (warp == kNWC) {
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_h = l2_policy_evict_last();
+    int m = 0, gen = 0;
     bool ok = true;
-    while (active > 0 && ok) {
-      for (int w = 0; w < NWC && ok; ++w) {
-        if (cu[w] < 0) continue;
-        const int slot = cm[w] % NSW;
-        uint64_t* fb = &full[w * NSW + slot];
-        if (cm[w] >= NSW && !mbar_wait(&empty[w * NSW + slot], ((cm[w] / NSW) - 1) & 1)) {
-          ok = false;
-          break;
+    while (ok && walk_next_segment(p, wk, SPP)) {
+      for (int pass = 0; pass < wk.passes && ok; ++pass, ++gen) {
+        const int nh = min(SPP, wk.ne - pass * SPP);
+        // the raw h buffer is single: wait until every consumer has converted the previous pass
+        if (gen >= 1) ok = warp_wait(&S.aempty[0], (gen - 1) & 1, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          // the pass's h rows are consecutive in routed order: one copy
+          mbar_arrive_expect_tx(&S.afull[0], nh * 4 * a.I);
+          bulk_g2s(S.abuf, p.db.h + (int64_t)(wk.off + pass * SPP) * a.I, nh * 4 * a.I, &S.afull[0], pol_h);
         }
-        const G2Unit& un = cun[w];
-        const int kc0 = ckc[w] * KC;
-        const int kcb = min(KC, a.I - kc0);
-        mbar_arrive_expect_tx(fb, ROWS * kcb);
-        uint8_t* dst = ring + (w * NSW + slot) * STAGE;
-        const uint8_t* src = a.w2 + ((int64_t)un.e * a.H + un.n0) * a.I + kc0;
-        if (kcb == a.I) {
-          bulk_g2s(dst, src, ROWS * kcb, fb, pol);   // whole rows: one contiguous tile
-        } else {
-#pragma unroll 1
-          for (int r = 0; r < ROWS; ++r) bulk_g2s(dst + r * kcb, src + (int64_t)r * a.I, kcb, fb, pol);
-        }
-        ++cm[w];
-        if (++ckc[w] == nk) {
-          ckc[w] = 0;
-          if (++cpass[w] == un.passes) {
-            cpass[w] = 0;
-            cu[w] += NWC;
-            if (cu[w] >= ue) {
-              cu[w] = -1;
-              --active;
-            } else {
-              cun[w] = g2_unit(p, cu[w]);
-            }
+        __syncwarp();
+        for (long u = wk.seg_b; u < wk.seg_e && ok; ++u, ++m) {
+          const int slot = m % NS;
+          if (m >= NS) ok = warp_wait(&S.empty[slot], ((m / NS) - 1) & 1, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            const int n0 = (int)(u % upe) * R2;
+            mbar_arrive_expect_tx(&S.full[slot], tileb);
+            bulk_g2s(S.ring + slot * cfg.SB, a.w2 + ((int64_t)wk.e * a.H + n0) * a.I, tileb, &S.full[slot], pol_w);
           }
+          __syncwarp();
         }
+        if (*(volatile int*)&abort_flag) ok = false;
       }
-      if (*(volatile int*)&abort_flag) ok = false;
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       abort_flag = 1;
       raise_status(p.status, MOE_STATUS_TIMEOUT);
-      for (int w = 0; w < NWC; ++w)
-        for (int m = max(0, cm[w] - NSW); m < cm[w]; ++m) mbar_wait(&full[w * NSW + (m % NSW)], (m / NSW) & 1);
+      for (int mm = max(0, m - NS); mm < m; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
+      if (gen > 0) mbar_wait(&S.afull[0], (gen - 1) & 1);
     }
     return;
   }
-
-  int m = 0;
-  for (long u = ub + warp; u < ue; u += NWC) {
-    const G2Unit un = g2_unit(p, u);
-    const uint16_t* srow = a.w2s + (int64_t)un.e * a.s2_exp + (int64_t)(un.n0 / 128) * a.s2_row;
-    for (int pass = 0; pass < un.passes; ++pass) {
-      const int nsl = min(SPP, un.ne - pass * SPP);
-      float acc[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-      for (int kc = 0; kc < nk; ++kc) {
-        const int slot = m % NSW;
-        if (!mbar_wait(&full[warp * NSW + slot], (m / NSW) & 1)) {
-          abort_flag = 1;
-          raise_status(p.status, MOE_STATUS_TIMEOUT);
-          return;
-        }
-        const uint8_t* stage = ring + (warp * NSW + slot) * STAGE;
-        const int kc0 = kc * KC;
-        const int kcb = min(KC, a.I - kc0);
-        if (lane * 16 < kcb) {
-          const int kpos = kc0 + lane * 16;
-          float hv[4][16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j < nsl) {
-              const float* hp = p.db.h + (int64_t)(un.off + pass * SPP + j) * a.I + kpos;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 f = ldg_f4(hp + 4 * q);
-                hv[j][4 * q + 0] = f.x;
-                hv[j][4 * q + 1] = f.y;
-                hv[j][4 * q + 2] = f.z;
-                hv[j][4 * q + 3] = f.w;
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 16; ++q) hv[j][q] = 0.f;
-            }
-          }
-          const float sc = bf16_bits_to_f32(__ldg(srow + (kpos >> 7)));
-          switch (nsl) {
-            case 1: g2_stage_rows<1>(stage, kcb, lane, hv, sc, acc); break;
-            case 2: g2_stage_rows<2>(stage, kcb, lane, hv, sc, acc); break;
-            case 3: g2_stage_rows<3>(stage, kcb, lane, hv, sc, acc); break;
-            default: g2_stage_rows<4>(stage, kcb, lane, hv, sc, acc); break;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[warp * NSW + slot]);
-        ++m;
-        if (*(volatile int*)&abort_flag) return;
-      }
-      warp_transpose_reduce64(acc, lane);
-      // lane L: row L/2, slots 2*(L&1) + {0,1}
-      const int r = lane >> 1;
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int j = 2 * (lane & 1) + i;
-        if (j < nsl) {
-          const int s = p.rb.perm[un.off + pass * SPP + j];
-          p.db.ybuf[(int64_t)s * a.H + un.n0 + r] = acc[i] * a.wts[s];
-        }
-      }
-    }
+  switch (R2 / 16) {
+    case 1: gemm2_consumers<1>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+    case 2: gemm2_consumers<2>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+    default: gemm2_consumers<4>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
   }
 }
 
@@ -600,27 +747,82 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
+static inline int align128(int x) { return (x + 127) / 128 * 128; }
+
+// Place the regions of one streaming kernel: barriers, reduction area,
+// activation buffer(s), converted-h buffers, ring.
+static bool place(StreamCfg& c, int nabuf) {
+  c.red_off = 1024;
+  c.abuf_off = align128(c.red_off + kGroups * 2 * kGW * 32 * c.V * 4);
+  c.hb_off = c.abuf_off + nabuf * c.XB;
+  c.ring_off = c.hb_off + 2 * c.HBB;
+  c.smem = c.ring_off + c.NS * c.SB;
+  return c.smem <= kSmemLimit;
+}
+
+// GEMM1: R row pairs per unit with R*H <= 16 KiB (whole-row copies of 8-16
+// KiB keep the per-SM bulk-copy engine near its peak); as many ring stages
+// as fit next to two activation buffers of up to 8 slots.
+static bool config_gemm1(int H, StreamCfg& c) {
+  c.R = H <= 2048 ? 8 : (H <= 4096 ? 4 : 2);
+  c.SB = align128(2 * c.R * H);
+  c.XP = 2 * H + 16;          // == 16 mod 128: conflict-free B fragment loads
+  c.HBB = 0;
+  c.HP = 0;
+  c.V = 4;
+  for (int spp = 8; spp >= 1; --spp) {
+    c.SPP = spp;
+    c.XB = align128(spp * c.XP);
+    for (c.NS = kMaxNS; c.NS >= 3; --c.NS)
+      if (place(c, 2) && (c.NS >= 4 || spp <= 4)) return true;
+  }
+  return false;
+}
+
+// GEMM2: R2 rows per unit (16, 32 or 64) with R2*I near 16 KiB; a raw h
+// buffer for 4 slots and two converted buffers of 8 f16 rows.
+static bool config_gemm2(int H, int I, StreamCfg& c) {
+  c.R = 16;
+  while (c.R < 64 && 2 * c.R * I <= 16384 && 2 * c.R <= H) c.R *= 2;
+  c.SB = align128(c.R * I);
+  c.V = 4 * (c.R / 16);
+  c.XP = 4 * I;
+  c.HP = 2 * I + 16;          // == 16 mod 128: conflict-free B fragment loads
+  c.HBB = align128(8 * c.HP);
+  c.SPP = 4;
+  c.XB = align128(c.SPP * c.XP);
+  for (c.NS = kMaxNS; c.NS >= 2; --c.NS)
+    if (place(c, 1)) return true;
+  return false;
+}
+
+bool decode_supported(int H, int I) {
+  StreamCfg c1, c2;
+  return H % 128 == 0 && I % 128 == 0 && config_gemm1(H, c1) && config_gemm2(H, I, c2);
+}
+
 cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeBufs& db, uint32_t* status,
                           int device, cudaStream_t st, int* launches) {
-  DecodeArgs p{a, rb, db, status};
+  DecodeArgs p{a, rb, db, status, {}, {}};
+  if (!config_gemm1(a.H, p.c1) || !config_gemm2(a.H, a.I, p.c2)) return cudaErrorNotSupported;
   const int sms = num_sms(device);
   cudaError_t err;
   const int nt = route_threads(a.E);
   const size_t rsm = route_smem_bytes(a.E, nt);
   if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm)))
     return err;
-  if ((err = cudaFuncSetAttribute(decode_gemm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g1::SMEM)))
+  if ((err = cudaFuncSetAttribute(decode_gemm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c1.smem)))
     return err;
-  if ((err = cudaFuncSetAttribute(decode_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g2::SMEM)))
+  if ((err = cudaFuncSetAttribute(decode_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c2.smem)))
     return err;
   // prep: route (CTA 0) + f16 activations (CTAs 1..T)
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
   if ((err = launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(nt), rsm, st, false, p))) return err;
   stage_mark(st, 1);
-  if ((err = launch_pdl(decode_gemm1_kernel, dim3(sms), dim3(g1::THREADS), g1::SMEM, st, pdl, p))) return err;
+  if ((err = launch_pdl(decode_gemm1_kernel, dim3(sms), dim3(kThreads), p.c1.smem, st, pdl, p))) return err;
   stage_mark(st, 2);
-  if ((err = launch_pdl(decode_gemm2_kernel, dim3(sms), dim3(g2::THREADS), g2::SMEM, st, pdl, p))) return err;
+  if ((err = launch_pdl(decode_gemm2_kernel, dim3(sms), dim3(kThreads), p.c2.smem, st, pdl, p))) return err;
   stage_mark(st, 3);
   if ((err = launch_pdl(decode_combine_kernel, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, pdl, p)))
     return err;

@@ -32,7 +32,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Byte layout of one workspace.
 struct Layout {
-  size_t status, counts, offsets, perm, inv, glist, nd;
+  size_t status, counts, offsets, perm, inv, glist, nd, meta;
   size_t xh, xexp, h, ybuf;                       // decode
   size_t xq, xs, hq, hs, slots, tiles, ntiles;    // prefill
   size_t hid, tids, twts, outb;                   // host-io staging
@@ -56,6 +56,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   L.inv = take(4 * (size_t)S);
   L.glist = take(4 * (size_t)(g > 0 ? g : 1));
   L.nd = take(16);
+  L.meta = take(16 * (size_t)(g > 0 ? g : 1));
   if (path == MOE_PATH_DECODE) {
     L.xh = take(2 * (size_t)(T * H));
     L.xexp = take(4 * (size_t)T);
@@ -204,7 +205,8 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
   const int64_t I = I2 / 2;
   if (H <= 0 || I <= 0 || H % 128 != 0 || I % 128 != 0) return MOE_ERR_SHAPE;
   if (w2->shape[0] != E || w2->shape[1] != H || w2->shape[2] != I) return MOE_ERR_SHAPE;
-  if (H > (1 << 20) || I > (1 << 20) || T > (1 << 24) / k) return MOE_ERR_ARG;
+  if (H > 8192 || I > 8192) return MOE_ERR_SHAPE;
+  if (T > (1 << 24) / k) return MOE_ERR_ARG;
   if ((rc = check_scale_bank(w13_scale, E, 2 * I / 128, H / 128, w13_scale_stride))) return rc;
   if ((rc = check_scale_bank(w2_scale, E, H / 128, I / 128, w2_scale_stride))) return rc;
   if (!contiguous(w13) || !contiguous(w2)) return MOE_ERR_STRIDE;
@@ -281,6 +283,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
   rb.inv = reinterpret_cast<int32_t*>(w + L.inv);
   rb.glist = reinterpret_cast<int32_t*>(w + L.glist);
   rb.nd = reinterpret_cast<int32_t*>(w + L.nd);
+  rb.meta = reinterpret_cast<int4*>(w + L.meta);
   (void)hostio;
   int path = force;
   if (path == MOE_PATH_NONE)
@@ -321,7 +324,8 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
 
 int choose_path(const LayerArgs& a, float ratio, int force) {
   if (force != MOE_PATH_NONE) return force;
-  return ((double)a.T * a.k <= (double)a.E * ratio) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  const bool gathered = (double)a.T * a.k <= (double)a.E * ratio;
+  return gathered && decode_supported(a.H, a.I) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
 int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
@@ -344,6 +348,7 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LayerArgs a = c.a;
   const int path = choose_path(a, ratio, force);
+  if (path == MOE_PATH_DECODE && !decode_supported(a.H, a.I)) return MOE_ERR_SHAPE;
   const Layout L = make_layout(c.T, a.k, a.H, a.I, a.E, path, hostio);
   void* ws = nullptr;
   if ((rc = get_workspace(st, L.total, &ws))) return rc;
@@ -447,7 +452,7 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   if ((rc = get_workspace(st, 16, &ws))) return rc;
-  RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct};
+  RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr};
   if (launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb, static_cast<uint32_t*>(ws), st) !=
       cudaSuccess) {
     cudaGetLastError();

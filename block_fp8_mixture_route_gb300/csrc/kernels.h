@@ -32,6 +32,8 @@ struct RouteBufs {
   int32_t* inv;       // [S]
   int32_t* glist;     // [min(E,S)]
   int32_t* nd;        // [1]
+  int4* meta;         // [min(E,S)]: {expert, first routed position, slot count, 0} per distinct expert
+                      // (optional: may be null)
 };
 
 // Scratch of the decode path.
@@ -68,6 +70,9 @@ bool stage_mark(cudaStream_t st, int i);
 cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, uint32_t* status,
                          cudaStream_t st);
 cudaError_t launch_widen(const uint8_t* codes, int64_t n, float* out, cudaStream_t st);
+
+// Whether the decode path can stage rows of this layer shape in shared memory.
+bool decode_supported(int H, int I);
 
 // Decode (W8A16) path: prep (route + f16 activations), GEMM1+silu*up,
 // GEMM2, combine.  Adds the number of launches to *launches.

@@ -109,7 +109,10 @@ static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E
     rb.counts[e] = c;
     rb.offsets[e] = oc;
     eoff[e] = oc;
-    if (c > 0) rb.glist[od++] = e;
+    if (c > 0) {
+      if (rb.meta) rb.meta[od] = make_int4(e, oc, c, 0);
+      rb.glist[od++] = e;
+    }
     oc += c;
   }
   const int g = min(E, S);

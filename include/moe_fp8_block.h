@@ -131,7 +131,8 @@ typedef struct {
  *                with w2_scale_stride >= I/128.
  *  out           bf16 [T, H], contiguous; must not overlap any input.
  *  stream        cudaStream_t.
- * H and I must be multiples of 128; k in [1, 64]; E in [1, 4096].  Every
+ * H and I must be multiples of 128 and at most 8192; k in [1, 64];
+ * E in [1, 4096]; T*k <= 2^24.  Every
  * base pointer must be 16-byte aligned.  T == 0 is a no-op returning MOE_OK.
  */
 int moe_fp8_block_forward(const moe_tensor* hidden, const moe_tensor* topk_ids,
