@@ -29,7 +29,7 @@ EXPORTS = [
     "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_hostio",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
-    "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_error_string",
+    "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_last_error_detail", "moe_fp8_block_error_string",
     "moe_fp8_block_release",
 ]
 
@@ -55,7 +55,8 @@ class MoeOptions(ctypes.Structure):
 class MoeError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {ERRORS.get(code, code)} ({error_string(code)})")
+        detail = load().moe_fp8_block_last_error_detail().decode() if code == -8 else ""
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({error_string(code)}) {detail}".rstrip())
 
 
 _lib = None
@@ -87,6 +88,8 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_last_launches.argtypes = []
         lib.moe_fp8_block_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.moe_fp8_block_abi_version.argtypes = []
+        lib.moe_fp8_block_last_error_detail.argtypes = []
+        lib.moe_fp8_block_last_error_detail.restype = ctypes.c_char_p
         lib.moe_fp8_block_error_string.argtypes = [ctypes.c_int]
         lib.moe_fp8_block_error_string.restype = ctypes.c_char_p
         lib.moe_fp8_block_release.argtypes = []

@@ -818,13 +818,20 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   // prep: route (CTA 0) + f16 activations (CTAs 1..T)
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
-  if ((err = launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(nt), rsm, st, false, p))) return err;
+  if ((err = launch_check(launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(nt), rsm, st, false, p), st,
+                          "decode_prep")))
+    return err;
   stage_mark(st, 1);
-  if ((err = launch_pdl(decode_gemm1_kernel, dim3(sms), dim3(kThreads), p.c1.smem, st, pdl, p))) return err;
+  if ((err = launch_check(launch_pdl(decode_gemm1_kernel, dim3(sms), dim3(kThreads), p.c1.smem, st, pdl, p), st,
+                          "decode_gemm1")))
+    return err;
   stage_mark(st, 2);
-  if ((err = launch_pdl(decode_gemm2_kernel, dim3(sms), dim3(kThreads), p.c2.smem, st, pdl, p))) return err;
+  if ((err = launch_check(launch_pdl(decode_gemm2_kernel, dim3(sms), dim3(kThreads), p.c2.smem, st, pdl, p), st,
+                          "decode_gemm2")))
+    return err;
   stage_mark(st, 3);
-  if ((err = launch_pdl(decode_combine_kernel, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, pdl, p)))
+  if ((err = launch_check(launch_pdl(decode_combine_kernel, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, pdl, p),
+                          st, "decode_combine")))
     return err;
   stage_mark(st, 4);
   *launches += 4;

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -32,9 +34,9 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Byte layout of one workspace.
 struct Layout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta;
+  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp;
   size_t xh, xexp, h, ybuf;                       // decode
-  size_t xq, xs, hq, hs, slots, tiles, ntiles;    // prefill
+  size_t xq, xs, hq, hs, slots;                   // prefill
   size_t hid, tids, twts, outb;                   // host-io staging
   size_t total;
 };
@@ -57,20 +59,18 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   L.glist = take(4 * (size_t)(g > 0 ? g : 1));
   L.nd = take(16);
   L.meta = take(16 * (size_t)(g > 0 ? g : 1));
+  L.mtp = take(4 * (size_t)(E + 1));
   if (path == MOE_PATH_DECODE) {
     L.xh = take(2 * (size_t)(T * H));
     L.xexp = take(4 * (size_t)T);
     L.h = take(4 * (size_t)(S * I));
     L.ybuf = take(4 * (size_t)(S * H));
   } else if (path == MOE_PATH_PREFILL) {
-    L.xq = take((size_t)(T * H));
-    L.xs = take(4 * (size_t)(T * (H / 128)));
+    L.xq = take((size_t)(S * H));
+    L.xs = take(4 * (size_t)(S * (H / 128)));
     L.hq = take((size_t)(S * I));
     L.hs = take(4 * (size_t)(S * (I / 128)));
     L.slots = take(2 * (size_t)(S * H));
-    // tile list: at most ceil(S/128) + E tiles of 128 rows, 2 ints each
-    L.tiles = take(8 * (size_t)((S + 127) / 128 + E + 1));
-    L.ntiles = take(16);
   }
   if (hostio) {
     L.hid = take(2 * (size_t)(T * H));
@@ -284,6 +284,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
   rb.glist = reinterpret_cast<int32_t*>(w + L.glist);
   rb.nd = reinterpret_cast<int32_t*>(w + L.nd);
   rb.meta = reinterpret_cast<int4*>(w + L.meta);
+  rb.mtp = reinterpret_cast<int32_t*>(w + L.mtp);
   (void)hostio;
   int path = force;
   if (path == MOE_PATH_NONE)
@@ -304,8 +305,6 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     pb.hq = reinterpret_cast<uint8_t*>(w + L.hq);
     pb.hs = reinterpret_cast<float*>(w + L.hs);
     pb.slots = reinterpret_cast<uint16_t*>(w + L.slots);
-    pb.tiles = reinterpret_cast<int32_t*>(w + L.tiles);
-    pb.ntiles = reinterpret_cast<int32_t*>(w + L.ntiles);
     err = launch_prefill(a, rb, pb, status, dev, st, &launches);
   }
   if (err == cudaErrorNotSupported) {
@@ -382,6 +381,28 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
 
 }  // namespace
 
+static thread_local char g_err_detail[256] = "";
+
+cudaError_t note_error(cudaError_t e, const char* stage) {
+  if (e != cudaSuccess && e != cudaErrorNotSupported)
+    snprintf(g_err_detail, sizeof(g_err_detail), "%s: %s (%s)", stage, cudaGetErrorName(e), cudaGetErrorString(e));
+  return e;
+}
+
+static bool sync_check_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_FP8_BLOCK_SYNC_CHECK");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+cudaError_t launch_check(cudaError_t launch_err, cudaStream_t st, const char* stage) {
+  if (launch_err != cudaSuccess) return note_error(launch_err, stage);
+  if (sync_check_enabled()) return note_error(cudaStreamSynchronize(st), stage);
+  return cudaSuccess;
+}
+
 StageEvents& stage_events() {
   static thread_local StageEvents se;
   return se;
@@ -452,7 +473,7 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   if ((rc = get_workspace(st, 16, &ws))) return rc;
-  RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr};
+  RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr, nullptr};
   if (launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb, static_cast<uint32_t*>(ws), st) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -543,6 +564,8 @@ int moe_fp8_block_set_stage_events(void* const* events, int n) {
 }
 
 int moe_fp8_block_abi_version(void) { return MOE_FP8_BLOCK_ABI_VERSION; }
+
+const char* moe_fp8_block_last_error_detail(void) { return g_err_detail; }
 
 const char* moe_fp8_block_error_string(int code) {
   switch (code) {

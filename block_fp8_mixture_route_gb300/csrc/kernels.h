@@ -34,6 +34,7 @@ struct RouteBufs {
   int32_t* nd;        // [1]
   int4* meta;         // [min(E,S)]: {expert, first routed position, slot count, 0} per distinct expert
                       // (optional: may be null)
+  int32_t* mtp;       // [E+1]: exclusive prefix of ceil(count/128) per expert (optional)
 };
 
 // Scratch of the decode path.
@@ -44,15 +45,13 @@ struct DecodeBufs {
   float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
 };
 
-// Scratch of the prefill path.
+// Scratch of the prefill path (rows in routed order unless stated).
 struct PrefillBufs {
-  uint8_t* xq;        // e4m3 [T, H] activation codes
-  float* xs;          // [T, H/128] activation scales
-  uint8_t* hq;        // e4m3 [S, I] h codes, routed order
+  uint8_t* xq;        // e4m3 [S, H] activation codes of each routed slot's token
+  float* xs;          // [S, H/128] their scales
+  uint8_t* hq;        // e4m3 [S, I] h codes
   float* hs;          // [S, I/128] h scales
   uint16_t* slots;    // bf16 [S, H] per-slot outputs times top-k weight, slot order
-  int32_t* tiles;     // tile work list
-  int32_t* ntiles;    // [1]
 };
 
 int num_sms(int device);
@@ -66,6 +65,11 @@ StageEvents& stage_events();
 // Record stage event i on st if one was requested; returns true while stage
 // events are active (the launchers then drop programmatic dependent launch).
 bool stage_mark(cudaStream_t st, int i);
+
+// Record a CUDA failure for moe_fp8_block_last_error_detail; with
+// MOE_FP8_BLOCK_SYNC_CHECK=1 also synchronise and check after each launch.
+cudaError_t note_error(cudaError_t e, const char* stage);
+cudaError_t launch_check(cudaError_t launch_err, cudaStream_t st, const char* stage);
 
 cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, uint32_t* status,
                          cudaStream_t st);

@@ -101,13 +101,18 @@ static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E
     lc += eoff[e];
     ld += eoff[e] > 0;
   }
-  int tot_c, tot_d;
+  int lm = 0;
+  for (int e = e0; e < e1; ++e) lm += (eoff[e] + 127) >> 7;
+  int tot_c, tot_d, tot_m;
   int oc = block_exclusive_scan(lc, red, &tot_c);
   int od = block_exclusive_scan(ld, red, &tot_d);
+  int om = block_exclusive_scan(lm, red, &tot_m);
   for (int e = e0; e < e1; ++e) {
     const int c = eoff[e];
     rb.counts[e] = c;
     rb.offsets[e] = oc;
+    if (rb.mtp) rb.mtp[e] = om;
+    om += (c + 127) >> 7;
     eoff[e] = oc;
     if (c > 0) {
       if (rb.meta) rb.meta[od] = make_int4(e, oc, c, 0);
@@ -120,6 +125,7 @@ static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E
   if (tid == 0) {
     rb.offsets[E] = tot_c;
     *rb.nd = tot_d;
+    if (rb.mtp) rb.mtp[E] = tot_m;
   }
   __syncthreads();
   // pass 2: stable placement

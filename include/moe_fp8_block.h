@@ -229,6 +229,13 @@ int moe_fp8_block_set_stage_events(void* const* events, int n);
 /* MOE_FP8_BLOCK_ABI_VERSION of the built library. */
 int moe_fp8_block_abi_version(void);
 
+/* Text of the CUDA error behind the last MOE_ERR_CUDA returned on this host
+ * thread, with the stage that raised it (empty string if none).  Setting
+ * the environment variable MOE_FP8_BLOCK_SYNC_CHECK=1 makes every forward
+ * synchronise after each kernel and report the first failing one here
+ * (a debugging aid; it serialises the stream). */
+const char* moe_fp8_block_last_error_detail(void);
+
 /* Static description of a return code (never NULL). */
 const char* moe_fp8_block_error_string(int code);
 

@@ -157,3 +157,73 @@ def test_empty_and_all_skipped(cuda_lib):
     out = api.forward_problem(prob, force_path="decode")
     torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0
+
+
+# ------------------------------------------------------- prefill (W8A8)
+def test_tiny_prefill_all_expert_oracle(cuda_lib):
+    prob = problem(syn.TINY, 4)
+    r, _ = run_and_check(prob, "prefill", mode="all")
+    assert r < TOL
+
+
+@pytest.mark.parametrize("T", [1, 7, 16])
+def test_prefill_small_experts(cuda_lib, T):
+    r, _ = run_and_check(problem(syn.DECODE_SMALL, T), "prefill")
+    assert r < TOL
+
+
+@pytest.mark.parametrize("T", [8, 32])
+def test_prefill_padded_skewed(cuda_lib, T):
+    r, _ = run_and_check(problem(syn.PADDED_SKEWED, T, routing="hot"), "prefill")
+    assert r < TOL
+
+
+@pytest.mark.parametrize("T,routing,tokens", [
+    (1024, "softmax", None), (1024, "zipf", None),
+    (4096, "softmax", [0, 1, 2047, 4095]), (4096, "zipf", [3, 100, 4000]),
+    (16384, "zipf", [0, 8191, 16383]),
+])
+def test_prefill_grouped_gemm(cuda_lib, T, routing, tokens):
+    r, _ = run_and_check(problem(syn.PREFILL, T, routing=routing), "prefill", tokens=tokens)
+    assert r < TOL
+
+
+def test_default_gate_prefill(cuda_lib):
+    prob = problem(syn.DECODE_SMALL, 7)
+    api.forward_problem(prob)
+    assert api.moe_fp8_block_last_path() == 2
+
+
+def test_prefill_deterministic_and_padded(cuda_lib):
+    prob = problem(syn.PADDED_SKEWED, 32, routing="hot")
+    a = api.forward_problem(prob, force_path="prefill")
+    b = api.forward_problem(prob, force_path="prefill")
+    unp = dict(prob)
+    unp["w2_scale"] = prob["w2_scale"][..., :5].contiguous()
+    c = api.forward_problem(unp, force_path="prefill")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_prefill_matches_decode_closely(cuda_lib):
+    """Gathered W8A16 and W8A8 paths on the same inputs agree to the
+    activation-quantisation error (the pages' VERIFY mode compares the two
+    paths of one layer)."""
+    prob = problem(syn.DECODE_SMALL, 8)
+    d = api.forward_problem(prob, force_path="decode").float()
+    p = api.forward_problem(prob, force_path="prefill").float()
+    torch.cuda.synchronize()
+    scale = d.abs().amax(dim=1)
+    assert torch.all((d - p).abs().amax(dim=1) <= 0.1 * scale)
+
+
+def test_prefill_status_and_skipped_slots(cuda_lib):
+    prob = problem(syn.DECODE_SMALL, 16)
+    ids = prob["topk_ids"].clone()
+    ids[0, 1] = -1
+    ids[1, 0] = 128
+    ids[2, 1] = ids[2, 0]
+    prob["topk_ids"] = ids
+    api.moe_fp8_block_device_status()
+    r, _ = run_and_check(prob, "prefill")
+    assert api.moe_fp8_block_device_status() == 1
