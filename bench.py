@@ -298,6 +298,7 @@ def run_ours(args, world, rank, local):
 
     # end to end through the host-buffer entry point (pinned host inputs/outputs)
     e2e_v, h2d, d2h = e2e_hostio(probs, s, flush, args.steps, args.warmup)
+    prefill = prefill_leg(dev, s, flush, max(5, args.steps)) if not args.no_prefill else None
 
     if rank != 0:
         return
@@ -326,6 +327,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{src} hbm_gbs (copy, burst)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "prefill": prefill,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
         "wall_s": wall,
@@ -386,12 +388,74 @@ def e2e_hostio(probs, s, flush, steps, warmup):
     return total_b / total_s / 1e9, h2d, d2h
 
 
+PREFILL_CASES = [(1024, "softmax"), (4096, "softmax"), (4096, "zipf"), (16384, "softmax"), (16384, "zipf")]
+
+
+def prefill_leg(dev, s, flush, reps):
+    """Prefill grouped GEMM workload (E=128, H=2048, I=512, top_k=8): FP8
+    TFLOPS = 6*T*k*H*I / forward time, per-kernel times from stage events."""
+    import ctypes
+    from block_fp8_mixture_route_gb300 import _lib
+    lib = _lib.load()
+    shp = syn.PREFILL
+    w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
+    _, bf16_peak, src = peaks()
+    fp8_peak = 2.0 * bf16_peak
+    res = {}
+    for T, routing in PREFILL_CASES:
+        ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, routing, step=T)
+        prob = dict(hidden=syn.make_hidden(T, shp.H, 0, dev, step=T), topk_ids=ids, topk_weights=w, w13=w13,
+                    w13_scale=w13s, w2=w2, w2_scale=w2s)
+        out = torch.empty(T, shp.H, dtype=torch.bfloat16, device=dev)
+        flops = 6.0 * T * shp.k * shp.H * shp.I
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                api.forward_problem(prob, out=out, stream=s, force_path="prefill")
+        s.synchronize()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                flush.zero_()
+                e0.record(s)
+                api.forward_problem(prob, out=out, stream=s, force_path="prefill")
+                e1.record(s)
+            s.synchronize()
+            times.append(e0.elapsed_time(e1))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in evs:
+            e.record(s)
+        s.synchronize()
+        arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in evs])
+        st = []
+        for _ in range(max(3, reps // 2)):
+            with torch.cuda.stream(s):
+                flush.zero_()
+                _lib.check(lib.moe_fp8_block_set_stage_events(arr, 6), "set_stage_events")
+                api.forward_problem(prob, out=out, stream=s, force_path="prefill")
+            s.synchronize()
+            st.append([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
+        stage = [statistics.median(x[i] for x in st) for i in range(5)]
+        ms = statistics.median(times)
+        g1f, g2f = 4.0 * T * shp.k * shp.H * shp.I, 2.0 * T * shp.k * shp.H * shp.I
+        res[f"T{T}_{routing}"] = {
+            "us": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12, "frac_of_fp8_peak": flops / (ms / 1e3) / 1e12 / fp8_peak,
+            "stage_us": {n: round(1e3 * v, 2) for n, v in
+                         zip(("route", "act_quant_permute", "gemm1", "gemm2", "combine"), stage)},
+            "gemm1_tflops": g1f / (stage[2] / 1e3) / 1e12, "gemm2_tflops": g2f / (stage[3] / 1e3) / 1e12,
+        }
+    res["fp8_peak_tflops"] = fp8_peak
+    res["peak_source"] = f"2 x {src} bf16_tflops (burst)"
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

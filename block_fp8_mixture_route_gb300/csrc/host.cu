@@ -34,7 +34,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Byte layout of one workspace.
 struct Layout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp;
+  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, rcnt;
   size_t xh, xexp, h, ybuf;                       // decode
   size_t xq, xs, hq, hs, slots;                   // prefill
   size_t hid, tids, twts, outb;                   // host-io staging
@@ -60,6 +60,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   L.nd = take(16);
   L.meta = take(16 * (size_t)(g > 0 ? g : 1));
   L.mtp = take(4 * (size_t)(E + 1));
+  L.rcnt = take(4 * (size_t)route_chunks((int)S) * (size_t)E);
   if (path == MOE_PATH_DECODE) {
     L.xh = take(2 * (size_t)(T * H));
     L.xexp = take(4 * (size_t)T);
@@ -305,7 +306,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     pb.hq = reinterpret_cast<uint8_t*>(w + L.hq);
     pb.hs = reinterpret_cast<float*>(w + L.hs);
     pb.slots = reinterpret_cast<uint16_t*>(w + L.slots);
-    err = launch_prefill(a, rb, pb, status, dev, st, &launches);
+    err = launch_prefill(a, rb, pb, reinterpret_cast<int32_t*>(w + L.rcnt), status, dev, st, &launches);
   }
   if (err == cudaErrorNotSupported) {
     cudaGetLastError();
@@ -472,10 +473,13 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, 
   if ((rc = device_ok(&dev))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if ((rc = get_workspace(st, 16, &ws))) return rc;
+  const size_t scratch_bytes = 4 * (size_t)route_chunks((int)S) * (size_t)E;
+  if ((rc = get_workspace(st, 256 + scratch_bytes, &ws))) return rc;
   RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr, nullptr};
-  if (launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb, static_cast<uint32_t*>(ws), st) !=
-      cudaSuccess) {
+  int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
+  if (note_error(launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb,
+                              static_cast<uint32_t*>(ws), scratch, st, nullptr),
+                 "route") != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }

@@ -71,8 +71,15 @@ bool stage_mark(cudaStream_t st, int i);
 cudaError_t note_error(cudaError_t e, const char* stage);
 cudaError_t launch_check(cudaError_t launch_err, cudaStream_t st, const char* stage);
 
+// Routing lists.  With `scratch` (route_chunks(S) * E ints) large slot
+// counts use the three-kernel route; without it one CTA does everything.
+// Adds the number of launches to *launches (if given).
+constexpr int kRouteSingleMax = 16384;   // slots one CTA handles
+constexpr int kRouteChunk = 1024;        // slots per chunk of the three-kernel route
+constexpr int kRouteMaxChunks = 512;
+int route_chunks(int S);
 cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, uint32_t* status,
-                         cudaStream_t st);
+                         int32_t* scratch, cudaStream_t st, int* launches);
 cudaError_t launch_widen(const uint8_t* codes, int64_t n, float* out, cudaStream_t st);
 
 // Whether the decode path can stage rows of this layer shape in shared memory.
@@ -86,8 +93,8 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
 // Prefill (W8A8) path.
 cudaError_t launch_act_quant(const uint16_t* x, int64_t ld, int R, int K, uint8_t* codes, float* scales,
                              cudaStream_t st, bool pdl);
-cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, uint32_t* status,
-                           int device, cudaStream_t st, int* launches);
+cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, int32_t* route_scratch,
+                           uint32_t* status, int device, cudaStream_t st, int* launches);
 
 // Shared-memory bytes the route kernel needs for E experts with nthreads.
 size_t route_smem_bytes(int E, int nthreads);

@@ -105,27 +105,55 @@ struct PrefillArgs {
 };
 
 // The same quantisation, with the codes and scale of token t written to the
-// rows of all its routed slots (routed order: row inv[t*k + j]).
+// rows of all its routed slots (routed order: row inv[t*k + j]).  A warp
+// covers four 128-column groups of one token; eight lanes per group, 16
+// values per lane, 16-byte code stores.
 __global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p) {
   pdl_wait();
   pdl_trigger();
   const LayerArgs& a = p.a;
   const int groups = a.H / 128;
+  const int nq = (groups + 3) / 4;
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (wid >= (int64_t)a.T * groups) return;
+  if (wid >= (int64_t)a.T * nq) return;
   const int lane = threadIdx.x & 31;
-  const int t = (int)(wid / groups);
-  const int gi = (int)(wid % groups);
-  const uint2 raw = *reinterpret_cast<const uint2*>(a.hidden + (int64_t)t * a.hidden_ld + gi * 128 + lane * 4);
-  const float v[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xFFFFu),
-                      bf16_to_f32(raw.y >> 16)};
-  float sc;
-  const uint32_t packed = quant_group_warp(v, sc);
+  const int t = (int)(wid / nq);
+  const int gi = (int)(wid % nq) * 4 + (lane >> 3);
+  const bool valid = gi < groups;
+  const int col = gi * 128 + (lane & 7) * 16;
+  float v[16];
+  float m = 0.f;
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * a.hidden_ld + col);
+    const uint4 r0 = src[0], r1 = src[1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_to_f32(w[i] & 0xFFFFu);
+      v[2 * i + 1] = bf16_to_f32(w[i] >> 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (!valid) return;
+  const float sc = __fdiv_rn(m, 448.0f);
+  uint32_t q[4] = {0u, 0u, 0u, 0u};
+  if (sc != 0.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i], sc), __fdiv_rn(v[4 * i + 1], sc));
+      const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 2], sc), __fdiv_rn(v[4 * i + 3], sc));
+      q[i] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+    }
+  }
+  const uint4 qq = make_uint4(q[0], q[1], q[2], q[3]);
   for (int j = 0; j < a.k; ++j) {
     const int pos = p.rb.inv[t * a.k + j];
     if (pos < 0) continue;
-    *reinterpret_cast<uint32_t*>(p.pb.xq + (int64_t)pos * a.H + gi * 128 + lane * 4) = packed;
-    if (lane == 0) p.pb.xs[(int64_t)pos * groups + gi] = sc;
+    *reinterpret_cast<uint4*>(p.pb.xq + (int64_t)pos * a.H + col) = qq;
+    if ((lane & 7) == 0) p.pb.xs[(int64_t)pos * groups + gi] = sc;
   }
 }
 
@@ -244,9 +272,33 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const uint64_t pol_b = l2_policy_evict_last();
       long it = 0;
       bool ok = true;
+      // L2 prefetch runs PD K blocks ahead of the shared-memory loads (across
+      // tile boundaries), so the stage loads find their tiles in L2.
+      constexpr int PD = 8;
+      long pt = blockIdx.x;
+      int pkb = 0;
+      Tile ptl = pt < total ? tile_of(p, pt, NBT) : Tile{0, 0, 0, 0};
+      auto prefetch_next = [&]() {
+        if (pt >= total) return;
+        tc::tma_prefetch_2d(&tmA, pkb * BK, ptl.p0);
+        if (MODE == 1) {
+          const int r0 = ptl.e * 2 * a.I + ptl.nb * 128;
+          tc::tma_prefetch_2d(&tmB, pkb * BK, r0);
+          tc::tma_prefetch_2d(&tmB, pkb * BK, r0 + a.I);
+        } else {
+          tc::tma_prefetch_2d(&tmB, pkb * BK, ptl.e * a.H + ptl.nb * BN);
+        }
+        if (++pkb == nkb) {
+          pkb = 0;
+          pt += gridDim.x;
+          if (pt < total) ptl = tile_of(p, pt, NBT);
+        }
+      };
+      for (int i = 0; i < PD; ++i) prefetch_next();
       for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = tile_of(p, t, NBT);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
+          prefetch_next();
           const int s = (int)(it % NS);
           if (it >= NS && !mbar_wait(&empty[s], (uint32_t)((it / NS) - 1) & 1)) {
             ok = false;
@@ -500,8 +552,8 @@ static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, uint32_t* status,
-                           int device, cudaStream_t st, int* launches) {
+cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, int32_t* route_scratch,
+                           uint32_t* status, int device, cudaStream_t st, int* launches) {
   PrefillArgs p{a, rb, pb, status};
   CUtensorMap mx, m13, mh, m2;
   if (!make_map(&mx, pb.xq, (uint64_t)a.S, (uint64_t)a.H, 128) ||
@@ -521,9 +573,11 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   const int sms = num_sms(device);
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
-  if ((err = launch_check(launch_route(a.ids, a.S, a.E, rb, status, st), st, "route"))) return err;
+  int nl = 0;
+  if ((err = launch_check(launch_route(a.ids, a.S, a.E, rb, status, route_scratch, st, &nl), st, "route")))
+    return err;
   stage_mark(st, 1);
-  const int64_t warps = (int64_t)a.T * (a.H / 128);
+  const int64_t warps = (int64_t)a.T * ((a.H / 128 + 3) / 4);
   if ((err = launch_check(launch_ex(act_quant_permute_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st,
                                     pdl, p),
                           st, "act_quant_permute")))
@@ -544,7 +598,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                           st, "prefill_combine")))
     return err;
   stage_mark(st, 5);
-  *launches += 5;
+  *launches += 4 + nl;
   return cudaSuccess;
 }
 

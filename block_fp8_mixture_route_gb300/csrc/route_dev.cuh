@@ -1,19 +1,21 @@
-// route_dev.cuh -- the routing-list computation as a device function, used
-// by the standalone route kernel and by the first kernel of each path.
+// route_dev.cuh -- the routing-list computation, as device functions used by
+// the single-CTA route (small slot counts, fused into the decode path's
+// first kernel) and by the three-kernel route for large slot counts.
 //
 // The gathered path reads only the g = min(E, T*k) routed experts
 // (fp8-moe-gather page, sections Problem and The fix).  The routing lists
 // tell the expert kernels which slots each routed expert serves: per-expert
 // counts and offsets, the slots grouped by expert (stable in slot index),
-// the inverse permutation and the ascending list of distinct routed experts
-// padded with -1 to its static length g.
+// the inverse permutation, the ascending list of distinct routed experts
+// padded with -1 to its static length g, one (expert, offset, count) record
+// per distinct expert and the per-expert prefix of 128-row tiles.
 //
-// One CTA.  Every warp owns a contiguous segment of slots.  Pass 1 counts
-// each warp's slots per expert with __match_any_sync (one leader per group
-// of equal ids); a per-expert prefix over warps plus a block scan over
-// experts gives every (warp, expert) its first output position; pass 2
-// walks the segments again and places each slot at
-// offset[e] + warp_prefix[w][e] + (rank among equal ids in the 32-slot step),
+// Stable placement: every warp owns a contiguous segment of slots.  Pass 1
+// counts each warp's slots per expert with __match_any_sync (one leader per
+// group of equal ids); a per-expert prefix over warps plus the expert's base
+// gives every (warp, expert) its first output position; pass 2 walks the
+// segments again and places each slot at
+// base[e] + warp_prefix[w][e] + (rank among equal ids in the 32-slot step),
 // which keeps the grouping stable in the slot index.
 #pragma once
 
@@ -56,53 +58,84 @@ static __device__ int block_exclusive_scan(int v, int* red /*[33]*/, int* total)
   return base + x - v;
 }
 
-// The route computation for one CTA (blockDim.x threads, a multiple of 32).
-// Dynamic shared memory: route_smem_bytes(E, blockDim.x).
-static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E, RouteBufs rb, uint32_t* status,
-                           int* smem) {
-  __shared__ int red[33];
-  __shared__ int bad;
+// Pass 1 over slots [s0, s1) split into contiguous per-warp segments:
+// wcnt[w][e] = slots of warp w routed to expert e.  Sets *bad if an id >= E
+// is seen.  Ends with __syncthreads.
+static __device__ void route_warp_counts(const int32_t* __restrict__ ids, int s0, int s1, int E, int* wcnt,
+                                         int* bad) {
   const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = nt >> 5;
-  int* wcnt = smem;            // [nw][E]
-  int* eoff = smem + nw * E;   // [E]
   for (int i = tid; i < nw * E; i += nt) wcnt[i] = 0;
-  if (tid == 0) bad = 0;
   __syncthreads();
-
-  const int seg = (S + nw - 1) / nw;
-  const int s0 = min(S, w * seg), s1 = min(S, s0 + seg);
-  // pass 1: per-warp counts
-  for (int base = s0; base < s1; base += 32) {
+  const int seg = (s1 - s0 + nw - 1) / nw;
+  const int a = min(s1, s0 + w * seg), b = min(s1, a + seg);
+  for (int base = a; base < b; base += 32) {
     const int s = base + lane;
-    const int id = s < s1 ? ids[s] : -1;
-    const bool valid = s < s1 && id >= 0 && id < E;
-    if (s < s1 && id >= E) bad = 1;
+    const int id = s < b ? ids[s] : -1;
+    const bool valid = s < b && id >= 0 && id < E;
+    if (s < b && id >= E) *bad = 1;
     const uint32_t peers = __match_any_sync(0xffffffffu, valid ? id : -1);
     if (valid && lane == __ffs(peers) - 1) wcnt[w * E + id] += __popc(peers);
     __syncwarp();
   }
   __syncthreads();
-  // per expert: exclusive prefix over warps, total count
-  for (int e = tid; e < E; e += nt) {
+}
+
+// wcnt[w][e] -> exclusive prefix over warps; tot[e] = column totals.
+// Ends with __syncthreads.
+static __device__ void route_warp_prefix(int* wcnt, int E, int* tot) {
+  const int nt = blockDim.x, nw = nt >> 5;
+  for (int e = threadIdx.x; e < E; e += nt) {
     int run = 0;
     for (int ww = 0; ww < nw; ++ww) {
       const int c = wcnt[ww * E + e];
       wcnt[ww * E + e] = run;
       run += c;
     }
-    eoff[e] = run;
+    tot[e] = run;
   }
   __syncthreads();
-  // block scan over experts: counts -> offsets; distinct flags -> glist
+}
+
+// Pass 2: place every valid slot of [s0, s1) at base(e) + wcnt[w][e] + rank.
+template <typename BaseF>
+static __device__ void route_warp_place(const int32_t* __restrict__ ids, int s0, int s1, int E, int* wcnt,
+                                        BaseF base_of, RouteBufs rb) {
+  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = nt >> 5;
+  const int seg = (s1 - s0 + nw - 1) / nw;
+  const int a = min(s1, s0 + w * seg), b = min(s1, a + seg);
+  for (int base = a; base < b; base += 32) {
+    const int s = base + lane;
+    const int id = s < b ? ids[s] : -1;
+    const bool valid = s < b && id >= 0 && id < E;
+    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+    if (valid) {
+      const int pos = base_of(id) + wcnt[w * E + id] + __popc(peers & lanemask_lt());
+      rb.perm[pos] = s;
+      rb.inv[s] = pos;
+    } else if (s < b) {
+      rb.inv[s] = -1;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wcnt[w * E + id] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Expert-level lists from per-expert counts in eoff[E] (shared memory):
+// writes counts, offsets, glist (padded to min(E, S)), meta, mtp, n_distinct
+// and fills perm[offsets[E] .. S) with -1.  On return eoff[e] holds the
+// offset of expert e.  Ends with __syncthreads.
+static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) {
+  __shared__ int red[33];
+  const int nt = blockDim.x, tid = threadIdx.x;
   const int per = (E + nt - 1) / nt;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int lc = 0, ld = 0;
+  int lc = 0, ld = 0, lm = 0;
   for (int e = e0; e < e1; ++e) {
     lc += eoff[e];
     ld += eoff[e] > 0;
+    lm += (eoff[e] + 127) >> 7;
   }
-  int lm = 0;
-  for (int e = e0; e < e1; ++e) lm += (eoff[e] + 127) >> 7;
   int tot_c, tot_d, tot_m;
   int oc = block_exclusive_scan(lc, red, &tot_c);
   int od = block_exclusive_scan(ld, red, &tot_d);
@@ -127,26 +160,24 @@ static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E
     *rb.nd = tot_d;
     if (rb.mtp) rb.mtp[E] = tot_m;
   }
-  __syncthreads();
-  // pass 2: stable placement
-  for (int base = s0; base < s1; base += 32) {
-    const int s = base + lane;
-    const int id = s < s1 ? ids[s] : -1;
-    const bool valid = s < s1 && id >= 0 && id < E;
-    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? id : -1);
-    if (valid) {
-      const int pos = eoff[id] + wcnt[w * E + id] + __popc(peers & lanemask_lt());
-      rb.perm[pos] = s;
-      rb.inv[s] = pos;
-    } else if (s < s1) {
-      rb.inv[s] = -1;
-    }
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) wcnt[w * E + id] += __popc(peers);
-    __syncwarp();
-  }
   for (int q = tot_c + tid; q < S; q += nt) rb.perm[q] = -1;
-  if (tid == 0 && bad) raise_status(status, MOE_STATUS_BAD_ID);
+  __syncthreads();
+}
+
+// The whole route for one CTA (blockDim.x threads, a multiple of 32).
+// Dynamic shared memory: route_smem_bytes(E, blockDim.x).
+static __device__ void route_block(const int32_t* __restrict__ ids, int S, int E, RouteBufs rb, uint32_t* status,
+                                   int* smem) {
+  __shared__ int bad;
+  const int nw = blockDim.x >> 5;
+  int* wcnt = smem;            // [nw][E]
+  int* eoff = smem + nw * E;   // [E]
+  if (threadIdx.x == 0) bad = 0;
+  route_warp_counts(ids, 0, S, E, wcnt, &bad);
+  route_warp_prefix(wcnt, E, eoff);
+  route_expert_scan(eoff, E, S, rb);
+  route_warp_place(ids, 0, S, E, wcnt, [&](int e) { return eoff[e]; }, rb);
+  if (threadIdx.x == 0 && bad) raise_status(status, MOE_STATUS_BAD_ID);
 }
 
 }  // namespace moe
