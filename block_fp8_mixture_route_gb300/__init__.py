@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     moe_fp8_block_act_quant,
     moe_fp8_block_device_status,
     moe_fp8_block_forward,
+    moe_fp8_block_forward_decode_noalloc,
     moe_fp8_block_forward_hostio,
     moe_fp8_block_last_launches,
     moe_fp8_block_last_path,

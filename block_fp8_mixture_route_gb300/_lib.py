@@ -27,6 +27,7 @@ ERRORS = {
 # every symbol the header declares
 EXPORTS = [
     "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_hostio",
+    "moe_fp8_block_forward_decode_noalloc",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
     "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_last_error_detail", "moe_fp8_block_error_string",
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_forward.argtypes = fwd
         lib.moe_fp8_block_forward_ex.argtypes = fwd + [P(MoeOptions)]
         lib.moe_fp8_block_forward_hostio.argtypes = fwd + [P(MoeOptions)]
+        lib.moe_fp8_block_forward_decode_noalloc.argtypes = fwd
         lib.moe_fp8_block_route.argtypes = [T, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.moe_fp8_block_act_quant.argtypes = [T, vp, vp, vp]
         lib.moe_fp8_block_widen_e4m3.argtypes = [vp, i64, vp, vp]

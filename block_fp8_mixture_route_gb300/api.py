@@ -97,6 +97,21 @@ def moe_fp8_block_forward_hostio(hidden, topk_ids, topk_weights, w13, w13_scale,
     return out
 
 
+def moe_fp8_block_forward_decode_noalloc(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
+                                         w2_scale, w2_scale_stride, out, stream=None):
+    """The decode path without any device allocation (scratch in a fixed
+    library-owned array); `out` must be supplied by the caller."""
+    lib = _lib.load()
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    o = desc(out)
+    P = ctypes.byref
+    rc = lib.moe_fp8_block_forward_decode_noalloc(*[P(x) for x in args], int(w13_scale_stride),
+                                                  *[P(x) for x in a2], int(w2_scale_stride), P(o), _stream(stream))
+    check(rc, "moe_fp8_block_forward_decode_noalloc")
+    return out
+
+
 def moe_fp8_block_route(topk_ids: torch.Tensor, E: int, stream=None):
     """Routing lists (see the header): dict of int32 device tensors."""
     lib = _lib.load()

@@ -416,6 +416,21 @@ bool stage_mark(cudaStream_t st, int i) {
   return true;
 }
 
+int validate_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
+                     const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                     const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride,
+                     const moe_tensor* out, LayerArgs* args, int* device) {
+  Checked c{};
+  int rc = check_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                         w2_scale_stride, out, false, &c);
+  if (rc) return rc;
+  *args = c.a;
+  if (c.T == 0) return MOE_OK;
+  return device_ok(device);
+}
+
+void set_error_detail(const char* text) { snprintf(g_err_detail, sizeof(g_err_detail), "%s", text); }
+
 int num_sms(int device) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_sms.find(device);

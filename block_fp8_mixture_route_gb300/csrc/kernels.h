@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "moe_fp8_block.h"
+
 namespace moe {
 
 // Arguments shared by the kernels of one forward call.  All pointers are
@@ -55,6 +57,15 @@ struct PrefillBufs {
 };
 
 int num_sms(int device);
+
+// Argument checks of moe_fp8_block_forward for other entry points: fills
+// *args and, when T > 0, the current device (which must be sm_103).
+int validate_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
+                     const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                     const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride,
+                     const moe_tensor* out, LayerArgs* args, int* device);
+// Text returned by moe_fp8_block_last_error_detail on this thread.
+void set_error_detail(const char* text);
 
 // Stage events of moe_fp8_block_set_stage_events (per host thread).
 struct StageEvents {

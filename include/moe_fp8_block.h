@@ -162,6 +162,46 @@ int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* top
                                  int64_t w2_scale_stride, moe_tensor* out, void* stream,
                                  const moe_options* opt);
 
+/* Size in bytes of the fixed device array behind
+ * moe_fp8_block_forward_decode_noalloc. */
+#define MOE_FP8_BLOCK_NOALLOC_BYTES (8u << 20)
+
+/*
+ * moe_fp8_block_forward_decode_noalloc -- the decode (W8A16) path of
+ * moe_fp8_block_forward, for callers that cannot let the library allocate
+ * device memory.  It has no counterpart in the pages this library follows;
+ * it exists for deployments where every byte of device memory is planned up
+ * front (a framework-owned pool, a fixed per-model budget) or where an
+ * allocation inside a serving loop is unacceptable (cudaMalloc can
+ * synchronise the device and can fail under memory pressure), so that the
+ * per-stream workspace that moe_fp8_block_forward grows on demand is not an
+ * option.
+ *
+ * Arguments, layouts and return codes are those of moe_fp8_block_forward;
+ * the path is always decode.  The caller passes inputs and outputs as usual;
+ * all scratch (routing lists, the f16 activation copy, h and the per-slot
+ * outputs) lives in one statically allocated device array of
+ * MOE_FP8_BLOCK_NOALLOC_BYTES bytes that every GPU using the library keeps
+ * until the process exits.  A call needs about
+ * 4*T*k*(H + I) + 2*T*H + 16*(E + T*k) bytes of it; a larger call returns
+ * MOE_ERR_ARG and moe_fp8_block_last_error_detail says how many bytes it
+ * needed.  Nothing is allocated: no cudaMalloc or cudaFree, no allocating
+ * library routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before capturing the stream into a CUDA graph.  Every call on every stream
+ * of a device uses the same array: calls whose kernels overlap on the GPU
+ * race and give wrong results, so serialise them (one stream, or events).
+ * Each call clears the array's status word first; the status bits of this
+ * entry point are not reported by moe_fp8_block_device_status.
+ */
+int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                         const moe_tensor* topk_weights, const moe_tensor* w13,
+                                         const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                                         const moe_tensor* w2, const moe_tensor* w2_scale,
+                                         int64_t w2_scale_stride, moe_tensor* out, void* stream);
+
 /*
  * moe_fp8_block_route -- the routing lists of the gathered path, on their
  * own (the same kernel the forward runs).  For S = T*k slots s = t*k + j:

@@ -1,0 +1,58 @@
+"""The allocation-free decode entry point, through the C ABI.
+
+For callers that cannot let the library allocate device memory (a
+pre-planned memory budget, or a serving loop where cudaMalloc's implicit
+synchronisation and possible failure are not acceptable), the library
+offers moe_fp8_block_forward_decode_noalloc, whose scratch is a fixed,
+statically allocated device array.  Its output must match the regular
+forward on the same inputs -- on two calls in a row, since every call
+reuses the same array -- and a call too large for the array must be
+refused with an error instead of running.
+
+This file is collected last so that a failure here does not hide the
+results of the other GPU tests."""
+import pytest
+import torch
+
+from block_fp8_mixture_route_gb300 import _lib, api, synthetic as syn
+
+from helpers import check_per_token
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(shape, T, step, weights):
+    w13, w13s, w2, w2s = weights
+    ids, w = syn.make_routing(T, shape.E, shape.k, 0, "cuda", "softmax", step=step)
+    return dict(hidden=syn.make_hidden(T, shape.H, 0, "cuda", step), topk_ids=ids, topk_weights=w, w13=w13,
+                w13_scale=w13s, w2=w2, w2_scale=w2s)
+
+
+def _noalloc(prob, out):
+    return api.moe_fp8_block_forward_decode_noalloc(
+        prob["hidden"], prob["topk_ids"], prob["topk_weights"], prob["w13"], prob["w13_scale"],
+        prob["w13_scale"].stride(1), prob["w2"], prob["w2_scale"], prob["w2_scale"].stride(1), out)
+
+
+def test_noalloc_matches_forward_on_two_calls(cuda_lib):
+    shape = syn.DECODE_SMALL
+    weights = syn.make_weights(shape, 0, "cuda")
+    for T, step in ((16, 1), (4, 2)):          # two calls in a row on the shared scratch
+        prob = _problem(shape, T, step, weights)
+        out = torch.empty(T, shape.H, dtype=torch.bfloat16, device="cuda")
+        _noalloc(prob, out)
+        ref = api.forward_problem(prob, force_path="decode")
+        torch.cuda.synchronize()
+        check_per_token(out.float().cpu().numpy(), ref.float().cpu().numpy())
+
+
+def test_noalloc_refuses_calls_too_large_for_its_array(cuda_lib):
+    shape = syn.DECODE_WIDE
+    small = syn.MoeShape(E=8, H=shape.H, I=shape.I, k=8)
+    weights = syn.make_weights(small, 0, "cuda")
+    prob = _problem(small, 256, 3, weights)   # 2048 slots x (7168 + 2048) x 4 B > 8 MiB
+    out = torch.empty(256, small.H, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(_lib.MoeError) as ei:
+        _noalloc(prob, out)
+    assert ei.value.code == -9
+    assert "needs" in _lib.load().moe_fp8_block_last_error_detail().decode()
