@@ -324,6 +324,9 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": "decode_gemm1", "bound": "hbm", "achieved": g1_achieved, "peak": hbm,
                      "unit": "GB/s", "frac": g1_achieved / hbm,
                      "traffic": profile_traffic("decode_gemm1_kernel", "decode_small_T16"),
+                     "traffic_launch": "T=16 launch (ncu capture); achieved aggregates T=1..16",
+                     "algorithmic_bytes_T16": g1_bytes[16],
+                     "achieved_T16": g1_bytes[16] / (g1_ms[16] / 1e3) / 1e9,
                      "peak_source": f"{src} hbm_gbs (copy, burst)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -449,6 +452,35 @@ def prefill_leg(dev, s, flush, reps):
     return res
 
 
+PROFILE_CASES = ("decode_T16", "decode_T1", "prefill_T4096", "prefill_T16384")
+
+
+def profile_case(name: str, reps: int = 3):
+    """Run `reps` forwards of one case and nothing else (no timing, no
+    oracle): the command an ncu capture of a single kernel wraps."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream(device=dev)
+    if name.startswith("decode"):
+        T = int(name.split("_T")[1])
+        prob = make_problems(dev)[T]
+        path, H = "decode", SHAPE.H
+    else:
+        T = int(name.split("_T")[1])
+        shp = syn.PREFILL
+        w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
+        ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, "softmax", step=T)
+        prob = dict(hidden=syn.make_hidden(T, shp.H, 0, dev, step=T), topk_ids=ids, topk_weights=w, w13=w13,
+                    w13_scale=w13s, w2=w2, w2_scale=w2s)
+        path, H = "prefill", shp.H
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            api.forward_problem(prob, out=out, stream=s, force_path=path)
+    s.synchronize()
+    print(json.dumps({"profile_case": name, "reps": reps, "launches_per_forward": api.moe_fp8_block_last_launches()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,7 +488,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
+                    help="only run 3 forwards of one case (for ncu captures); prints no bench line")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
