@@ -36,7 +36,8 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
   size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, rcnt;
   size_t xh, xexp, h, ybuf;                       // decode
-  size_t xq, xs, hq, hs, slots;                   // prefill
+  size_t xq, xs, hq, hs, ys, pinv, wsc13, wsc2;  // prefill
+  int64_t prows;
   size_t hid, tids, twts, outb;                   // host-io staging
   size_t total;
 };
@@ -67,11 +68,16 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
     L.h = take(4 * (size_t)(S * I));
     L.ybuf = take(4 * (size_t)(S * H));
   } else if (path == MOE_PATH_PREFILL) {
-    L.xq = take((size_t)(S * H));
-    L.xs = take(4 * (size_t)(S * (H / 128)));
-    L.hq = take((size_t)(S * I));
-    L.hs = take(4 * (size_t)(S * (I / 128)));
-    L.slots = take(2 * (size_t)(S * H));
+    const int64_t R = prefill_rows(S, E);
+    L.prows = R;
+    L.xq = take((size_t)(R * H));
+    L.xs = take(4 * (size_t)(R * (H / 128)));
+    L.hq = take((size_t)(R * I));
+    L.hs = take(4 * (size_t)(R * (I / 128)));
+    L.ys = take(2 * (size_t)(R * H));
+    L.pinv = take(4 * (size_t)S);
+    L.wsc13 = take(16 * (size_t)E * (size_t)(H / 128) * (size_t)(I / 128));
+    L.wsc2 = take(16 * (size_t)E * (size_t)(I / 128) * (size_t)((H + 255) / 256));
   }
   if (hostio) {
     L.hid = take(2 * (size_t)(T * H));
@@ -302,10 +308,14 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
   } else {
     PrefillBufs pb;
     pb.xq = reinterpret_cast<uint8_t*>(w + L.xq);
-    pb.xs = reinterpret_cast<float*>(w + L.xs);
+    pb.xsT = reinterpret_cast<float*>(w + L.xs);
     pb.hq = reinterpret_cast<uint8_t*>(w + L.hq);
-    pb.hs = reinterpret_cast<float*>(w + L.hs);
-    pb.slots = reinterpret_cast<uint16_t*>(w + L.slots);
+    pb.hsT = reinterpret_cast<float*>(w + L.hs);
+    pb.ys = reinterpret_cast<uint16_t*>(w + L.ys);
+    pb.pinv = reinterpret_cast<int32_t*>(w + L.pinv);
+    pb.wsc13 = reinterpret_cast<float*>(w + L.wsc13);
+    pb.wsc2 = reinterpret_cast<float*>(w + L.wsc2);
+    pb.rows = L.prows;
     err = launch_prefill(a, rb, pb, reinterpret_cast<int32_t*>(w + L.rcnt), status, dev, st, &launches);
   }
   if (err == cudaErrorNotSupported) {

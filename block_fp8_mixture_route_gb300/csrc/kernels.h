@@ -47,14 +47,22 @@ struct DecodeBufs {
   float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
 };
 
-// Scratch of the prefill path (rows in routed order unless stated).
+// Scratch of the prefill path.  Per-row buffers hold `rows` rows in the
+// expert-padded routed order: expert e's slots start at row 128*mtp[e].
 struct PrefillBufs {
-  uint8_t* xq;        // e4m3 [S, H] activation codes of each routed slot's token
-  float* xs;          // [S, H/128] their scales
-  uint8_t* hq;        // e4m3 [S, I] h codes
-  float* hs;          // [S, I/128] h scales
-  uint16_t* slots;    // bf16 [S, H] per-slot outputs times top-k weight, slot order
+  uint8_t* xq;        // e4m3 [rows, H] activation codes of each routed slot's token
+  float* xsT;         // [H/128, rows] their scales, K-block major
+  uint8_t* hq;        // e4m3 [rows, I] h codes
+  float* hsT;         // [I/128, rows] h scales, K-block major
+  uint16_t* ys;       // bf16 [rows, H] down-projection output of each row (not yet weighted)
+  int32_t* pinv;      // [S] row of each slot, -1 for a skipped slot
+  float* wsc13;       // [E, H/128, I/128, 4] fp32 (gate, up, 0, 0) block scales
+  float* wsc2;        // [E, I/128, ceil(H/256), 4] fp32 (row block 2p, 2p+1, 0, 0) block scales
+  int64_t rows;       // row capacity, prefill_rows(S, E)
 };
+
+// Rows the expert-padded layout can need for S slots over E experts.
+int64_t prefill_rows(int64_t S, int E);
 
 int num_sms(int device);
 

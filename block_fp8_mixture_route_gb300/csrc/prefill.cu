@@ -8,18 +8,29 @@
 // accumulators in tensor memory), with h = silu(gate) * up fused into the
 // first GEMM's epilogue and quantised the same way, per slot per 128 columns.
 //
+// Row layout: the routed slots of expert e occupy rows [128*mtp[e],
+// 128*mtp[e] + count[e]) of every per-row buffer (mtp = exclusive prefix of
+// ceil(count/128)), so a 128-row tile never spans two experts; the rows
+// after count[e] up to the next multiple of 128 are padding whose contents
+// are never read back.  pinv[s] is the row of slot s.
+//
 // Kernels, in stream order (chained with programmatic dependent launch):
-//   route               routing lists + per-expert 128-row tile counts
-//   act_quant_permute   e4m3 codes/scales of every token, written to each of
-//                       its routed slots' rows (routed order), so that every
-//                       GEMM operand tile is one contiguous tensor-map load
-//   prefill_gemm<1>     per (expert, 128 slots, 128-row block of gate + the
-//                       matching block of up): X[128 x H] W13^T -> silu*up ->
-//                       e4m3 h codes + scales
-//   prefill_gemm<2>     per (expert, 128 slots, 256 rows of the down
-//                       projection): H[128 x I] W2^T * top-k weight -> bf16
-//                       slot rows
-//   prefill_combine     out[t] = sum_j slot[t*k + j] in j order
+//   route               routing lists + per-expert 128-row tile prefix
+//   act_quant_permute   e4m3 codes of every token written to the rows of
+//                       its routed slots, their scales K-block major
+//                       (xsT[kb][row]); extra CTAs repack the bf16 weight
+//                       block scales into fp32 records a tensor map can load
+//   prefill_gemm<1>     tile = (128 rows, 128-column block nb of gate and
+//                       the same block of up): silu*up -> e4m3 h + scales
+//   prefill_gemm<2>     tile = (128 rows, 256 rows of the down projection)
+//                       -> bf16 y rows
+//   prefill_combine     out[t] = sum_j w[t,j] * y[pinv[t*k + j]] in j order
+//
+// Every operand, scale and output of the GEMMs moves by tensor-map copies
+// (loads into a shared-memory ring, stores from a shared-memory staging
+// tile): ordinary global loads and stores issued while bulk tensor traffic
+// is in flight wait thousands of cycles on this part, so the GEMM kernels
+// issue none after their prologue.
 //
 // Block-scale promotion: a tcgen05 MMA chain covers one 128-wide K block
 // into a fresh TMEM accumulator; the epilogue warps read it back and add
@@ -104,11 +115,51 @@ struct PrefillArgs {
   uint32_t* status;
 };
 
-// The same quantisation, with the codes and scale of token t written to the
-// rows of all its routed slots (routed order: row inv[t*k + j]).  A warp
-// covers four 128-column groups of one token; eight lanes per group, 16
-// values per lane, 16-byte code stores.
-__global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p) {
+// Weight block scales as fp32 records of four (two used), one per (expert,
+// K block, output tile), so one 16-byte tensor-map load brings the two
+// column-block scales a tile needs for one K block:
+//   wsc13[e][kb][p] = (w13 scale of gate block p, of up block p, 0, 0)
+//   wsc2 [e][kb][p] = (w2 scale of row block 2p, of row block 2p+1 or 0, 0, 0)
+__device__ void repack_weight_scales(const PrefillArgs& p, int64_t idx) {
+  const LayerArgs& a = p.a;
+  const int np1 = a.I / 128, nk1 = a.H / 128;
+  const int np2 = (a.H + 255) / 256, nk2 = a.I / 128, nrow2 = a.H / 128;
+  const int64_t n13 = (int64_t)a.E * nk1 * np1;
+  const int64_t n2 = (int64_t)a.E * nk2 * np2;
+  if (idx < n13) {
+    const int pp = (int)(idx % np1);
+    const int kb = (int)((idx / np1) % nk1);
+    const int e = (int)(idx / ((int64_t)np1 * nk1));
+    const uint16_t* s = a.w13s + (int64_t)e * a.s13_exp + kb;
+    const float g = bf16_to_f32(s[(int64_t)pp * a.s13_row]);
+    const float u = bf16_to_f32(s[(int64_t)(np1 + pp) * a.s13_row]);
+    reinterpret_cast<float4*>(p.pb.wsc13)[idx] = make_float4(g, u, 0.f, 0.f);
+    return;
+  }
+  idx -= n13;
+  if (idx < n2) {
+    const int pp = (int)(idx % np2);
+    const int kb = (int)((idx / np2) % nk2);
+    const int e = (int)(idx / ((int64_t)np2 * nk2));
+    const uint16_t* s = a.w2s + (int64_t)e * a.s2_exp + kb;
+    const float r0 = bf16_to_f32(s[(int64_t)(2 * pp) * a.s2_row]);
+    const float r1 = 2 * pp + 1 < nrow2 ? bf16_to_f32(s[(int64_t)(2 * pp + 1) * a.s2_row]) : 0.f;
+    reinterpret_cast<float4*>(p.pb.wsc2)[idx] = make_float4(r0, r1, 0.f, 0.f);
+  }
+}
+
+// The activation quantisation of act_quant_kernel, with the codes of token
+// t written to the rows of all its routed slots and the scales K-block
+// major.  A warp covers four 128-column groups of one token; eight lanes
+// per group, 16 values per lane, 16-byte code stores.  CTAs from qblocks on
+// repack the weight scales instead (they read only the weights, so they do
+// it before waiting for the route kernel).
+__global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p, int qblocks) {
+  if ((int)blockIdx.x >= qblocks) {
+    repack_weight_scales(p, (int64_t)(blockIdx.x - qblocks) * blockDim.x + threadIdx.x);
+    pdl_trigger();
+    return;
+  }
   pdl_wait();
   pdl_trigger();
   const LayerArgs& a = p.a;
@@ -118,6 +169,7 @@ __global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p) {
   if (wid >= (int64_t)a.T * nq) return;
   const int lane = threadIdx.x & 31;
   const int t = (int)(wid / nq);
+  const bool first = (wid % nq) == 0;
   const int gi = (int)(wid % nq) * 4 + (lane >> 3);
   const bool valid = gi < groups;
   const int col = gi * 128 + (lane & 7) * 16;
@@ -150,191 +202,270 @@ __global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p) {
   }
   const uint4 qq = make_uint4(q[0], q[1], q[2], q[3]);
   for (int j = 0; j < a.k; ++j) {
-    const int pos = p.rb.inv[t * a.k + j];
-    if (pos < 0) continue;
-    *reinterpret_cast<uint4*>(p.pb.xq + (int64_t)pos * a.H + col) = qq;
-    if ((lane & 7) == 0) p.pb.xs[(int64_t)pos * groups + gi] = sc;
+    const int s = t * a.k + j;
+    const int e = a.ids[s];
+    if (e < 0 || e >= a.E) {
+      if (first && lane == 0) p.pb.pinv[s] = -1;
+      continue;
+    }
+    const int64_t row = (int64_t)p.rb.inv[s] - p.rb.offsets[e] + (int64_t)p.rb.mtp[e] * 128;
+    *reinterpret_cast<uint4*>(p.pb.xq + row * a.H + col) = qq;
+    if ((lane & 7) == 0) p.pb.xsT[(int64_t)gi * p.pb.rows + row] = sc;
+    if (first && lane == 0) p.pb.pinv[s] = (int32_t)row;
   }
 }
 
 // ---------------------------------------------------------- grouped GEMM --
 namespace pf {
-constexpr int BM = 128;            // rows (routed slots) per tile
-constexpr int BN = 256;            // output columns per tile
+constexpr int BM = 128;            // rows per tile
+constexpr int BN = 256;            // accumulator columns per tile
 constexpr int BK = 128;            // K block (bytes = e4m3 elements)
-constexpr int NS = 4;              // shared-memory stages
 constexpr int A_BYTES = BM * BK;   // 16 KiB
 constexpr int B_BYTES = BN * BK;   // 32 KiB
 constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int NSS = 8;             // scale-ring entries (>= stages + 2 accumulators)
 constexpr int NEPI = 8;            // epilogue warps (two per TMEM lane quarter)
 constexpr int THREADS = 32 * (2 + NEPI);
-constexpr int BAR_OFF = NS * STAGE;
-constexpr int XCH_OFF = BAR_OFF + 256;
-constexpr int SMEM = 1024 + XCH_OFF + 2 * BM * 2 * 4;
+constexpr int OUT1 = BM * 128;     // GEMM1 staging: 128 rows x 128 h codes (+ 128 fp32 scales)
+constexpr int OUT2 = BM * 128 * 2; // GEMM2 staging: 128 rows x 128 bf16, as two 64-column boxes
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 }  // namespace pf
 
-// Tile t -> (expert e, first routed row p0, valid rows, column block nb).
-struct Tile {
-  int e, p0, nvalid, nb;
+// Shared-memory layout of prefill_gemm_kernel<mode> with ns stages (byte
+// offsets from a 1024-aligned base; the same function on host and device).
+struct PfLayout {
+  uint32_t out, ring_a, ring_w, xch, bars, mtp, total;
 };
 
-__device__ __forceinline__ Tile tile_of(const PrefillArgs& p, long t, int NBT) {
-  const int mi = (int)(t / NBT);
-  Tile r;
-  r.nb = (int)(t % NBT);
-  const int* mtp = p.rb.mtp;
-  int lo = 0, hi = p.a.E;   // mtp[lo] <= mi < mtp[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(mtp + mid) <= mi) lo = mid;
-    else hi = mid;
-  }
-  r.e = lo;
-  const int mt = mi - __ldg(mtp + lo);
-  r.p0 = __ldg(p.rb.offsets + lo) + mt * pf::BM;
-  r.nvalid = min(pf::BM, __ldg(p.rb.counts + lo) - mt * pf::BM);
-  return r;
+__host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
+  PfLayout L;
+  uint32_t o = (uint32_t)ns * pf::STAGE;
+  L.out = o;
+  o += mode == 1 ? pf::OUT1 + 512 : pf::OUT2;
+  L.ring_a = o;
+  o += pf::NSS * 512;
+  L.ring_w = o;
+  o += pf::NSS * 128;   // 16 bytes used per entry; tensor copies into shared memory need 128-byte alignment
+  L.xch = o;
+  o += pf::BM * 2 * 4;
+  L.bars = o;
+  o += (2 * ns + 2 * pf::NSS + 4) * 8 + 16;
+  o = (o + 15u) & ~15u;
+  L.mtp = o;
+  o += 4u * (uint32_t)(E + 1);
+  L.total = o + 1024;   // slack for aligning the dynamic shared memory base
+  return L;
 }
 
-// 64 fp32 values times wt -> 64 bf16 (RNE), stored as 128 contiguous bytes.
-__device__ __forceinline__ void store_bf16_row64(uint16_t* dst, const float (&v)[64], float wt) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+// The tensor maps one GEMM uses: A rows, B rows, A scales (K-block major),
+// B scale records, and the output(s).
+struct PfMaps {
+  CUtensorMap a, b, sa, sw, o, os;
+};
+
+// Largest expert e with mtp[e] <= mi (the expert owning 128-row tile mi).
+__device__ __forceinline__ int expert_of_tile(const int* mtp, int E, int mi) {
+  int lo = 0, hi = E;   // mtp[lo] <= mi < mtp[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (mtp[mid] <= mi) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Barrier among the 8 epilogue warps (named barrier 1).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier, returning the OR of `v` over the 256 threads: every
+// epilogue thread gets the same answer, so all leave the tile loop together.
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// 64 fp32 values -> bf16 (RNE) into one 128-byte row of a 128-byte-swizzled
+// staging box (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+__device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const float (&v)[64]) {
+  uint8_t* r = box + row * 128;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int c = 0; c < 8; ++c) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * i + 2 * q] * wt, v[8 * i + 2 * q + 1] * wt);
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * c + 2 * q], v[8 * c + 2 * q + 1]);
       w[q] = *reinterpret_cast<uint32_t*>(&b);
     }
-    d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(r + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 // MODE 1: gate/up projection, silu(gate)*up, e4m3 h codes + scales.
-// MODE 2: down projection times the slot's top-k weight -> bf16 slot rows.
+// MODE 2: down projection -> bf16 y rows.
+// 10 warps: warp 0 issues tensor-map loads, warp 1 owns TMEM and issues the
+// MMAs, warps 2..9 promote, finish and store.
 template <int MODE>
-// 10 warps: two SM sub-partitions hold three of them, so each thread may
-// use at most 16384 / (3 * 32) -> 168 registers.
 __global__ void __launch_bounds__(pf::THREADS, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        PrefillArgs p) {
+    prefill_gemm_kernel(const __grid_constant__ PfMaps m, PrefillArgs p, int ns) {
   using namespace pf;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + BAR_OFF);
-  uint64_t* empty = full + NS;
-  uint64_t* tfull = empty + NS;
+  const LayerArgs& a = p.a;
+  const int E = a.E;
+  const PfLayout L = pf_layout(MODE, ns, E);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);
+  uint64_t* empty = full + ns;
+  uint64_t* sfull = empty + ns;
+  uint64_t* sempty = sfull + NSS;
+  uint64_t* tfull = sempty + NSS;
   uint64_t* tempty = tfull + 2;
-  uint64_t* xfull = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 2);
-  float* xch = reinterpret_cast<float*>(base + XCH_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  float* ring_a = reinterpret_cast<float*>(base + L.ring_a);
+  float* ring_w = reinterpret_cast<float*>(base + L.ring_w);
+  float* xch = reinterpret_cast<float*>(base + L.xch);
+  int* mtp_s = reinterpret_cast<int*>(base + L.mtp);
+  uint8_t* outs = base + L.out;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < ns; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < NSS; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], NEPI);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], NEPI);
-      mbar_init(&xfull[i], NEPI);
     }
     fence_mbar_init();
     abort_flag = 0;
-    tc::prefetch_tensormap(&tmA);
-    tc::prefetch_tensormap(&tmB);
+    tc::prefetch_tensormap(&m.a);
+    tc::prefetch_tensormap(&m.b);
+    tc::prefetch_tensormap(&m.sa);
+    tc::prefetch_tensormap(&m.sw);
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
     tc::tmem_relinquish();
   }
+  pdl_wait();
+  // the tile table, read once before any tensor-map traffic starts
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) mtp_s[i] = __ldg(p.rb.mtp + i);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  pdl_wait();
   pdl_trigger();
+  const uint32_t tmem = *tmem_slot;
 
-  const LayerArgs& a = p.a;
   const int K = MODE == 1 ? a.H : a.I;
   const int nkb = K / BK;
   const int NBT = MODE == 1 ? a.I / 128 : (a.H + BN - 1) / BN;
-  const long total = (long)__ldg(p.rb.mtp + a.E) * NBT;
+  const long total = (long)mtp_s[E] * NBT;
 
   if (warp == 0) {
     // -------------------------------------------------- TMA producer
     if (lane == 0) {
-      const uint64_t pol_a = l2_policy_evict_last();
-      const uint64_t pol_b = l2_policy_evict_last();
-      long it = 0;
+      const uint64_t pol = l2_policy_evict_last();
+      long n_main = 0, n_sc = 0;   // stage / scale-ring loads issued
       bool ok = true;
       // L2 prefetch runs PD K blocks ahead of the shared-memory loads (across
       // tile boundaries), so the stage loads find their tiles in L2.
       constexpr int PD = 8;
       long pt = blockIdx.x;
-      int pkb = 0;
-      Tile ptl = pt < total ? tile_of(p, pt, NBT) : Tile{0, 0, 0, 0};
+      int pkb = 0, pmi = 0, pnb = 0, pe = 0;
+      auto pset = [&]() {
+        if (pt < total) {
+          pmi = (int)(pt / NBT);
+          pnb = (int)(pt % NBT);
+          pe = expert_of_tile(mtp_s, E, pmi);
+        }
+      };
       auto prefetch_next = [&]() {
         if (pt >= total) return;
-        tc::tma_prefetch_2d(&tmA, pkb * BK, ptl.p0);
+        tc::tma_prefetch_2d(&m.a, pkb * BK, pmi * BM);
         if (MODE == 1) {
-          const int r0 = ptl.e * 2 * a.I + ptl.nb * 128;
-          tc::tma_prefetch_2d(&tmB, pkb * BK, r0);
-          tc::tma_prefetch_2d(&tmB, pkb * BK, r0 + a.I);
+          const int r0 = pe * 2 * a.I + pnb * 128;
+          tc::tma_prefetch_2d(&m.b, pkb * BK, r0);
+          tc::tma_prefetch_2d(&m.b, pkb * BK, r0 + a.I);
         } else {
-          tc::tma_prefetch_2d(&tmB, pkb * BK, ptl.e * a.H + ptl.nb * BN);
+          tc::tma_prefetch_2d(&m.b, pkb * BK, pe * a.H + pnb * BN);
         }
         if (++pkb == nkb) {
           pkb = 0;
           pt += gridDim.x;
-          if (pt < total) ptl = tile_of(p, pt, NBT);
+          pset();
         }
       };
+      pset();
       for (int i = 0; i < PD; ++i) prefetch_next();
       for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = tile_of(p, t, NBT);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int mi = (int)(t / NBT), nb = (int)(t % NBT);
+        const int e = expert_of_tile(mtp_s, E, mi);
+        const int p0 = mi * BM;
+        for (int kb = 0; kb < nkb; ++kb) {
           prefetch_next();
-          const int s = (int)(it % NS);
-          if (it >= NS && !mbar_wait(&empty[s], (uint32_t)((it / NS) - 1) & 1)) {
+          const int s = (int)(n_main % ns);
+          if (n_main >= ns && !mbar_wait(&empty[s], (uint32_t)((n_main / ns) - 1) & 1)) {
             ok = false;
             break;
           }
           uint8_t* st = base + s * STAGE;
           mbar_arrive_expect_tx(&full[s], STAGE);
-          tc::tma_load_2d(st, &tmA, kb * BK, tl.p0, &full[s], pol_a);
+          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[s], pol);
           if (MODE == 1) {
-            const int r0 = tl.e * 2 * a.I + tl.nb * 128;
-            tc::tma_load_2d(st + A_BYTES, &tmB, kb * BK, r0, &full[s], pol_b);
-            tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &tmB, kb * BK, r0 + a.I, &full[s], pol_b);
+            const int r0 = e * 2 * a.I + nb * 128;
+            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, r0, &full[s], pol);
+            tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, r0 + a.I, &full[s], pol);
           } else {
-            tc::tma_load_2d(st + A_BYTES, &tmB, kb * BK, tl.e * a.H + tl.nb * BN, &full[s], pol_b);
+            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, e * a.H + nb * BN, &full[s], pol);
           }
+          ++n_main;
+          const int q = (int)(n_sc % NSS);
+          if (n_sc >= NSS && !mbar_wait(&sempty[q], (uint32_t)((n_sc / NSS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sfull[q], 512 + 16);
+          tc::tma_load_2d(ring_a + q * 128, &m.sa, p0, kb, &sfull[q], pol);
+          tc::tma_load_2d(ring_w + q * 32, &m.sw, 4 * nb, e * nkb + kb, &sfull[q], pol);
+          ++n_sc;
         }
         if (*(volatile int*)&abort_flag) ok = false;
       }
       if (!ok) {
         abort_flag = 1;
         raise_status(p.status, MOE_STATUS_TIMEOUT);
-        for (long i = it > NS ? it - NS : 0; i < it; ++i) mbar_wait(&full[i % NS], (uint32_t)(i / NS) & 1);
+        // let the copies already issued land before the CTA goes away
+        for (long i = n_main > ns ? n_main - ns : 0; i < n_main; ++i)
+          mbar_wait(&full[i % ns], (uint32_t)(i / ns) & 1);
+        for (long i = n_sc > NSS ? n_sc - NSS : 0; i < n_sc; ++i)
+          mbar_wait(&sfull[i % NSS], (uint32_t)(i / NSS) & 1);
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
-      long it = 0, j = 0;
+      long it = 0;
       bool ok = true;
       for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb, ++it, ++j) {
-          const int s = (int)(it % NS);
-          const int buf = (int)(j & 1);
-          if (!mbar_wait(&full[s], (uint32_t)(it / NS) & 1) ||
-              (j >= 2 && !mbar_wait(&tempty[buf], (uint32_t)((j >> 1) - 1) & 1))) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = (int)(it % ns);
+          const int buf = (int)(it & 1);
+          if (!mbar_wait(&full[s], (uint32_t)(it / ns) & 1) ||
+              (it >= 2 && !mbar_wait(&tempty[buf], (uint32_t)((it >> 1) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -354,73 +485,62 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         raise_status(p.status, MOE_STATUS_TIMEOUT);
       }
       // the last commits must land before TMEM is released
-      if (j > 0) mbar_wait(&tfull[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1);
+      if (it > 0) mbar_wait(&tfull[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1);
     }
   } else {
     // -------------------------------------------------- epilogue warps
-    const int eq = warp & 3;                 // TMEM lane quarter of this warp
-    const int hf = (warp - 2) >> 2;          // which 64-column half of each 128-column block
+    const int ew = warp - 2;
+    const int eq = warp & 3;                 // TMEM lane quarter this warp may access
+    const int hf = ew >> 2;                  // which 64-column half of each 128-column block
     const int row = eq * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(eq * 32) << 16);
-    long j = 0;
-    int tcount = 0;
-    for (long t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-      const Tile tl = tile_of(p, t, NBT);
-      const bool rvalid = row < tl.nvalid;
-      const int pos = tl.p0 + row;
+    const bool issuer = ew == 0 && lane == 0;
+    long it = 0;
+    bool ok = true;
+    for (long t = blockIdx.x; t < total; t += gridDim.x) {
+      const int mi = (int)(t / NBT), nb = (int)(t % NBT);
+      const int p0 = mi * BM;
+      const bool has1 = MODE == 1 || nb * BN + 128 < a.H;
       float acc0[64], acc1[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
-      const uint16_t* ws0;
-      const uint16_t* ws1;
-      const float* as;
-      bool has1 = true;
-      if (MODE == 1) {
-        ws0 = a.w13s + (int64_t)tl.e * a.s13_exp + (int64_t)tl.nb * a.s13_row;
-        ws1 = a.w13s + (int64_t)tl.e * a.s13_exp + (int64_t)(a.I / 128 + tl.nb) * a.s13_row;
-        as = p.pb.xs + (int64_t)pos * (a.H / 128);
-      } else {
-        const int b0 = tl.nb * 2;
-        has1 = (b0 + 1) * 128 < a.H;
-        ws0 = a.w2s + (int64_t)tl.e * a.s2_exp + (int64_t)b0 * a.s2_row;
-        ws1 = has1 ? ws0 + a.s2_row : ws0;
-        as = p.pb.hs + (int64_t)pos * (a.I / 128);
-      }
-      bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++j) {
-        const float sa = rvalid ? __ldg(as + kb) : 0.f;
-        const float f0 = sa * bf16_to_f32(__ldg(ws0 + kb));
-        const float f1 = has1 ? sa * bf16_to_f32(__ldg(ws1 + kb)) : 0.f;
-        const int buf = (int)(j & 1);
-        if (!mbar_wait(&tfull[buf], (uint32_t)(j >> 1) & 1)) {
-          ok = false;
-          break;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        if (*(volatile int*)&abort_flag) ok = false;
+        const int q = (int)(it % NSS);
+        const int buf = (int)(it & 1);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[q], (uint32_t)(it / NSS) & 1));
+        float f0 = 0.f, f1 = 0.f;
+        if (ok) {
+          const float sa = ring_a[q * 128 + row];
+          f0 = sa * ring_w[q * 32];
+          f1 = sa * ring_w[q * 32 + 1];
         }
-        tc::fence_after_sync();
-        const uint32_t tb = trow + buf * BN + hf * 64;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[q]);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&tfull[buf], (uint32_t)(it >> 1) & 1));
+        if (ok) {
+          tc::fence_after_sync();
+          const uint32_t tb = trow + buf * BN + hf * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          tc::tmem_ld16(tb + c * 16, v);
+          for (int c = 0; c < 4; ++c) {
+            float v[16];
+            tc::tmem_ld16(tb + c * 16, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc0[c * 16 + i] = fmaf(f0, v[i], acc0[c * 16 + i]);
-        }
+            for (int i = 0; i < 16; ++i) acc0[c * 16 + i] = fmaf(f0, v[i], acc0[c * 16 + i]);
+          }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          tc::tmem_ld16(tb + 128 + c * 16, v);
+          for (int c = 0; c < 4; ++c) {
+            float v[16];
+            tc::tmem_ld16(tb + 128 + c * 16, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc1[c * 16 + i] = fmaf(f1, v[i], acc1[c * 16 + i]);
+            for (int i = 0; i < 16; ++i) acc1[c * 16 + i] = fmaf(f1, v[i], acc1[c * 16 + i]);
+          }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      if (!ok || *(volatile int*)&abort_flag) {
-        abort_flag = 1;
-        raise_status(p.status, MOE_STATUS_TIMEOUT);
-        break;
-      }
+      bool stop;
       if (MODE == 1) {
         // h = silu(gate) * up for this thread's 64 columns of the 128-block
         float amax = 0.f;
@@ -431,44 +551,71 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           acc0[i] = h;
           amax = fmaxf(amax, fabsf(h));
         }
-        // the other half of the row's 128-group sits in warp (warp +- 4)
-        const int xb = tcount & 1;
-        xch[(xb * BM + row) * 2 + hf] = amax;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&xfull[xb]);
-        if (!mbar_wait(&xfull[xb], (uint32_t)(tcount >> 1) & 1)) {
-          abort_flag = 1;
-          raise_status(p.status, MOE_STATUS_TIMEOUT);
-          break;
-        }
-        amax = fmaxf(amax, xch[(xb * BM + row) * 2 + (1 - hf)]);
+        // the other half of the row's 128-group is held by warp ew ^ 4
+        xch[row * 2 + hf] = amax;
+        if (issuer) tc::bulk_wait_read0();   // the previous tile's store has left the staging tile
+        epi_sync();
+        amax = fmaxf(amax, xch[row * 2 + (1 - hf)]);
         const float sc = __fdiv_rn(amax, 448.0f);
-        if (rvalid) {
-          uint32_t w[16];
+        uint8_t* orow = outs + row * 128;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 4; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int b = 16 * i + 4 * u;
             uint32_t c01 = 0, c23 = 0;
             if (sc != 0.f) {
-              c01 = f32x2_to_e4m3x2(__fdiv_rn(acc0[4 * i], sc), __fdiv_rn(acc0[4 * i + 1], sc));
-              c23 = f32x2_to_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sc), __fdiv_rn(acc0[4 * i + 3], sc));
+              c01 = f32x2_to_e4m3x2(__fdiv_rn(acc0[b], sc), __fdiv_rn(acc0[b + 1], sc));
+              c23 = f32x2_to_e4m3x2(__fdiv_rn(acc0[b + 2], sc), __fdiv_rn(acc0[b + 3], sc));
             }
-            w[i] = c01 | (c23 << 16);
+            w[u] = c01 | (c23 << 16);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.pb.hq + (int64_t)pos * a.I + tl.nb * 128 + hf * 64);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          if (hf == 0) p.pb.hs[(int64_t)pos * (a.I / 128) + tl.nb] = sc;
+          const int c = hf * 4 + i;
+          *reinterpret_cast<uint4*>(orow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (hf == 0) reinterpret_cast<float*>(outs + OUT1)[row] = sc;
+        tc::fence_proxy_async_smem();
+        stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
+        if (issuer && !stop) {
+          tc::tma_store_2d(&m.o, outs, nb * 128, p0);
+          tc::tma_store_2d(&m.os, outs + OUT1, p0, nb);
+          tc::bulk_commit();
         }
       } else {
-        if (rvalid) {
-          const int s = p.rb.perm[pos];
-          const float wt = a.wts[s];
-          uint16_t* dst = p.pb.slots + (int64_t)s * a.H + tl.nb * BN + hf * 64;
-          store_bf16_row64(dst, acc0, wt);
-          if (has1) store_bf16_row64(dst + 128, acc1, wt);
+        const int c0 = nb * BN;
+        if (issuer) tc::bulk_wait_read0();
+        epi_sync();
+        stage_bf16_row64(outs + hf * (OUT2 / 2), row, acc0);
+        tc::fence_proxy_async_smem();
+        stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
+        if (issuer && !stop) {
+          tc::tma_store_2d(&m.o, outs, c0, p0);
+          tc::tma_store_2d(&m.o, outs + OUT2 / 2, c0 + 64, p0);
+          tc::bulk_commit();
+        }
+        if (has1 && !stop) {
+          if (issuer) tc::bulk_wait_read0();
+          epi_sync();
+          stage_bf16_row64(outs + hf * (OUT2 / 2), row, acc1);
+          tc::fence_proxy_async_smem();
+          stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
+          if (issuer && !stop) {
+            tc::tma_store_2d(&m.o, outs, c0 + 128, p0);
+            tc::tma_store_2d(&m.o, outs + OUT2 / 2, c0 + 192, p0);
+            tc::bulk_commit();
+          }
         }
       }
+      if (stop) {
+        if (lane == 0) {
+          abort_flag = 1;
+          raise_status(p.status, MOE_STATUS_TIMEOUT);
+        }
+        break;
+      }
     }
+    if (issuer) tc::bulk_wait0();
   }
   // ---------------------------------------------------------- teardown
   tc::fence_before_sync();
@@ -488,14 +635,15 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillArgs p) {
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < a.k; ++j) {
     const int s = t * a.k + j;
-    const int id = a.ids[s];
-    if (id < 0 || id >= a.E) continue;
-    const uint4 v = *reinterpret_cast<const uint4*>(p.pb.slots + (int64_t)s * a.H + n);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int row = p.pb.pinv[s];
+    if (row < 0) continue;
+    const float w = a.wts[s];
+    const uint4 v = *reinterpret_cast<const uint4*>(p.pb.ys + (int64_t)row * a.H + n);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += bf16_to_f32(w[i] & 0xFFFFu);
-      acc[2 * i + 1] += bf16_to_f32(w[i] >> 16);
+      acc[2 * i] = fmaf(w, bf16_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, bf16_to_f32(u[i] >> 16), acc[2 * i + 1]);
     }
   }
   uint32_t o[4];
@@ -522,18 +670,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major uint8 matrix [rows, cols] (row pitch = cols bytes), boxes of
-// 128 bytes x box_rows, 128-byte swizzle; rows past the end read as zero.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major 2-D tensor [rows, cols] of `esize`-byte elements, rows `pitch`
+// bytes apart, copied in boxes of box_cols x box_rows; parts of a box
+// outside the tensor read as zero and are not written by stores.
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t rows,
+                     uint64_t cols, uint64_t pitch, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
+  (void)esize;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename Kern, typename... Args>
@@ -552,22 +703,50 @@ static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Stages that fit in shared memory for this GEMM (0 if even two do not).
+static int pick_stages(int mode, int E) {
+  for (int ns = 4; ns >= 2; --ns)
+    if (pf_layout(mode, ns, E).total <= (uint32_t)pf::kSmemMax) return ns;
+  return 0;
+}
+
+int64_t prefill_rows(int64_t S, int E) {
+  const int64_t g = S < E ? S : E;
+  const int64_t r = (S + 127 * g + 127) / 128 * 128;
+  return r > 128 ? r : 128;
+}
+
 cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, int32_t* route_scratch,
                            uint32_t* status, int device, cudaStream_t st, int* launches) {
   PrefillArgs p{a, rb, pb, status};
-  CUtensorMap mx, m13, mh, m2;
-  if (!make_map(&mx, pb.xq, (uint64_t)a.S, (uint64_t)a.H, 128) ||
-      !make_map(&m13, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 128) ||
-      !make_map(&mh, pb.hq, (uint64_t)a.S, (uint64_t)a.I, 128) ||
-      !make_map(&m2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, pf::BN))
-    return note_error(cudaErrorInvalidValue, "tensor map encode");
+  const uint64_t R = (uint64_t)pb.rows;
+  const uint64_t np1 = a.I / 128, nk1 = a.H / 128, np2 = (a.H + 255) / 256, nk2 = a.I / 128;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                            BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  PfMaps g1, g2;
+  bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
+            make_map(&g1.b, U8, 1, a.w13, (uint64_t)a.E * 2 * a.I, a.H, a.H, 128, 128, true) &&
+            make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, 1, false) &&
+            make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, 1, false) &&
+            make_map(&g1.o, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true) &&
+            make_map(&g1.os, F32, 4, pb.hsT, nk2, R, 4 * R, 128, 1, false);
+  ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN, true) &&
+       make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, 1, false) &&
+       make_map(&g2.o, BF, 2, pb.ys, R, a.H, 2 * (uint64_t)a.H, 64, 128, true);
+  if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
+  g2.a = g1.o;
+  g2.sa = g1.os;
+  g2.os = g2.o;
+  const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
+  if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
+  const int sm1 = (int)pf_layout(1, ns1, a.E).total, sm2 = (int)pf_layout(2, ns2, a.E).total;
   cudaError_t err;
   if ((err = note_error(
-           cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM),
+           cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1),
            "prefill_gemm1 smem attribute")))
     return err;
   if ((err = note_error(
-           cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM),
+           cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2),
            "prefill_gemm2 smem attribute")))
     return err;
   const int sms = num_sms(device);
@@ -578,18 +757,21 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
     return err;
   stage_mark(st, 1);
   const int64_t warps = (int64_t)a.T * ((a.H / 128 + 3) / 4);
-  if ((err = launch_check(launch_ex(act_quant_permute_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st,
-                                    pdl, p),
+  const int qblocks = (int)((warps + 7) / 8);
+  const int64_t nrep = (int64_t)a.E * (nk1 * np1 + nk2 * np2);
+  const int rblocks = (int)((nrep + 255) / 256);
+  if ((err = launch_check(launch_ex(act_quant_permute_kernel, dim3((unsigned)(qblocks + rblocks)), dim3(256), 0,
+                                    st, pdl, p, qblocks),
                           st, "act_quant_permute")))
     return err;
   stage_mark(st, 2);
-  if ((err = launch_check(launch_ex(prefill_gemm_kernel<1>, dim3(sms), dim3(pf::THREADS), pf::SMEM, st, pdl, mx,
-                                    m13, p),
+  if ((err = launch_check(launch_ex(prefill_gemm_kernel<1>, dim3(sms), dim3(pf::THREADS), (size_t)sm1, st, pdl,
+                                    g1, p, ns1),
                           st, "prefill_gemm1")))
     return err;
   stage_mark(st, 3);
-  if ((err = launch_check(launch_ex(prefill_gemm_kernel<2>, dim3(sms), dim3(pf::THREADS), pf::SMEM, st, pdl, mh,
-                                    m2, p),
+  if ((err = launch_check(launch_ex(prefill_gemm_kernel<2>, dim3(sms), dim3(pf::THREADS), (size_t)sm2, st, pdl,
+                                    g2, p, ns2),
                           st, "prefill_gemm2")))
     return err;
   stage_mark(st, 4);
