@@ -223,7 +223,13 @@ constexpr int BK = 128;            // K block (bytes = e4m3 elements)
 constexpr int A_BYTES = BM * BK;   // 16 KiB
 constexpr int B_BYTES = BN * BK;   // 32 KiB
 constexpr int STAGE = A_BYTES + B_BYTES;
-constexpr int NSS = 8;             // scale-ring entries (>= stages + 2 accumulators)
+constexpr int KG = 4;              // K blocks per scale group (one scale-ring entry)
+constexpr int NSG = 6;             // scale-ring entries
+constexpr int LEAD_G = 3;          // groups the scale loads run ahead of the operand loads
+                                   // (NSG - LEAD_G >= 3: the epilogue is never more than
+                                   // 2 accumulators + 4 stages, i.e. under 3 groups, behind)
+constexpr int SA_BYTES = BM * KG * 4;   // activation scales of one group: [KG][BM] fp32
+constexpr int SW_BYTES = KG * 16;       // weight scale records of one group: [KG][4] fp32
 constexpr int NEPI = 8;            // epilogue warps (two per TMEM lane quarter)
 constexpr int THREADS = 32 * (2 + NEPI);
 constexpr int OUT1 = BM * 128;     // GEMM1 staging: 128 rows x 128 h codes (+ 128 fp32 scales)
@@ -234,6 +240,7 @@ constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 
 // Shared-memory layout of prefill_gemm_kernel<mode> with ns stages (byte
 // offsets from a 1024-aligned base; the same function on host and device).
+// Every tensor-copy destination or source is 128-byte aligned.
 struct PfLayout {
   uint32_t out, ring_a, ring_w, xch, bars, mtp, total;
 };
@@ -244,13 +251,13 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   L.out = o;
   o += mode == 1 ? pf::OUT1 + 512 : pf::OUT2;
   L.ring_a = o;
-  o += pf::NSS * 512;
+  o += pf::NSG * pf::SA_BYTES;
   L.ring_w = o;
-  o += pf::NSS * 128;   // 16 bytes used per entry; tensor copies into shared memory need 128-byte alignment
+  o += pf::NSG * 128;
   L.xch = o;
   o += pf::BM * 2 * 4;
   L.bars = o;
-  o += (2 * ns + 2 * pf::NSS + 4) * 8 + 16;
+  o += (2 * ns + 2 * pf::NSG + 4) * 8 + 16;
   o = (o + 15u) & ~15u;
   L.mtp = o;
   o += 4u * (uint32_t)(E + 1);
@@ -258,8 +265,9 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   return L;
 }
 
-// The tensor maps one GEMM uses: A rows, B rows, A scales (K-block major),
-// B scale records, and the output(s).
+// The tensor maps one GEMM uses: A rows, B rows (GEMM1: 3-D view of w13 so
+// one load brings a gate block and the matching up block), A scales (K-block
+// major), B scale records, and the output(s).
 struct PfMaps {
   CUtensorMap a, b, sa, sw, o, os;
 };
@@ -308,10 +316,24 @@ __device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const fl
   }
 }
 
+// Position in a ring of n entries: index and phase parity, advanced by one.
+struct RingPos {
+  int i = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 // MODE 1: gate/up projection, silu(gate)*up, e4m3 h codes + scales.
 // MODE 2: down projection -> bf16 y rows.
 // 10 warps: warp 0 issues tensor-map loads, warp 1 owns TMEM and issues the
-// MMAs, warps 2..9 promote, finish and store.
+// MMAs, warps 2..9 promote, finish and store.  Each CTA takes tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ...; tile t = (128-row tile t / NBT,
+// column block t % NBT).
 template <int MODE>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ PfMaps m, PrefillArgs p, int ns) {
@@ -324,8 +346,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);
   uint64_t* empty = full + ns;
   uint64_t* sfull = empty + ns;
-  uint64_t* sempty = sfull + NSS;
-  uint64_t* tfull = sempty + NSS;
+  uint64_t* sempty = sfull + NSG;
+  uint64_t* tfull = sempty + NSG;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   float* ring_a = reinterpret_cast<float*>(base + L.ring_a);
@@ -341,7 +363,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < NSS; ++i) {
+    for (int i = 0; i < NSG; ++i) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sempty[i], NEPI);
     }
@@ -371,76 +393,57 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
   const int K = MODE == 1 ? a.H : a.I;
   const int nkb = K / BK;
+  const int ngpt = (nkb + KG - 1) / KG;   // scale groups per tile
   const int NBT = MODE == 1 ? a.I / 128 : (a.H + BN - 1) / BN;
-  const long total = (long)mtp_s[E] * NBT;
+  const int total = mtp_s[E] * NBT;
+  const int bx = blockIdx.x, gx = gridDim.x;
 
   if (warp == 0) {
     // -------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
-      long n_main = 0, n_sc = 0;   // stage / scale-ring loads issued
+      const int my_tiles = total > bx ? (total - bx + gx - 1) / gx : 0;
+      const int n_groups = my_tiles * ngpt;
+      int n_main = 0, n_g = 0;          // operand stages / scale groups issued
+      RingPos sp, gp;
       bool ok = true;
-      // L2 prefetch runs PD K blocks ahead of the shared-memory loads (across
-      // tile boundaries), so the stage loads find their tiles in L2.
-      constexpr int PD = 8;
-      long pt = blockIdx.x;
-      int pkb = 0, pmi = 0, pnb = 0, pe = 0;
-      auto pset = [&]() {
-        if (pt < total) {
-          pmi = (int)(pt / NBT);
-          pnb = (int)(pt % NBT);
-          pe = expert_of_tile(mtp_s, E, pmi);
+      // scale group g of this CTA: tile g / ngpt of its list, K blocks
+      // KG * (g % ngpt) ... ; issued up to LEAD_G groups ahead
+      auto issue_groups = [&](int upto) -> bool {
+        if (upto > n_groups) upto = n_groups;
+        for (; n_g < upto; ++n_g, gp.next(NSG)) {
+          if (n_g >= NSG && !mbar_wait(&sempty[gp.i], gp.ph ^ 1u)) return false;
+          const int ti = n_g / ngpt, g = n_g - ti * ngpt;
+          const int t = bx + ti * gx;
+          const int mi = t / NBT, nb = t - mi * NBT;
+          const int e = expert_of_tile(mtp_s, E, mi);
+          mbar_arrive_expect_tx(&sfull[gp.i], SA_BYTES + SW_BYTES);
+          tc::tma_load_2d(ring_a + gp.i * (SA_BYTES / 4), &m.sa, mi * BM, g * KG, &sfull[gp.i], pol);
+          tc::tma_load_2d(ring_w + gp.i * 32, &m.sw, 4 * nb, e * nkb + g * KG, &sfull[gp.i], pol);
         }
+        return true;
       };
-      auto prefetch_next = [&]() {
-        if (pt >= total) return;
-        tc::tma_prefetch_2d(&m.a, pkb * BK, pmi * BM);
-        if (MODE == 1) {
-          const int r0 = pe * 2 * a.I + pnb * 128;
-          tc::tma_prefetch_2d(&m.b, pkb * BK, r0);
-          tc::tma_prefetch_2d(&m.b, pkb * BK, r0 + a.I);
-        } else {
-          tc::tma_prefetch_2d(&m.b, pkb * BK, pe * a.H + pnb * BN);
-        }
-        if (++pkb == nkb) {
-          pkb = 0;
-          pt += gridDim.x;
-          pset();
-        }
-      };
-      pset();
-      for (int i = 0; i < PD; ++i) prefetch_next();
-      for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int mi = (int)(t / NBT), nb = (int)(t % NBT);
+      int ti = 0;
+      for (int t = bx; t < total && ok; t += gx, ++ti) {
+        const int mi = t / NBT, nb = t - mi * NBT;
         const int e = expert_of_tile(mtp_s, E, mi);
         const int p0 = mi * BM;
-        for (int kb = 0; kb < nkb; ++kb) {
-          prefetch_next();
-          const int s = (int)(n_main % ns);
-          if (n_main >= ns && !mbar_wait(&empty[s], (uint32_t)((n_main / ns) - 1) & 1)) {
+        for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(ns)) {
+          if (!issue_groups(ti * ngpt + kb / KG + 1 + LEAD_G)) {
             ok = false;
             break;
           }
-          uint8_t* st = base + s * STAGE;
-          mbar_arrive_expect_tx(&full[s], STAGE);
-          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[s], pol);
-          if (MODE == 1) {
-            const int r0 = e * 2 * a.I + nb * 128;
-            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, r0, &full[s], pol);
-            tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, r0 + a.I, &full[s], pol);
-          } else {
-            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, e * a.H + nb * BN, &full[s], pol);
-          }
-          ++n_main;
-          const int q = (int)(n_sc % NSS);
-          if (n_sc >= NSS && !mbar_wait(&sempty[q], (uint32_t)((n_sc / NSS) - 1) & 1)) {
+          if (n_main >= ns && !mbar_wait(&empty[sp.i], sp.ph ^ 1u)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sfull[q], 512 + 16);
-          tc::tma_load_2d(ring_a + q * 128, &m.sa, p0, kb, &sfull[q], pol);
-          tc::tma_load_2d(ring_w + q * 32, &m.sw, 4 * nb, e * nkb + kb, &sfull[q], pol);
-          ++n_sc;
+          uint8_t* st = base + sp.i * STAGE;
+          mbar_arrive_expect_tx(&full[sp.i], STAGE);
+          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
+          if (MODE == 1)
+            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, nb * 128, 2 * e, &full[sp.i], pol);
+          else
+            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, e * a.H + nb * BN, &full[sp.i], pol);
         }
         if (*(volatile int*)&abort_flag) ok = false;
       }
@@ -448,34 +451,33 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         abort_flag = 1;
         raise_status(p.status, MOE_STATUS_TIMEOUT);
         // let the copies already issued land before the CTA goes away
-        for (long i = n_main > ns ? n_main - ns : 0; i < n_main; ++i)
+        for (int i = n_main > ns ? n_main - ns : 0; i < n_main; ++i)
           mbar_wait(&full[i % ns], (uint32_t)(i / ns) & 1);
-        for (long i = n_sc > NSS ? n_sc - NSS : 0; i < n_sc; ++i)
-          mbar_wait(&sfull[i % NSS], (uint32_t)(i / NSS) & 1);
+        for (int i = n_g > NSG ? n_g - NSG : 0; i < n_g; ++i) mbar_wait(&sfull[i % NSG], (uint32_t)(i / NSG) & 1);
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
-      long it = 0;
+      int it = 0;
+      RingPos sp;
       bool ok = true;
-      for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = (int)(it % ns);
-          const int buf = (int)(it & 1);
-          if (!mbar_wait(&full[s], (uint32_t)(it / ns) & 1) ||
+      for (int t = bx; t < total && ok; t += gx) {
+        for (int kb = 0; kb < nkb; ++kb, ++it, sp.next(ns)) {
+          const int buf = it & 1;
+          if (!mbar_wait(&full[sp.i], sp.ph) ||
               (it >= 2 && !mbar_wait(&tempty[buf], (uint32_t)((it >> 1) - 1) & 1))) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint8_t* st = base + s * STAGE;
+          const uint8_t* st = base + sp.i * STAGE;
           const uint32_t d = tmem + buf * BN;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             tc::mma_f8(d, tc::sw128_desc(st + k * 32), tc::sw128_desc(st + A_BYTES + k * 32), idesc, k > 0);
-          tc::commit(&empty[s]);
+          tc::commit(&empty[sp.i]);
           tc::commit(&tfull[buf]);
         }
         if (*(volatile int*)&abort_flag) ok = false;
@@ -495,10 +497,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int row = eq * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(eq * 32) << 16);
     const bool issuer = ew == 0 && lane == 0;
-    long it = 0;
+    int it = 0;
+    RingPos gp;
     bool ok = true;
-    for (long t = blockIdx.x; t < total; t += gridDim.x) {
-      const int mi = (int)(t / NBT), nb = (int)(t % NBT);
+    for (int t = bx; t < total; t += gx) {
+      const int mi = t / NBT, nb = t - mi * NBT;
       const int p0 = mi * BM;
       const bool has1 = MODE == 1 || nb * BN + 128 < a.H;
       float acc0[64], acc1[64];
@@ -506,34 +509,33 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         if (*(volatile int*)&abort_flag) ok = false;
-        const int q = (int)(it % NSS);
-        const int buf = (int)(it & 1);
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[q], (uint32_t)(it / NSS) & 1));
+        const int sub = kb % KG;
+        const int buf = it & 1;
+        if (sub == 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[gp.i], gp.ph));
         float f0 = 0.f, f1 = 0.f;
         if (ok) {
-          const float sa = ring_a[q * 128 + row];
-          f0 = sa * ring_w[q * 32];
-          f1 = sa * ring_w[q * 32 + 1];
+          const float sa = ring_a[gp.i * (SA_BYTES / 4) + sub * BM + row];
+          f0 = sa * ring_w[gp.i * 32 + sub * 4];
+          f1 = sa * ring_w[gp.i * 32 + sub * 4 + 1];
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[q]);
+        if (sub == KG - 1 || kb == nkb - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[gp.i]);
+          gp.next(NSG);
+        }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(&tfull[buf], (uint32_t)(it >> 1) & 1));
         if (ok) {
           tc::fence_after_sync();
           const uint32_t tb = trow + buf * BN + hf * 64;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float v[16];
-            tc::tmem_ld16(tb + c * 16, v);
+            float v0[16], v1[16];
+            tc::tmem_ld16x2(tb + c * 16, tb + 128 + c * 16, v0, v1);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc0[c * 16 + i] = fmaf(f0, v[i], acc0[c * 16 + i]);
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[16];
-            tc::tmem_ld16(tb + 128 + c * 16, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc1[c * 16 + i] = fmaf(f1, v[i], acc1[c * 16 + i]);
+            for (int i = 0; i < 16; ++i) {
+              acc0[c * 16 + i] = fmaf(f0, v0[i], acc0[c * 16 + i]);
+              acc1[c * 16 + i] = fmaf(f1, v1[i], acc1[c * 16 + i]);
+            }
           }
         }
         tc::fence_before_sync();
@@ -542,12 +544,18 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       bool stop;
       if (MODE == 1) {
-        // h = silu(gate) * up for this thread's 64 columns of the 128-block
+        // h = silu(gate) * up for this thread's 64 columns of the 128-block.
+        // silu(g) = g / (1 + e^-g) with the fast exponential and division:
+        // an IEEE division here takes its slow path whenever e^-g overflows
+        // (every strongly negative gate value), which made this loop cost
+        // more than the whole K loop of a tile.  h feeds a quantiser, and
+        // both approximations are within a few fp32 ulps (a denominator
+        // past 2^126 gives 0, the limit silu takes there anyway).
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const float g = acc0[i];
-          const float h = g / (1.0f + expf(-g)) * acc1[i];
+          const float h = __fdividef(g, 1.0f + __expf(-g)) * acc1[i];
           acc0[i] = h;
           amax = fmaxf(amax, fabsf(h));
         }
@@ -557,6 +565,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         epi_sync();
         amax = fmaxf(amax, xch[row * 2 + (1 - hf)]);
         const float sc = __fdiv_rn(amax, 448.0f);
+        // code = e4m3(h * (1 / scale)): one IEEE reciprocal per group instead
+        // of a division per value
+        const float inv = sc != 0.f ? __frcp_rn(sc) : 0.f;
         uint8_t* orow = outs + row * 128;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -564,11 +575,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int b = 16 * i + 4 * u;
-            uint32_t c01 = 0, c23 = 0;
-            if (sc != 0.f) {
-              c01 = f32x2_to_e4m3x2(__fdiv_rn(acc0[b], sc), __fdiv_rn(acc0[b + 1], sc));
-              c23 = f32x2_to_e4m3x2(__fdiv_rn(acc0[b + 2], sc), __fdiv_rn(acc0[b + 3], sc));
-            }
+            const uint32_t c01 = f32x2_to_e4m3x2(acc0[b] * inv, acc0[b + 1] * inv);
+            const uint32_t c23 = f32x2_to_e4m3x2(acc0[b + 2] * inv, acc0[b + 3] * inv);
             w[u] = c01 | (c23 << 16);
           }
           const int c = hf * 4 + i;
@@ -687,6 +695,21 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, con
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// w13 [E, 2I, H] viewed as [2E][I][H] (x = K byte, y = row within a gate or
+// up half, z = 2e for gate, 2e + 1 for up): a box of 128 x 128 x 2 brings a
+// gate block and the matching up block in one copy, gate rows first.
+static bool make_map_w13(CUtensorMap* m, const void* base, int E, int I, int H) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)I, 2 * (cuuint64_t)E};
+  const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)I * H};
+  const cuuint32_t box[3] = {128, 128, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Kern, typename... Args>
 static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                              Args... args) {
@@ -725,17 +748,17 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                             BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
-            make_map(&g1.b, U8, 1, a.w13, (uint64_t)a.E * 2 * a.I, a.H, a.H, 128, 128, true) &&
-            make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, 1, false) &&
-            make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, 1, false) &&
+            make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
+            make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, pf::KG, false) &&
+            make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
             make_map(&g1.o, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true) &&
             make_map(&g1.os, F32, 4, pb.hsT, nk2, R, 4 * R, 128, 1, false);
   ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN, true) &&
-       make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, 1, false) &&
+       make_map(&g2.sa, F32, 4, pb.hsT, nk2, R, 4 * R, 128, pf::KG, false) &&
+       make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
        make_map(&g2.o, BF, 2, pb.ys, R, a.H, 2 * (uint64_t)a.H, 64, 128, true);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.a = g1.o;
-  g2.sa = g1.os;
   g2.os = g2.o;
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
