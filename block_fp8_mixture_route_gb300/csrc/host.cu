@@ -34,7 +34,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Byte layout of one workspace.
 struct Layout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, rcnt;
+  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, mtp2, rcnt;
   size_t xh, xexp, h, ybuf;                       // decode
   size_t xq, xs, hq, hs, ys, pinv, wsc13, wsc2;  // prefill
   int64_t prows;
@@ -61,6 +61,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   L.nd = take(16);
   L.meta = take(16 * (size_t)(g > 0 ? g : 1));
   L.mtp = take(4 * (size_t)(E + 1));
+  L.mtp2 = take(4 * (size_t)(E + 1));
   L.rcnt = take(4 * (size_t)route_chunks((int)S) * (size_t)E);
   if (path == MOE_PATH_DECODE) {
     L.xh = take(2 * (size_t)(T * H));
@@ -292,6 +293,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
   rb.nd = reinterpret_cast<int32_t*>(w + L.nd);
   rb.meta = reinterpret_cast<int4*>(w + L.meta);
   rb.mtp = reinterpret_cast<int32_t*>(w + L.mtp);
+  rb.mtp2 = reinterpret_cast<int32_t*>(w + L.mtp2);
   (void)hostio;
   int path = force;
   if (path == MOE_PATH_NONE)

@@ -34,9 +34,11 @@ struct RouteBufs {
   int32_t* inv;       // [S]
   int32_t* glist;     // [min(E,S)]
   int32_t* nd;        // [1]
-  int4* meta;         // [min(E,S)]: {expert, first routed position, slot count, 0} per distinct expert
-                      // (optional: may be null)
-  int32_t* mtp;       // [E+1]: exclusive prefix of ceil(count/128) per expert (optional)
+  int4* meta = nullptr;     // [min(E,S)]: {expert, first routed position, slot count, 0} per
+                            // distinct expert (optional)
+  int32_t* mtp = nullptr;   // [E+1]: exclusive prefix of ceil(count/128) per expert (optional)
+  int32_t* mtp2 = nullptr;  // [E+1]: exclusive prefix of ceil(ceil(count/128)/2), the pairs of
+                            // 128-row tiles per expert (optional)
 };
 
 // Scratch of the decode path.

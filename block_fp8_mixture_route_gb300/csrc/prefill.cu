@@ -233,7 +233,7 @@ constexpr int SW_BYTES = KG * 16;       // weight scale records of one group: [K
 constexpr int NEPI = 8;            // epilogue warps (two per TMEM lane quarter)
 constexpr int THREADS = 32 * (2 + NEPI);
 constexpr int OUT1 = BM * 128;     // GEMM1 staging: 128 rows x 128 h codes (+ 128 fp32 scales)
-constexpr int OUT2 = BM * 128 * 2; // GEMM2 staging: 128 rows x 128 bf16, as two 64-column boxes
+constexpr int OUT2 = BM * 256 * 2; // GEMM2 staging: 128 rows x 256 bf16, four 64-column quarters
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 }  // namespace pf
@@ -242,7 +242,7 @@ constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 // offsets from a 1024-aligned base; the same function on host and device).
 // Every tensor-copy destination or source is 128-byte aligned.
 struct PfLayout {
-  uint32_t out, ring_a, ring_w, xch, bars, mtp, total;
+  uint32_t out, ring_a, ring_w, xch, bars, mtp, mtp2, total;
 };
 
 __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
@@ -260,6 +260,8 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   o += (2 * ns + 2 * pf::NSG + 4) * 8 + 16;
   o = (o + 15u) & ~15u;
   L.mtp = o;
+  o += 4u * (uint32_t)(E + 1);
+  L.mtp2 = o;
   o += 4u * (uint32_t)(E + 1);
   L.total = o + 1024;   // slack for aligning the dynamic shared memory base
   return L;
@@ -300,20 +302,61 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
   return r != 0;
 }
 
-// 64 fp32 values -> bf16 (RNE) into one 128-byte row of a 128-byte-swizzled
-// staging box (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
-__device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const float (&v)[64]) {
+// Two fp32 values in one 64-bit register (the first in the low half): the
+// operand form of the paired fp32 instructions.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// acc = ff * {x0, x1} + acc on both halves with one paired FMA (each half
+// rounded as fmaf would).
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t ff, uint32_t x0, uint32_t x1) {
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%2, %3};\n\tfma.rn.f32x2 %0, %1, t, %0;\n\t}"
+      : "+l"(acc)
+      : "l"(ff), "r"(x0), "r"(x1));
+}
+
+// 64 fp32 values (32 pairs) -> bf16 (RNE) into one 128-byte row of a
+// 128-byte-swizzled staging box (16-byte chunk c of row r sits at chunk
+// c ^ (r & 7)).
+__device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const uint64_t (&v)[32]) {
   uint8_t* r = box + row * 128;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * c + 2 * q], v[8 * c + 2 * q + 1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f2lo(v[4 * c + q]), f2hi(v[4 * c + q]));
       w[q] = *reinterpret_cast<uint32_t*>(&b);
     }
     *reinterpret_cast<uint4*>(r + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// A tile of a CTA pair: the two CTAs of a cluster take M tiles 2j and 2j+1
+// of the same expert and the same column block nb, so they share the B
+// operand (each loads one half and multicasts it to both).  When the expert
+// has an odd number of M tiles, the second CTA's last tile is a phantom: it
+// loads and multiplies like a real one but stores nothing.
+struct PairTile {
+  int mi, nb, e;
+  bool real;
+};
+
+__device__ __forceinline__ PairTile pair_tile(const int* mtp, const int* mtp2, int E, int NBT, int pt,
+                                              uint32_t rank) {
+  PairTile r;
+  const int mp = pt / NBT;
+  r.nb = pt - mp * NBT;
+  r.e = expert_of_tile(mtp2, E, mp);
+  const int j = 2 * (mp - mtp2[r.e]) + (int)rank;
+  r.mi = mtp[r.e] + j;
+  r.real = j < mtp[r.e + 1] - mtp[r.e];
+  return r;
 }
 
 // Position in a ring of n entries: index and phase parity, advanced by one.
@@ -330,10 +373,14 @@ struct RingPos {
 
 // MODE 1: gate/up projection, silu(gate)*up, e4m3 h codes + scales.
 // MODE 2: down projection -> bf16 y rows.
-// 10 warps: warp 0 issues tensor-map loads, warp 1 owns TMEM and issues the
-// MMAs, warps 2..9 promote, finish and store.  Each CTA takes tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ...; tile t = (128-row tile t / NBT,
-// column block t % NBT).
+// Launched in clusters of two CTAs.  10 warps per CTA: warp 0 issues
+// tensor-map loads, warp 1 owns TMEM and issues the MMAs, warps 2..9
+// promote, finish and store.  Cluster c takes pair tiles c, c + clusters,
+// ...; pair tile pt = (tile pair pt / NBT, column block pt % NBT).
+// A stage holds this CTA's A rows and both halves of B: its own half and
+// the peer's, written by the peer's multicast.  So a stage is free again
+// only when both CTAs' MMAs have read it: each MMA commit arrives on the
+// empty barrier of both CTAs, which therefore count two arrivals.
 template <int MODE>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ PfMaps m, PrefillArgs p, int ns) {
@@ -354,6 +401,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   float* ring_w = reinterpret_cast<float*>(base + L.ring_w);
   float* xch = reinterpret_cast<float*>(base + L.xch);
   int* mtp_s = reinterpret_cast<int*>(base + L.mtp);
+  int* mtp2_s = reinterpret_cast<int*>(base + L.mtp2);
+  const uint32_t rank = tc::cluster_ctarank();
+  constexpr uint16_t kPair = 0x3;
   uint8_t* outs = base + L.out;
   __shared__ int abort_flag;
 
@@ -361,7 +411,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < ns; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 2);
     }
     for (int i = 0; i < NSG; ++i) {
       mbar_init(&sfull[i], 1);
@@ -383,10 +433,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::tmem_relinquish();
   }
   pdl_wait();
-  // the tile table, read once before any tensor-map traffic starts
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) mtp_s[i] = __ldg(p.rb.mtp + i);
+  // the tile tables, read once before any tensor-map traffic starts
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    mtp_s[i] = __ldg(p.rb.mtp + i);
+    mtp2_s[i] = __ldg(p.rb.mtp2 + i);
+  }
   tc::fence_before_sync();
   __syncthreads();
+  // both CTAs' barriers are initialised before either multicasts into the other
+  tc::cluster_sync();
   tc::fence_after_sync();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
@@ -395,8 +450,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const int nkb = K / BK;
   const int ngpt = (nkb + KG - 1) / KG;   // scale groups per tile
   const int NBT = MODE == 1 ? a.I / 128 : (a.H + BN - 1) / BN;
-  const int total = mtp_s[E] * NBT;
-  const int bx = blockIdx.x, gx = gridDim.x;
+  const int total = mtp2_s[E] * NBT;   // pair tiles
+  const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // cluster index, clusters
 
   if (warp == 0) {
     // -------------------------------------------------- TMA producer
@@ -414,20 +469,18 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         for (; n_g < upto; ++n_g, gp.next(NSG)) {
           if (n_g >= NSG && !mbar_wait(&sempty[gp.i], gp.ph ^ 1u)) return false;
           const int ti = n_g / ngpt, g = n_g - ti * ngpt;
-          const int t = bx + ti * gx;
-          const int mi = t / NBT, nb = t - mi * NBT;
-          const int e = expert_of_tile(mtp_s, E, mi);
+          const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, bx + ti * gx, rank);
           mbar_arrive_expect_tx(&sfull[gp.i], SA_BYTES + SW_BYTES);
-          tc::tma_load_2d(ring_a + gp.i * (SA_BYTES / 4), &m.sa, mi * BM, g * KG, &sfull[gp.i], pol);
-          tc::tma_load_2d(ring_w + gp.i * 32, &m.sw, 4 * nb, e * nkb + g * KG, &sfull[gp.i], pol);
+          tc::tma_load_2d(ring_a + gp.i * (SA_BYTES / 4), &m.sa, tl.mi * BM, g * KG, &sfull[gp.i], pol);
+          tc::tma_load_2d(ring_w + gp.i * 32, &m.sw, 4 * tl.nb, tl.e * nkb + g * KG, &sfull[gp.i], pol);
         }
         return true;
       };
       int ti = 0;
       for (int t = bx; t < total && ok; t += gx, ++ti) {
-        const int mi = t / NBT, nb = t - mi * NBT;
-        const int e = expert_of_tile(mtp_s, E, mi);
-        const int p0 = mi * BM;
+        const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, t, rank);
+        const int p0 = tl.mi * BM;
+        uint8_t* const bhalf = base + A_BYTES + rank * (B_BYTES / 2);   // + stage offset
         for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(ns)) {
           if (!issue_groups(ti * ngpt + kb / KG + 1 + LEAD_G)) {
             ok = false;
@@ -438,12 +491,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             break;
           }
           uint8_t* st = base + sp.i * STAGE;
+          // A of this CTA's rows, 16 KB; B: this CTA's half, 16 KB, to both CTAs;
+          // the peer's half arrives the same way: 48 KB land here in all
           mbar_arrive_expect_tx(&full[sp.i], STAGE);
           tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
-          if (MODE == 1)
-            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, nb * 128, 2 * e, &full[sp.i], pol);
-          else
-            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, e * a.H + nb * BN, &full[sp.i], pol);
+          if (MODE == 1)   // rank 0: gate block nb, rank 1: up block nb
+            tc::tma_load_3d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + (int)rank, &full[sp.i],
+                               kPair, pol);
+          else             // rank r: rows 128 r .. 128 r + 127 of the 256-row block
+            tc::tma_load_2d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128 * (int)rank,
+                               &full[sp.i], kPair, pol);
         }
         if (*(volatile int*)&abort_flag) ok = false;
       }
@@ -477,7 +534,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             tc::mma_f8(d, tc::sw128_desc(st + k * 32), tc::sw128_desc(st + A_BYTES + k * 32), idesc, k > 0);
-          tc::commit(&empty[sp.i]);
+          tc::commit_mc(&empty[sp.i], kPair);
           tc::commit(&tfull[buf]);
         }
         if (*(volatile int*)&abort_flag) ok = false;
@@ -486,8 +543,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         abort_flag = 1;
         raise_status(p.status, MOE_STATUS_TIMEOUT);
       }
-      // the last commits must land before TMEM is released
+      // the last commits must land before TMEM is released, and the peer's
+      // commits to this CTA's stage barriers before the CTA goes away
       if (it > 0) mbar_wait(&tfull[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1);
+      for (int i = it > ns ? it - ns : 0; i < it; ++i) mbar_wait(&empty[i % ns], (uint32_t)(i / ns) & 1);
     }
   } else {
     // -------------------------------------------------- epilogue warps
@@ -501,12 +560,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     RingPos gp;
     bool ok = true;
     for (int t = bx; t < total; t += gx) {
-      const int mi = t / NBT, nb = t - mi * NBT;
-      const int p0 = mi * BM;
+      const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, t, rank);
+      const int nb = tl.nb;
+      const int p0 = tl.mi * BM;
       const bool has1 = MODE == 1 || nb * BN + 128 < a.H;
-      float acc0[64], acc1[64];
+      // this thread's 64 columns of each 128-column block, as 32 pairs
+      uint64_t acc0[32], acc1[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
+      for (int i = 0; i < 32; ++i) acc0[i] = acc1[i] = 0ull;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         if (*(volatile int*)&abort_flag) ok = false;
         const int sub = kb % KG;
@@ -527,14 +588,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         if (ok) {
           tc::fence_after_sync();
           const uint32_t tb = trow + buf * BN + hf * 64;
+          const uint64_t ff0 = f2pack(f0, f0), ff1 = f2pack(f1, f1);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float v0[16], v1[16];
-            tc::tmem_ld16x2(tb + c * 16, tb + 128 + c * 16, v0, v1);
+            uint32_t r[32];
+            tc::tmem_ld16x2_raw(tb + c * 16, tb + 128 + c * 16, r);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              acc0[c * 16 + i] = fmaf(f0, v0[i], acc0[c * 16 + i]);
-              acc1[c * 16 + i] = fmaf(f1, v1[i], acc1[c * 16 + i]);
+            for (int i = 0; i < 8; ++i) {
+              ffma2(acc0[c * 8 + i], ff0, r[2 * i], r[2 * i + 1]);
+              ffma2(acc1[c * 8 + i], ff1, r[16 + 2 * i], r[16 + 2 * i + 1]);
             }
           }
         }
@@ -553,11 +615,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         // past 2^126 gives 0, the limit silu takes there anyway).
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float g = acc0[i];
-          const float h = __fdividef(g, 1.0f + __expf(-g)) * acc1[i];
-          acc0[i] = h;
-          amax = fmaxf(amax, fabsf(h));
+        for (int i = 0; i < 32; ++i) {
+          const float g0 = f2lo(acc0[i]), g1 = f2hi(acc0[i]);
+          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * f2lo(acc1[i]);
+          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * f2hi(acc1[i]);
+          acc0[i] = f2pack(h0, h1);
+          amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
         }
         // the other half of the row's 128-group is held by warp ew ^ 4
         xch[row * 2 + hf] = amax;
@@ -574,9 +637,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int b = 16 * i + 4 * u;
-            const uint32_t c01 = f32x2_to_e4m3x2(acc0[b] * inv, acc0[b + 1] * inv);
-            const uint32_t c23 = f32x2_to_e4m3x2(acc0[b + 2] * inv, acc0[b + 3] * inv);
+            const int b = 8 * i + 2 * u;   // pairs b, b + 1 = values 16 i + 4 u .. + 3
+            const uint32_t c01 = f32x2_to_e4m3x2(f2lo(acc0[b]) * inv, f2hi(acc0[b]) * inv);
+            const uint32_t c23 = f32x2_to_e4m3x2(f2lo(acc0[b + 1]) * inv, f2hi(acc0[b + 1]) * inv);
             w[u] = c01 | (c23 << 16);
           }
           const int c = hf * 4 + i;
@@ -585,34 +648,23 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         if (hf == 0) reinterpret_cast<float*>(outs + OUT1)[row] = sc;
         tc::fence_proxy_async_smem();
         stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
-        if (issuer && !stop) {
+        if (issuer && !stop && tl.real) {
           tc::tma_store_2d(&m.o, outs, nb * 128, p0);
           tc::tma_store_2d(&m.os, outs + OUT1, p0, nb);
           tc::bulk_commit();
         }
       } else {
-        const int c0 = nb * BN;
-        if (issuer) tc::bulk_wait_read0();
+        // quarter q of the staging tile = output columns nb*256 + 64 q ..,
+        // 16 KB each; one store writes all four (quarters past H are clipped)
+        if (issuer) tc::bulk_wait_read0();   // the previous tile's store has left the staging tile
         epi_sync();
-        stage_bf16_row64(outs + hf * (OUT2 / 2), row, acc0);
+        stage_bf16_row64(outs + hf * (OUT2 / 4), row, acc0);
+        if (has1) stage_bf16_row64(outs + (2 + hf) * (OUT2 / 4), row, acc1);
         tc::fence_proxy_async_smem();
         stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
-        if (issuer && !stop) {
-          tc::tma_store_2d(&m.o, outs, c0, p0);
-          tc::tma_store_2d(&m.o, outs + OUT2 / 2, c0 + 64, p0);
+        if (issuer && !stop && tl.real) {
+          tc::tma_store_3d(&m.o, outs, 0, p0, nb * 4);
           tc::bulk_commit();
-        }
-        if (has1 && !stop) {
-          if (issuer) tc::bulk_wait_read0();
-          epi_sync();
-          stage_bf16_row64(outs + hf * (OUT2 / 2), row, acc1);
-          tc::fence_proxy_async_smem();
-          stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
-          if (issuer && !stop) {
-            tc::tma_store_2d(&m.o, outs, c0 + 128, p0);
-            tc::tma_store_2d(&m.o, outs + OUT2 / 2, c0 + 192, p0);
-            tc::bulk_commit();
-          }
         }
       }
       if (stop) {
@@ -628,6 +680,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // ---------------------------------------------------------- teardown
   tc::fence_before_sync();
   __syncthreads();
+  tc::cluster_sync();   // the peer no longer writes into this CTA's shared memory
   tc::fence_after_sync();
   if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -696,18 +749,83 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, con
 }
 
 // w13 [E, 2I, H] viewed as [2E][I][H] (x = K byte, y = row within a gate or
-// up half, z = 2e for gate, 2e + 1 for up): a box of 128 x 128 x 2 brings a
-// gate block and the matching up block in one copy, gate rows first.
+// up half, z = 2e for gate, 2e + 1 for up): a box of 128 x 128 x 1 is one
+// 128-row block of expert e's gate (z = 2e) or up (z = 2e + 1) rows.
 static bool make_map_w13(CUtensorMap* m, const void* base, int E, int I, int H) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)I, 2 * (cuuint64_t)E};
   const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)I * H};
-  const cuuint32_t box[3] = {128, 128, 2};
+  const cuuint32_t box[3] = {128, 128, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ys [rows, H] bf16 viewed as [H/64][rows][64] (x = column within a 64-column
+// quarter, y = row, z = quarter): a box of 64 x 128 x 4 is 128 rows x 256
+// columns, stored from four 128-byte-swizzled 16 KB quarters.
+static bool make_map_ys(CUtensorMap* m, const void* base, uint64_t rows, int H) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, rows, (cuuint64_t)(H / 64)};
+  const cuuint64_t strides[2] = {2 * (cuuint64_t)H, 128};
+  const cuuint32_t box[3] = {64, 128, 4};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch as clusters of two CTAs (the GEMMs' CTA pairs).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pairs(Kern kernel, int clusters, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(pf::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Clusters of two that can be resident at once (the persistent grid), per
+// device and GEMM.
+template <typename Kern>
+static int resident_pairs(Kern kernel, int device, int mode, size_t smem) {
+  static std::mutex mu;
+  static int cache[64][2][2];   // [device][mode - 1] -> {smem, clusters}
+  std::lock_guard<std::mutex> lk(mu);
+  int* c = cache[device & 63][mode - 1];
+  if (c[0] == (int)smem && c[1] > 0) return c[1];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 512);
+  cfg.blockDim = dim3(pf::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  c[0] = (int)smem;
+  c[1] = n;
+  return n;
 }
 
 template <typename Kern, typename... Args>
@@ -744,8 +862,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   PrefillArgs p{a, rb, pb, status};
   const uint64_t R = (uint64_t)pb.rows;
   const uint64_t np1 = a.I / 128, nk1 = a.H / 128, np2 = (a.H + 255) / 256, nk2 = a.I / 128;
-  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                            BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
             make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
@@ -753,10 +870,10 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
             make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
             make_map(&g1.o, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true) &&
             make_map(&g1.os, F32, 4, pb.hsT, nk2, R, 4 * R, 128, 1, false);
-  ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN, true) &&
+  ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN / 2, true) &&
        make_map(&g2.sa, F32, 4, pb.hsT, nk2, R, 4 * R, 128, pf::KG, false) &&
        make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
-       make_map(&g2.o, BF, 2, pb.ys, R, a.H, 2 * (uint64_t)a.H, 64, 128, true);
+       make_map_ys(&g2.o, pb.ys, R, a.H);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.a = g1.o;
   g2.os = g2.o;
@@ -773,6 +890,11 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
            "prefill_gemm2 smem attribute")))
     return err;
   const int sms = num_sms(device);
+  int cl1 = resident_pairs(prefill_gemm_kernel<1>, device, 1, (size_t)sm1);
+  int cl2 = resident_pairs(prefill_gemm_kernel<2>, device, 2, (size_t)sm2);
+  cl1 = cl1 < sms / 2 ? cl1 : sms / 2;
+  cl2 = cl2 < sms / 2 ? cl2 : sms / 2;
+  if (cl1 < 1 || cl2 < 1) return note_error(cudaErrorNotSupported, "prefill CTA pairs do not fit");
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
   int nl = 0;
@@ -788,14 +910,12 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                           st, "act_quant_permute")))
     return err;
   stage_mark(st, 2);
-  if ((err = launch_check(launch_ex(prefill_gemm_kernel<1>, dim3(sms), dim3(pf::THREADS), (size_t)sm1, st, pdl,
-                                    g1, p, ns1),
-                          st, "prefill_gemm1")))
+  if ((err = launch_check(launch_pairs(prefill_gemm_kernel<1>, cl1, (size_t)sm1, st, pdl, g1, p, ns1), st,
+                          "prefill_gemm1")))
     return err;
   stage_mark(st, 3);
-  if ((err = launch_check(launch_ex(prefill_gemm_kernel<2>, dim3(sms), dim3(pf::THREADS), (size_t)sm2, st, pdl,
-                                    g2, p, ns2),
-                          st, "prefill_gemm2")))
+  if ((err = launch_check(launch_pairs(prefill_gemm_kernel<2>, cl2, (size_t)sm2, st, pdl, g2, p, ns2), st,
+                          "prefill_gemm2")))
     return err;
   stage_mark(st, 4);
   if ((err = launch_check(launch_ex(prefill_combine_kernel, dim3(a.T, (a.H + 2047) / 2048), dim3(256), 0, st,

@@ -122,7 +122,7 @@ static __device__ void route_warp_place(const int32_t* __restrict__ ids, int s0,
 }
 
 // Expert-level lists from per-expert counts in eoff[E] (shared memory):
-// writes counts, offsets, glist (padded to min(E, S)), meta, mtp, n_distinct
+// writes counts, offsets, glist (padded to min(E, S)), meta, mtp, mtp2, n_distinct
 // and fills perm[offsets[E] .. S) with -1.  On return eoff[e] holds the
 // offset of expert e.  Ends with __syncthreads.
 static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) {
@@ -130,22 +130,26 @@ static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) 
   const int nt = blockDim.x, tid = threadIdx.x;
   const int per = (E + nt - 1) / nt;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int lc = 0, ld = 0, lm = 0;
+  int lc = 0, ld = 0, lm = 0, lp = 0;
   for (int e = e0; e < e1; ++e) {
     lc += eoff[e];
     ld += eoff[e] > 0;
     lm += (eoff[e] + 127) >> 7;
+    lp += (((eoff[e] + 127) >> 7) + 1) >> 1;
   }
-  int tot_c, tot_d, tot_m;
+  int tot_c, tot_d, tot_m, tot_p;
   int oc = block_exclusive_scan(lc, red, &tot_c);
   int od = block_exclusive_scan(ld, red, &tot_d);
   int om = block_exclusive_scan(lm, red, &tot_m);
+  int op = block_exclusive_scan(lp, red, &tot_p);
   for (int e = e0; e < e1; ++e) {
     const int c = eoff[e];
     rb.counts[e] = c;
     rb.offsets[e] = oc;
     if (rb.mtp) rb.mtp[e] = om;
+    if (rb.mtp2) rb.mtp2[e] = op;
     om += (c + 127) >> 7;
+    op += (((c + 127) >> 7) + 1) >> 1;
     eoff[e] = oc;
     if (c > 0) {
       if (rb.meta) rb.meta[od] = make_int4(e, oc, c, 0);
@@ -159,6 +163,7 @@ static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) 
     rb.offsets[E] = tot_c;
     *rb.nd = tot_d;
     if (rb.mtp) rb.mtp[E] = tot_m;
+    if (rb.mtp2) rb.mtp2[E] = tot_p;
   }
   for (int q = tot_c + tid; q < S; q += nt) rb.perm[q] = -1;
   __syncthreads();
