@@ -65,7 +65,7 @@ struct DecodeArgs {
   StreamCfg c1, c2;
 };
 
-constexpr int kMaxNS = 8;
+constexpr int kMaxNS = 12;
 constexpr int kGroups = 2;             // consumer groups taking alternate units
 constexpr int kGW = 4;                 // warps per group (they split K)
 constexpr int kNWC = kGroups * kGW;    // consumer warps
@@ -287,6 +287,47 @@ __device__ __forceinline__ void chunk_mma(float (&b0)[4], float (&b1)[4], const 
   mma_f16_16816(b1, A[3], x1.z, x1.w);
 }
 
+// GEMM1 unit, K slice of KW blocks per warp: the warp first copies all of
+// its weight bytes of the unit from the ring stage into registers (16 bytes
+// per lane per 64-wide chunk and row) and releases the stage at once, so the
+// stage is held only for those loads, not for the MMAs.  The arrive has
+// release semantics and so orders the shared-memory reads before the
+// producer's next copy into the stage.
+template <int KW>
+__device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8_t* brow, const uint8_t* xrow,
+                                                int kb0, bool has_w, bool has_x, float sgl, float sul,
+                                                uint64_t* empty_bar, int lane, float (&acc)[4]) {
+  uint4 wa[2 * KW], wb[2 * KW];
+#pragma unroll
+  for (int i = 0; i < 2 * KW; ++i) {
+    const int kk = (kb0 + (i >> 1)) * 128 + (i & 1) * 64;
+    wa[i] = has_w ? lds128(arow + kk) : make_uint4(0, 0, 0, 0);
+    wb[i] = has_w ? lds128(brow + kk) : make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+#pragma unroll
+  for (int j = 0; j < KW; ++j) {
+    float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      const int kk = (kb0 + j) * 128 + ch * 64;
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+      if (has_x) {
+        x0 = lds128(xrow + 2 * kk);
+        x1 = lds128(xrow + 2 * kk + 16);
+      }
+      chunk_mma(b0, b1, wa[2 * j + ch], wb[2 * j + ch], x0, x1);
+    }
+    const float sg = __shfl_sync(0xffffffffu, sgl, j);
+    const float su = __shfl_sync(0xffffffffu, sul, j);
+    acc[0] = fmaf(sg, b0[0] + b1[0], acc[0]);
+    acc[1] = fmaf(sg, b0[1] + b1[1], acc[1]);
+    acc[2] = fmaf(su, b0[2] + b1[2], acc[2]);
+    acc[3] = fmaf(su, b0[3] + b1[3], acc[3]);
+  }
+}
+
 #define MOE_FAIL()                              \
   do {                                          \
     abort_flag = 1;                             \
@@ -407,6 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         const uint8_t* arow = st + g * a.H + c * 16;
         const uint8_t* brow = arow + rowb;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int kw = kb1 - kb0;
+        if (kw >= 1 && kw <= 4) {
+          switch (kw) {
+            case 1: gemm1_unit_regs<1>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
+            case 2: gemm1_unit_regs<2>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
+            case 3: gemm1_unit_regs<3>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
+            default: gemm1_unit_regs<4>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
+          }
+        } else {
 #pragma unroll 1
         for (int kb = kb0; kb < kb1; ++kb) {
           float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -434,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
+        }
         float tot[4];
         if (!group_reduce<4>(S, gr, wq, lane, m >> 1, acc, tot)) MOE_FAIL();
         if (wq == 0 && has_w) {
@@ -443,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
             if (2 * c + j < nx) {
               const float gv = ldexpf(tot[j], sx[j]);
               const float uv = ldexpf(tot[2 + j], sx[j]);
-              p.db.h[(int64_t)(pos0 + j) * a.I + i0 + g] = gv / (1.0f + expf(-gv)) * uv;
+              p.db.h[(int64_t)(pos0 + j) * a.I + i0 + g] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
           }
         }
@@ -505,7 +556,56 @@ __device__ void gemm2_unit_compute(const uint8_t* st, const uint8_t* hbrow, int 
   }
 }
 
-template <int MT>
+// The same with the warp's weight bytes first copied into registers and the
+// ring stage released before the MMAs (KW K blocks per warp, MT * KW <= 4).
+template <int MT, int KW>
+__device__ __forceinline__ void gemm2_unit_regs(const uint8_t* st, const uint8_t* hbrow, int I, int kb0, int lane,
+                                                bool has_b, float sl, uint64_t* empty_bar, float (&acc)[MT][4]) {
+  const int g = lane >> 2, c = lane & 3;
+  uint4 wa[MT][2 * KW], wb[MT][2 * KW];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int i = 0; i < 2 * KW; ++i) {
+      const uint8_t* ra = st + (t * 16 + g) * I + (kb0 + (i >> 1)) * 128 + (i & 1) * 64 + c * 16;
+      wa[t][i] = lds128(ra);
+      wb[t][i] = lds128(ra + 8 * I);
+    }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+#pragma unroll
+  for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll
+  for (int j = 0; j < KW; ++j) {
+    float b0[MT][4], b1[MT][4];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b0[t][i] = b1[t][i] = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      const int kk = (kb0 + j) * 128 + ch * 64;
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+      if (has_b) {
+        x0 = lds128(hbrow + 2 * kk);
+        x1 = lds128(hbrow + 2 * kk + 16);
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) chunk_mma(b0[t], b1[t], wa[t][2 * j + ch], wb[t][2 * j + ch], x0, x1);
+    }
+    const float s = __shfl_sync(0xffffffffu, sl, j);
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[t][i] = fmaf(s, b0[t][i] + b1[t][i], acc[t][i]);
+  }
+}
+
+// ROWS: the four warps of a group take the unit's 16-row tiles (warp wq
+// rows wq*16 ..) over the whole K, so there is no cross-warp sum and every
+// warp writes its own rows (used when a unit of 64 rows fits a stage).
+// Otherwise the warps split K and the group's first warp sums and writes.
+template <int MT, bool ROWS>
 __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, int R2, int upe, int warp, int lane,
                                 int* abort_flag) {
   const LayerArgs& a = p.a;
@@ -514,7 +614,8 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
   const int gr = warp / kGW, wq = warp % kGW;
   const int g = lane >> 2, c = lane & 3;
   const int nkb = a.I >> 7;
-  const int kb0 = wq * nkb / kGW, kb1 = (wq + 1) * nkb / kGW;
+  const int kb0 = ROWS ? 0 : wq * nkb / kGW, kb1 = ROWS ? nkb : (wq + 1) * nkb / kGW;
+  const bool lead = ROWS || wq == 0;   // writes outputs
   // this warp's share of the h conversion
   const int ck0 = warp * a.I / kNWC, ck1 = (warp + 1) * a.I / kNWC;
   int m = 0, gen = 0;
@@ -528,10 +629,10 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
       const int b = gen & 1;
       uint8_t* hb = S.hb + b * cfg.HBB;
       const uint8_t* hraw = S.abuf;
-      // epilogue data (group leaders): slots 2c, 2c+1 (lanes with c < 2)
+      // epilogue data (output-writing warps): slots 2c, 2c+1 (lanes with c < 2)
       int so[2] = {-1, -1};
       float wo[2] = {0.f, 0.f};
-      if (wq == 0 && c < 2) {
+      if (lead && c < 2) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           if (2 * c + j < nh) {
@@ -590,22 +691,55 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
       }
       for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
         if ((m & 1) != gr) continue;
-        const int n0 = (int)(u % upe) * R2;
+        const int n0 = (int)(u % upe) * R2 + (ROWS ? wq * 16 : 0);
         const uint16_t* srow = a.w2s + (int64_t)wk.e * a.s2_exp + (int64_t)(n0 / 128) * a.s2_row;
         const float sl = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(srow + kb0 + lane)) : 0.f;
         const int slot = m % NS;
         if (!warp_wait(&S.full[slot], (m / NS) & 1, lane)) return fail();
+        if (ROWS && wq * 16 >= R2) {   // a unit narrower than four tiles: nothing for this warp
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.empty[slot]);
+          continue;
+        }
         float acc[MT][4];
-        gemm2_unit_compute<MT>(S.ring + slot * cfg.SB, hbrow, a.I, kb0, kb1, lane, has_b, sl, acc);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        const int kw = kb1 - kb0;
+        const uint8_t* st = S.ring + slot * cfg.SB + (ROWS ? wq * 16 * a.I : 0);
+        bool done = true;
+        if constexpr (MT == 1) {
+          switch (kw) {
+            case 1: gemm2_unit_regs<1, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 2: gemm2_unit_regs<1, 2>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 3: gemm2_unit_regs<1, 3>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 4: gemm2_unit_regs<1, 4>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            default: done = false;
+          }
+        } else if constexpr (MT == 2) {
+          switch (kw) {
+            case 1: gemm2_unit_regs<2, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 2: gemm2_unit_regs<2, 2>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            default: done = false;
+          }
+        } else {
+          if (kw == 1) gemm2_unit_regs<MT, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc);
+          else done = false;
+        }
+        if (!done) {
+          gemm2_unit_compute<MT>(st, hbrow, a.I, kb0, kb1, lane, has_b, sl, acc);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.empty[slot]);
+        }
         float part[MT * 4], tot[MT * 4];
 #pragma unroll
         for (int t = 0; t < MT; ++t)
 #pragma unroll
           for (int i = 0; i < 4; ++i) part[t * 4 + i] = acc[t][i];
-        if (!group_reduce<MT * 4>(S, gr, wq, lane, m >> 1, part, tot)) return fail();
-        if (wq == 0) {
+        if constexpr (ROWS) {
+#pragma unroll
+          for (int i = 0; i < MT * 4; ++i) tot[i] = part[i];
+        } else {
+          if (!group_reduce<MT * 4>(S, gr, wq, lane, m >> 1, part, tot)) return fail();
+        }
+        if (lead) {
           // columns 2c, 2c+1: hi terms on lanes c < 2, lo terms on lanes c >= 2
 #pragma unroll
           for (int i = 0; i < MT * 4; ++i) tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], 2);
@@ -696,10 +830,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     }
     return;
   }
-  switch (R2 / 16) {
-    case 1: gemm2_consumers<1>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
-    case 2: gemm2_consumers<2>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
-    default: gemm2_consumers<4>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+  if (cfg.V == 0) {
+    gemm2_consumers<1, true>(p, S, wk, R2, upe, warp, lane, &abort_flag);
+  } else {
+    switch (R2 / 16) {
+      case 1: gemm2_consumers<1, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+      case 2: gemm2_consumers<2, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+      default: gemm2_consumers<4, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+    }
   }
 }
 
@@ -770,11 +908,19 @@ static bool config_gemm1(int H, StreamCfg& c) {
   c.HBB = 0;
   c.HP = 0;
   c.V = 4;
-  for (int spp = 8; spp >= 1; --spp) {
+  // bytes in flight per SM set the streaming rate, so the ring comes first:
+  // the most stages that fit next to activation buffers of at least 4 slots
+  for (c.NS = kMaxNS; c.NS >= 3; --c.NS)
+    for (int spp = 8; spp >= 4; --spp) {
+      c.SPP = spp;
+      c.XB = align128(spp * c.XP);
+      if (place(c, 2)) return true;
+    }
+  for (int spp = 3; spp >= 1; --spp) {
     c.SPP = spp;
     c.XB = align128(spp * c.XP);
     for (c.NS = kMaxNS; c.NS >= 3; --c.NS)
-      if (place(c, 2) && (c.NS >= 4 || spp <= 4)) return true;
+      if (place(c, 2)) return true;
   }
   return false;
 }
@@ -782,10 +928,17 @@ static bool config_gemm1(int H, StreamCfg& c) {
 // GEMM2: R2 rows per unit (16, 32 or 64) with R2*I near 16 KiB; a raw h
 // buffer for 4 slots and two converted buffers of 8 f16 rows.
 static bool config_gemm2(int H, int I, StreamCfg& c) {
-  c.R = 16;
-  while (c.R < 64 && 2 * c.R * I <= 16384 && 2 * c.R <= H) c.R *= 2;
+  if (64 * I <= 32768 && H >= 64) {
+    // row-split units: 64 rows (one 16-row tile per warp of a group), no
+    // cross-warp reduction (V = 0 selects this form in the kernel)
+    c.R = 64;
+    c.V = 0;
+  } else {
+    c.R = 16;
+    while (c.R < 64 && 2 * c.R * I <= 16384 && 2 * c.R <= H) c.R *= 2;
+    c.V = 4 * (c.R / 16);
+  }
   c.SB = align128(c.R * I);
-  c.V = 4 * (c.R / 16);
   c.XP = 4 * I;
   c.HP = 2 * I + 16;          // == 16 mod 128: conflict-free B fragment loads
   c.HBB = align128(8 * c.HP);
