@@ -84,12 +84,31 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
     route_block(a.ids, a.S, a.E, p.rb, p.status, smem_prep);
     return;
   }
-  // token t: f16 copy scaled so that max |x_t| * 2^-s lands in [2^14, 2^15)
+  // token t: f16 copy scaled so that max |x_t| * 2^-s lands in [2^14, 2^15).
+  // Each thread reads its chunks of 8 values once (16-byte loads; at least
+  // 256 threads and H <= 8192 make at most 4 chunks) and keeps them for the
+  // conversion.
+  constexpr int kMaxChunks = 4;
   __shared__ float wmax[32];
   const int t = blockIdx.x - 1;
   const uint16_t* x = a.hidden + (int64_t)t * a.hidden_ld;
+  float v[kMaxChunks][8];
   float m = 0.f;
-  for (int i = threadIdx.x; i < a.H; i += blockDim.x) m = fmaxf(m, fabsf(bf16_bits_to_f32(x[i])));
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int i0 = (c * (int)blockDim.x + threadIdx.x) * 8;
+    if (i0 < a.H) {
+      const uint4 r = *reinterpret_cast<const uint4*>(x + i0);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[c][2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+        v[c][2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[c][j]));
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
@@ -102,9 +121,19 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
     frexpf(m, &ex);      // m = f * 2^ex, f in [0.5, 1)
     s = (ex - 1) - 14;   // floor(log2 m) - 14
   }
-  __half* xh = reinterpret_cast<__half*>(p.db.xh) + (int64_t)t * a.H;
-  for (int i = threadIdx.x; i < a.H; i += blockDim.x)
-    xh[i] = __float2half_rn(ldexpf(bf16_bits_to_f32(x[i]), -s));
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int i0 = (c * (int)blockDim.x + threadIdx.x) * 8;
+    if (i0 < a.H) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(ldexpf(v[c][2 * j], -s), ldexpf(v[c][2 * j + 1], -s));
+        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(p.db.xh + (int64_t)t * a.H + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
   if (threadIdx.x == 0) p.db.xexp[t] = s;
 }
 
@@ -219,6 +248,66 @@ __device__ __forceinline__ bool walk_next_segment(const DecodeArgs& p, Walk& w, 
   w.passes = (w.ne + SPP - 1) / SPP;
   w.u = w.seg_e;
   return true;
+}
+
+// The routed experts as a bitmap in shared memory (bit e set when some slot
+// routes to expert e, 0 <= e < E), built by one warp from the ids alone: the
+// same experts, in the same ascending order, as the routing lists, so a
+// kernel can know its first experts before the routing lists exist.  Lane l
+// keeps words 4l .. 4l+3 (E <= 4096) and the exclusive / inclusive counts of
+// set bits before and through them.  Returns the number of routed experts.
+struct ExpertBits {
+  uint32_t w[4];
+  int excl, incl;
+};
+
+__device__ __forceinline__ int expert_bits(const int32_t* __restrict__ ids, int S, int E, uint32_t* bits, int lane,
+                                           ExpertBits& eb) {
+  const int nwords = (E + 31) >> 5;
+  for (int i = lane; i < 128; i += 32) bits[i] = 0;
+  __syncwarp();
+  for (int s = lane; s < S; s += 32) {
+    const int id = __ldg(ids + s);
+    if (id >= 0 && id < E) atomicOr(&bits[id >> 5], 1u << (id & 31));
+  }
+  __syncwarp();
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int wi = lane * 4 + j;
+    eb.w[j] = wi < nwords ? bits[wi] : 0u;
+    cnt += __popc(eb.w[j]);
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  eb.excl = incl - cnt;
+  eb.incl = incl;
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// The d-th routed expert (0-based, ascending), on all lanes.
+__device__ __forceinline__ int expert_select(const ExpertBits& eb, int d, int lane) {
+  int e = -1;
+  if (eb.excl <= d && d < eb.incl) {
+    int r = d - eb.excl;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = __popc(eb.w[j]);
+      if (e < 0 && r < c) {
+        uint32_t v = eb.w[j];
+        for (int q = 0; q < r; ++q) v &= v - 1;   // drop the r lowest set bits
+        e = (lane * 4 + j) * 32 + __ffs(v) - 1;
+      } else if (e < 0) {
+        r -= c;
+      }
+    }
+  }
+  const uint32_t owner = __ballot_sync(0xffffffffu, e >= 0);
+  return owner ? __shfl_sync(0xffffffffu, e, __ffs(owner) - 1) : -1;
 }
 
 // Rows per unit after halving until every SM gets enough units to balance
@@ -347,17 +436,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
   const StreamCfg& cfg = p.c1;
   const Smem S = smem_layout(smem, cfg);
   __shared__ int abort_flag;
+  __shared__ uint32_t ebits[128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     smem_init(S, cfg.NS);
     abort_flag = 0;
   }
   __syncthreads();
-  pdl_wait();
   pdl_trigger();
 
+  // The producer finds the routed experts itself (from the ids, an input)
+  // and starts the weight stream before the prep kernel has finished; the
+  // consumers, which need its activation rows and routing lists, wait for it.
   const LayerArgs& a = p.a;
-  const int D = *p.rb.nd;
+  ExpertBits eb;
+  int D;
+  if (warp == kNWC) {
+    D = expert_bits(a.ids, a.S, a.E, ebits, lane, eb);
+  } else {
+    pdl_wait();
+    D = *p.rb.nd;
+  }
   const int R = balanced_rows(cfg.R, 1, a.I, D, gridDim.x);
   const int upe = a.I / R;
   const long U = (long)D * upe;
@@ -374,20 +473,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
     const uint64_t pol_x = l2_policy_evict_last();
     int m = 0, gen = 0;
     bool ok = true;
+    // weight copies of the first units (of the range's first expert) go out
+    // before the wait for the prep kernel
+    int pre = 0;
+    if (wk.u < wk.ue) {
+      const int d0 = (int)(wk.u / upe);
+      const int e0 = expert_select(eb, d0, lane);
+      const long n = min((long)NS, min(wk.ue, (long)(d0 + 1) * upe) - wk.u);
+      if (lane == 0 && e0 >= 0)
+        for (long i = 0; i < n; ++i) {
+          const int i0 = (int)((wk.u + i) % upe) * R;
+          const uint8_t* gsrc = a.w13 + ((int64_t)e0 * 2 * a.I + i0) * a.H;
+          mbar_arrive_expect_tx(&S.full[i], 2 * rowb);
+          bulk_g2s(S.ring + i * cfg.SB, gsrc, rowb, &S.full[i], pol_w);
+          bulk_g2s(S.ring + i * cfg.SB + rowb, gsrc + (int64_t)a.I * a.H, rowb, &S.full[i], pol_w);
+        }
+      pre = e0 >= 0 ? (int)n : 0;
+    }
+    pdl_wait();
     while (ok && walk_next_segment(p, wk, SPP)) {
       for (int pass = 0; pass < wk.passes && ok; ++pass, ++gen) {
         const int nx = min(SPP, wk.ne - pass * SPP);
         const int b = gen & 1;
-        // activation rows of this pass: lane j holds the token of slot j
+        // activation rows of this pass (lane j: the token of slot j), issued
+        // right after the pass's first weight copy, so that the routed-position
+        // lookup is off the path to the first weight bytes
         const int tok = lane < nx ? p.rb.perm[wk.off + pass * SPP + lane] / a.k : 0;
-        if (gen >= 2) ok = warp_wait(&S.aempty[b], ((gen >> 1) - 1) & 1, lane);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&S.afull[b], nx * 2 * a.H);
-        __syncwarp();
-        if (lane < nx)
-          bulk_g2s(S.abuf + b * cfg.XB + lane * cfg.XP, p.db.xh + (int64_t)tok * a.H, 2 * a.H, &S.afull[b], pol_x);
+        bool x_sent = false;
+        auto send_x = [&]() {
+          x_sent = true;
+          if (gen >= 2) ok = warp_wait(&S.aempty[b], ((gen >> 1) - 1) & 1, lane);
+          if (!ok) return;
+          if (lane == 0) mbar_arrive_expect_tx(&S.afull[b], nx * 2 * a.H);
+          __syncwarp();
+          if (lane < nx)
+            bulk_g2s(S.abuf + b * cfg.XB + lane * cfg.XP, p.db.xh + (int64_t)tok * a.H, 2 * a.H, &S.afull[b],
+                     pol_x);
+        };
         for (long u = wk.seg_b; u < wk.seg_e && ok; ++u, ++m) {
           const int slot = m % NS;
+          if (m >= pre) {
           if (m >= NS) ok = warp_wait(&S.empty[slot], ((m / NS) - 1) & 1, lane);
           if (!ok) break;
           if (lane == 0) {
@@ -398,7 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
             bulk_g2s(S.ring + slot * cfg.SB + rowb, gsrc + (int64_t)a.I * a.H, rowb, &S.full[slot], pol_w);
           }
           __syncwarp();
+          }
+          if (!x_sent) send_x();
         }
+        if (!x_sent && ok) send_x();
         if (*(volatile int*)&abort_flag) ok = false;
       }
     }
@@ -406,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
       abort_flag = 1;
       raise_status(p.status, MOE_STATUS_TIMEOUT);
       // let the copies already issued land before the CTA exits
-      for (int mm = max(0, m - NS); mm < m; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
+      const int issued = max(m, pre);
+      for (int mm = max(0, issued - NS); mm < issued; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
       for (int gg = max(0, gen - 1); gg <= gen; ++gg) mbar_wait(&S.afull[gg & 1], (gg >> 1) & 1);
     }
     return;
@@ -776,9 +905,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     abort_flag = 0;
   }
   __syncthreads();
-  pdl_wait();
   pdl_trigger();
 
+  // The routing lists come from the prep kernel, which had completed before
+  // the kernel this one follows (GEMM1) released its dependents, so they can
+  // be read before waiting for GEMM1; only h needs the wait.
   const LayerArgs& a = p.a;
   const int D = *p.rb.nd;
   const int R2 = balanced_rows(cfg.R, 16, a.H, D, gridDim.x);
@@ -796,6 +927,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     const uint64_t pol_h = l2_policy_evict_last();
     int m = 0, gen = 0;
     bool ok = true;
+    // weight copies of the first units (first pass of the first segment) go
+    // out before the wait for GEMM1, so they overlap its tail
+    int pre = 0;
+    {
+      Walk w0 = wk;
+      if (walk_next_segment(p, w0, SPP)) {
+        const long n = min((long)NS, w0.seg_e - w0.seg_b);
+        if (lane == 0)
+          for (long i = 0; i < n; ++i) {
+            const int n0 = (int)((w0.seg_b + i) % upe) * R2;
+            mbar_arrive_expect_tx(&S.full[i], tileb);
+            bulk_g2s(S.ring + i * cfg.SB, a.w2 + ((int64_t)w0.e * a.H + n0) * a.I, tileb, &S.full[i], pol_w);
+          }
+        pre = (int)n;
+      }
+    }
+    pdl_wait();
     while (ok && walk_next_segment(p, wk, SPP)) {
       for (int pass = 0; pass < wk.passes && ok; ++pass, ++gen) {
         const int nh = min(SPP, wk.ne - pass * SPP);
@@ -809,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
         }
         __syncwarp();
         for (long u = wk.seg_b; u < wk.seg_e && ok; ++u, ++m) {
+          if (m < pre) continue;   // copied before the wait
           const int slot = m % NS;
           if (m >= NS) ok = warp_wait(&S.empty[slot], ((m / NS) - 1) & 1, lane);
           if (!ok) break;
@@ -825,11 +974,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     if (!ok && lane == 0) {
       abort_flag = 1;
       raise_status(p.status, MOE_STATUS_TIMEOUT);
-      for (int mm = max(0, m - NS); mm < m; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
+      const int issued = max(m, pre);
+      for (int mm = max(0, issued - NS); mm < issued; ++mm) mbar_wait(&S.full[mm % NS], (mm / NS) & 1);
       if (gen > 0) mbar_wait(&S.afull[0], (gen - 1) & 1);
     }
     return;
   }
+  pdl_wait();
   if (cfg.V == 0) {
     gemm2_consumers<1, true>(p, S, wk, R2, upe, warp, lane, &abort_flag);
   } else {
@@ -960,7 +1111,11 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   if (!config_gemm1(a.H, p.c1) || !config_gemm2(a.H, a.I, p.c2)) return cudaErrorNotSupported;
   const int sms = num_sms(device);
   cudaError_t err;
-  const int nt = route_threads(a.E);
+  // few slots: a smaller CTA keeps the route's block-wide scans short; the
+  // activation CTAs need one thread per 8 values of a row
+  int nt = route_threads(a.E);
+  const int want = (a.S + 31) / 32 * 32;
+  if (want < nt) nt = want < 256 ? 256 : want;   // >= 256 threads: the activation CTAs rely on it
   const size_t rsm = route_smem_bytes(a.E, nt);
   if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm)))
     return err;

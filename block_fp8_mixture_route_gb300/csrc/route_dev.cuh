@@ -58,6 +58,45 @@ static __device__ int block_exclusive_scan(int v, int* red /*[33]*/, int* total)
   return base + x - v;
 }
 
+// The same for four independent counters at once (one pass of barriers).
+static __device__ int4 block_exclusive_scan4(int4 v, int4* red /*[33]*/, int4* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int4 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yx = __shfl_up_sync(0xffffffffu, x.x, o), yy = __shfl_up_sync(0xffffffffu, x.y, o);
+    const int yz = __shfl_up_sync(0xffffffffu, x.z, o), yw = __shfl_up_sync(0xffffffffu, x.w, o);
+    if (lane >= o) {
+      x.x += yx;
+      x.y += yy;
+      x.z += yz;
+      x.w += yw;
+    }
+  }
+  if (lane == 31) red[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int4 s = lane < nw ? red[lane] : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yx = __shfl_up_sync(0xffffffffu, s.x, o), yy = __shfl_up_sync(0xffffffffu, s.y, o);
+      const int yz = __shfl_up_sync(0xffffffffu, s.z, o), yw = __shfl_up_sync(0xffffffffu, s.w, o);
+      if (lane >= o) {
+        s.x += yx;
+        s.y += yy;
+        s.z += yz;
+        s.w += yw;
+      }
+    }
+    if (lane < nw) red[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int4 b = w > 0 ? red[w - 1] : make_int4(0, 0, 0, 0);
+  *total = red[nw - 1];
+  __syncthreads();
+  return make_int4(b.x + x.x - v.x, b.y + x.y - v.y, b.z + x.z - v.z, b.w + x.w - v.w);
+}
+
 // Pass 1 over slots [s0, s1) split into contiguous per-warp segments:
 // wcnt[w][e] = slots of warp w routed to expert e.  Sets *bad if an id >= E
 // is seen.  Ends with __syncthreads.
@@ -126,7 +165,7 @@ static __device__ void route_warp_place(const int32_t* __restrict__ ids, int s0,
 // and fills perm[offsets[E] .. S) with -1.  On return eoff[e] holds the
 // offset of expert e.  Ends with __syncthreads.
 static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) {
-  __shared__ int red[33];
+  __shared__ int4 red[33];
   const int nt = blockDim.x, tid = threadIdx.x;
   const int per = (E + nt - 1) / nt;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
@@ -137,11 +176,10 @@ static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) 
     lm += (eoff[e] + 127) >> 7;
     lp += (((eoff[e] + 127) >> 7) + 1) >> 1;
   }
-  int tot_c, tot_d, tot_m, tot_p;
-  int oc = block_exclusive_scan(lc, red, &tot_c);
-  int od = block_exclusive_scan(ld, red, &tot_d);
-  int om = block_exclusive_scan(lm, red, &tot_m);
-  int op = block_exclusive_scan(lp, red, &tot_p);
+  int4 tot;
+  const int4 ex = block_exclusive_scan4(make_int4(lc, ld, lm, lp), red, &tot);
+  int oc = ex.x, od = ex.y, om = ex.z, op = ex.w;
+  const int tot_c = tot.x, tot_d = tot.y, tot_m = tot.z, tot_p = tot.w;
   for (int e = e0; e < e1; ++e) {
     const int c = eoff[e];
     rb.counts[e] = c;
