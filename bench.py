@@ -402,8 +402,12 @@ def prefill_leg(dev, s, flush, reps):
     lib = _lib.load()
     shp = syn.PREFILL
     w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
-    _, bf16_peak, src = peaks()
+    hbm_peak, bf16_peak, src = peaks()
     fp8_peak = 2.0 * bf16_peak
+    # the least bytes a prefill forward moves: every expert's weights and valid
+    # block scales (all are routed at these sizes), x in and out
+    per_expert = (2 * shp.I * shp.H + shp.H * shp.I + 2 * ((2 * shp.I // 128) * (shp.H // 128))
+                  + 2 * ((shp.H // 128) * (shp.I // 128)))
     res = {}
     for T, routing in PREFILL_CASES:
         ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, routing, step=T)
@@ -441,8 +445,12 @@ def prefill_leg(dev, s, flush, reps):
         stage = [statistics.median(x[i] for x in st) for i in range(5)]
         ms = statistics.median(times)
         g1f, g2f = 4.0 * T * shp.k * shp.H * shp.I, 2.0 * T * shp.k * shp.H * shp.I
+        min_bytes = shp.E * per_expert + 2 * 2 * T * shp.H
+        bound_s = max(flops / (fp8_peak * 1e12), min_bytes / (hbm_peak * 1e9))
         res[f"T{T}_{routing}"] = {
             "us": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12, "frac_of_fp8_peak": flops / (ms / 1e3) / 1e12 / fp8_peak,
+            "frac_of_roofline": bound_s / (ms / 1e3),
+            "roofline_bound": "tensor" if flops / (fp8_peak * 1e12) >= min_bytes / (hbm_peak * 1e9) else "hbm",
             "stage_us": {n: round(1e3 * v, 2) for n, v in
                          zip(("route", "act_quant_permute", "gemm1", "gemm2", "combine"), stage)},
             "gemm1_tflops": g1f / (stage[2] / 1e3) / 1e12, "gemm2_tflops": g2f / (stage[3] / 1e3) / 1e12,
@@ -453,6 +461,59 @@ def prefill_leg(dev, s, flush, reps):
 
 
 PROFILE_CASES = ("decode_T16", "decode_T1", "prefill_T4096", "prefill_T16384")
+# gate sweeps: layer -> token counts.  wide: T = round(32 r), r = T*k/E = 0.1 .. 1.0;
+# small: r = T*k/E = 0.0625 .. 1.0
+SWEEPS = {
+    "wide": (syn.DECODE_WIDE, (1, 3, 6, 10, 13, 16, 19, 22, 26, 29, 32)),
+    "small": (syn.DECODE_SMALL, (1, 2, 3, 4, 6, 8, 10, 12, 16)),
+}
+
+
+def gate_sweep(which: str = "wide", reps: int = 5):
+    """Decode against prefill for r = T*k/E up to 1.0 on the wide-expert
+    layer (E=256, H=7168, I=2048, top_k=8, about 11 GB of e4m3 weights) or
+    the small-expert one (E=128, H=2048, I=512): median forward time of each
+    path after an L2 flush.  Prints one JSON object (not a bench line): the
+    data behind the default gate."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    shp, sweep_ts = SWEEPS[which]
+    w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    rows = []
+    for T in sweep_ts:
+        ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, "softmax", step=T)
+        prob = dict(hidden=syn.make_hidden(T, shp.H, 0, dev, step=T), topk_ids=ids, topk_weights=w, w13=w13,
+                    w13_scale=w13s, w2=w2, w2_scale=w2s)
+        out = torch.empty(T, shp.H, dtype=torch.bfloat16, device=dev)
+        D, nbytes = routed_bytes(shp, ids)
+        row = {"T": T, "r": T * shp.k / shp.E, "distinct_experts": D, "routed_GB": nbytes / 1e9}
+        for path in ("decode", "prefill"):
+            with torch.cuda.stream(s):
+                for _ in range(2):
+                    api.forward_problem(prob, out=out, stream=s, force_path=path)
+            s.synchronize()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(s):
+                    flush.zero_()
+                    e0.record(s)
+                    api.forward_problem(prob, out=out, stream=s, force_path=path)
+                    e1.record(s)
+                s.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            row[f"{path}_us"] = 1e3 * ms
+            row[f"{path}_GB_s"] = nbytes / (ms / 1e3) / 1e9
+        row["faster"] = "decode" if row["decode_us"] <= row["prefill_us"] else "prefill"
+        rows.append(row)
+    cross = next((r["r"] for r in rows if r["faster"] == "prefill"), None)
+    print(json.dumps({"gate_sweep": rows,
+                      "workload": f"E={shp.E} H={shp.H} I={shp.I} top_k={shp.k}, softmax routing",
+                      "default_gate": "decode while T*k <= E and the decode gate/up ring has >= 4 stages",
+                      "first_r_where_prefill_is_faster": cross}), flush=True)
 
 
 def profile_case(name: str, reps: int = 3):
@@ -488,11 +549,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
+    ap.add_argument("--gate-sweep", choices=tuple(SWEEPS), default=None,
+                    help="time decode against prefill for r = T*k/E up to 1.0 on one layer (one JSON object)")
     ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
                     help="only run 3 forwards of one case (for ncu captures); prints no bench line")
     args = ap.parse_args()
     if args.profile_case:
         profile_case(args.profile_case)
+        return
+    if args.gate_sweep:
+        gate_sweep(args.gate_sweep)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -1100,6 +1100,12 @@ static bool config_gemm2(int H, int I, StreamCfg& c) {
   return false;
 }
 
+int decode_ring_stages(int H, int I) {
+  StreamCfg c1, c2;
+  if (H % 128 || I % 128 || !config_gemm1(H, c1) || !config_gemm2(H, I, c2)) return 0;
+  return c1.NS;
+}
+
 bool decode_supported(int H, int I) {
   StreamCfg c1, c2;
   return H % 128 == 0 && I % 128 == 0 && config_gemm1(H, c1) && config_gemm2(H, I, c2);

@@ -259,7 +259,7 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
 }
 
 int check_options(const moe_options* opt, float* ratio, int* force) {
-  *ratio = 0.4f;
+  *ratio = 0.f;   // the measured default gate (choose_path)
   *force = MOE_PATH_NONE;
   if (!opt) return MOE_OK;
   for (int i = 0; i < 6; ++i)
@@ -334,10 +334,20 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
   return MOE_OK;
 }
 
+// Gate.  With a caller ratio: decode while T*k <= E*ratio (the rule of the
+// fp8-moe-gather page, environment-variable table).  Default, from sweeps of
+// both paths on GB300: decode while T*k <= E and the decode gate/up stream
+// gets at least 4 ring stages.  With H = 2048 (5 stages) decode was faster
+// at every T*k/E up to 1; with H = 7168 (3 stages: the 14 KB activation
+// rows crowd the ring) prefill was faster from T*k/E = 0.1 up.
 int choose_path(const LayerArgs& a, float ratio, int force) {
   if (force != MOE_PATH_NONE) return force;
-  const bool gathered = (double)a.T * a.k <= (double)a.E * ratio;
-  return gathered && decode_supported(a.H, a.I) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  if (ratio > 0.f) {
+    const bool gathered = (double)a.T * a.k <= (double)a.E * ratio;
+    return gathered && decode_supported(a.H, a.I) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  }
+  const bool gathered = (double)a.T * a.k <= (double)a.E;
+  return gathered && decode_ring_stages(a.H, a.I) >= 4 ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
 int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,

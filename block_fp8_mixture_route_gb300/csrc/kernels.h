@@ -105,6 +105,8 @@ cudaError_t launch_widen(const uint8_t* codes, int64_t n, float* out, cudaStream
 
 // Whether the decode path can stage rows of this layer shape in shared memory.
 bool decode_supported(int H, int I);
+// Ring stages the decode gate/up stream gets for this shape (0 if unsupported).
+int decode_ring_stages(int H, int I);
 
 // Decode (W8A16) path: prep (route + f16 activations), GEMM1+silu*up,
 // GEMM2, combine.  Adds the number of launches to *launches.

@@ -22,9 +22,13 @@
  *
  * Paths (chosen per call; the choice is readable through
  * moe_fp8_block_last_path):
- *   decode  (W8A16): taken while T*k <= E*ratio, ratio 0.4 by default
- *     (fp8-moe-gather page, environment-variable table).  bf16 activations,
- *     e4m3 weights widened in registers, fp32 accumulation and fp32 h.
+ *   decode  (W8A16): with a caller gate ratio, taken while T*k <= E*ratio
+ *     (fp8-moe-gather page, environment-variable table, where the ratio is
+ *     0.4).  By default, from measurements of both paths on GB300: taken
+ *     while T*k <= E and the layer's hidden rows leave the decode weight
+ *     stream at least 4 shared-memory ring stages (H = 2048: yes; H = 7168:
+ *     no, where the prefill path streams faster).  bf16 activations, e4m3
+ *     weights widened in registers, fp32 accumulation and fp32 h.
  *   prefill (W8A8): activations quantised per token per 128 columns with a
  *     dynamic scale amax/448 (fp8-moe-gather page, "Affects": dynamic
  *     activation scales), grouped FP8 tensor-core GEMMs, h quantised the same
@@ -106,7 +110,7 @@ enum {
 
 /* Options of moe_fp8_block_forward_ex.  Zero-initialise, then set fields. */
 typedef struct {
-  float gate_ratio;   /* decode while T*k <= E*gate_ratio; <= 0 -> 0.4          */
+  float gate_ratio;   /* decode while T*k <= E*gate_ratio; <= 0 -> measured rule */
   int32_t force_path; /* MOE_PATH_NONE (gate decides), _DECODE or _PREFILL     */
   int32_t reserved[6];/* must be zero                                          */
 } moe_options;

@@ -70,6 +70,15 @@ def test_decode_wide_experts(cuda_lib, T, tokens):
     assert r < TOL
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("T,tokens", [(32, [0, 15, 31])])
+def test_prefill_wide_experts(cuda_lib, T, tokens):
+    """The prefill path on the wide-expert layer (H=7168, I=2048), where
+    the default gate sends every token count."""
+    r, _ = run_and_check(problem(syn.DECODE_WIDE, T), "prefill", tokens=tokens)
+    assert r < TOL
+
+
 def test_decode_status_and_skipped_slots(cuda_lib):
     prob = problem(syn.TINY, 4)
     ids = prob["topk_ids"].clone()
@@ -105,10 +114,27 @@ def test_decode_padded_equals_unpadded(cuda_lib):
 
 
 def test_default_gate(cuda_lib):
-    """Decode while T*k <= E*0.4 (fp8-moe-gather page, environment table)."""
-    prob = problem(syn.DECODE_SMALL, 6)
-    api.forward_problem(prob)
+    """Default gate: decode while T*k <= E on a layer whose decode stream
+    keeps at least 4 ring stages (H = 2048)."""
+    for T in (6, 16):
+        api.forward_problem(problem(syn.DECODE_SMALL, T))
+        assert api.moe_fp8_block_last_path() == 1
+
+
+def test_gate_ratio_option(cuda_lib):
+    """A caller ratio applies the page's rule: decode while T*k <= E*ratio."""
+    prob = problem(syn.DECODE_SMALL, 7)   # 56 slots > 128 * 0.4
+    api.forward_problem(prob, gate_ratio=0.4)
+    assert api.moe_fp8_block_last_path() == 2
+    api.forward_problem(problem(syn.DECODE_SMALL, 6), gate_ratio=0.4)
     assert api.moe_fp8_block_last_path() == 1
+
+
+@pytest.mark.slow
+def test_default_gate_wide_layer(cuda_lib):
+    """H = 7168 leaves the decode stream 3 ring stages: prefill by default."""
+    api.forward_problem(problem(syn.DECODE_WIDE, 3))
+    assert api.moe_fp8_block_last_path() == 2
 
 
 def test_graph_capture_replay_new_routing(cuda_lib):
@@ -189,7 +215,7 @@ def test_prefill_grouped_gemm(cuda_lib, T, routing, tokens):
 
 
 def test_default_gate_prefill(cuda_lib):
-    prob = problem(syn.DECODE_SMALL, 7)
+    prob = problem(syn.DECODE_SMALL, 17)   # 136 slots > E = 128
     api.forward_problem(prob)
     assert api.moe_fp8_block_last_path() == 2
 
