@@ -562,15 +562,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         for (int j = 0; j < 2; ++j)
           if (2 * c + j < nx) sx[j] = p.db.xexp[p.rb.perm[pos0 + j] / a.k];
       }
+      // this warp's block scales of unit u (lane j: K block kb0 + j).  Loaded a
+      // unit ahead: ordinary global loads wait thousands of cycles while the
+      // weight stream is in flight, so each group fetches its next unit's
+      // scales while it computes the current one.
+      auto scales_of = [&](long u, float& g_, float& u_) {
+        const int i0u = (int)(u % upe) * R;
+        const uint16_t* gr_ = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)(i0u / 128) * a.s13_row;
+        const uint16_t* ur_ = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)((a.I + i0u) / 128) * a.s13_row;
+        g_ = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(gr_ + kb0 + lane)) : 0.f;
+        u_ = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(ur_ + kb0 + lane)) : 0.f;
+      };
+      long next_u = wk.seg_b + ((gr - m) & 1);   // this group's first unit of the pass
+      float next_g = 0.f, next_up = 0.f;
+      if (next_u < wk.seg_e) scales_of(next_u, next_g, next_up);
       if (!warp_wait(&S.afull[b], (gen >> 1) & 1, lane)) MOE_FAIL();
       for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
         if ((m & 1) != gr) continue;   // the other group's unit
         const int i0 = (int)(u % upe) * R;
-        // this warp's block scales of the unit: lane j holds K block kb0 + j
-        const uint16_t* sg_row = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)(i0 / 128) * a.s13_row;
-        const uint16_t* su_row = a.w13s + (int64_t)wk.e * a.s13_exp + (int64_t)((a.I + i0) / 128) * a.s13_row;
-        const float sgl = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(sg_row + kb0 + lane)) : 0.f;
-        const float sul = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(su_row + kb0 + lane)) : 0.f;
+        float sgl, sul;
+        if (u == next_u) {
+          sgl = next_g;
+          sul = next_up;
+        } else {
+          scales_of(u, sgl, sul);
+        }
+        next_u = u + 2;
+        if (next_u < wk.seg_e) scales_of(next_u, next_g, next_up);
         const int slot = m % NS;
         if (!warp_wait(&S.full[slot], (m / NS) & 1, lane)) MOE_FAIL();
         const uint8_t* st = S.ring + slot * cfg.SB;
@@ -770,6 +788,16 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
           }
         }
       }
+      // this warp's block scales of unit u (lane j: K block kb0 + j), loaded a
+      // unit ahead (see the GEMM1 consumers)
+      auto scales_of = [&](long u) -> float {
+        if (ROWS && wq * 16 >= R2) return 0.f;   // no rows for this warp in a narrow unit
+        const int n0u = (int)(u % upe) * R2 + (ROWS ? wq * 16 : 0);
+        const uint16_t* sr = a.w2s + (int64_t)wk.e * a.s2_exp + (int64_t)(n0u / 128) * a.s2_row;
+        return kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(sr + kb0 + lane)) : 0.f;
+      };
+      long next_u = wk.seg_b + ((gr - m) & 1);   // this group's first unit of the pass
+      float next_s = next_u < wk.seg_e ? scales_of(next_u) : 0.f;
       if (!warp_wait(&S.afull[0], gen & 1, lane)) return fail();
       // per-slot scale exponents from the row maxima (every warp computes them)
       int es[4] = {0, 0, 0, 0};
@@ -821,8 +849,14 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
       for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
         if ((m & 1) != gr) continue;
         const int n0 = (int)(u % upe) * R2 + (ROWS ? wq * 16 : 0);
-        const uint16_t* srow = a.w2s + (int64_t)wk.e * a.s2_exp + (int64_t)(n0 / 128) * a.s2_row;
-        const float sl = kb0 + lane < kb1 ? bf16_bits_to_f32(__ldg(srow + kb0 + lane)) : 0.f;
+        float sl;
+        if (u == next_u) {
+          sl = next_s;
+        } else {
+          sl = scales_of(u);
+        }
+        next_u = u + 2;
+        if (next_u < wk.seg_e) next_s = scales_of(next_u);
         const int slot = m % NS;
         if (!warp_wait(&S.full[slot], (m / NS) & 1, lane)) return fail();
         if (ROWS && wq * 16 >= R2) {   // a unit narrower than four tiles: nothing for this warp
