@@ -62,7 +62,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   L.meta = take(16 * (size_t)(g > 0 ? g : 1));
   L.mtp = take(4 * (size_t)(E + 1));
   L.mtp2 = take(4 * (size_t)(E + 1));
-  L.rcnt = take(4 * (size_t)route_chunks((int)S) * (size_t)E);
+  L.rcnt = take(8 * (size_t)route_chunks((int)S) * (size_t)E);   // chunk histograms + chunk bases
   if (path == MOE_PATH_DECODE) {
     L.xh = take(2 * (size_t)(T * H));
     L.xexp = take(4 * (size_t)T);
@@ -510,7 +510,7 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, 
   if ((rc = device_ok(&dev))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  const size_t scratch_bytes = 4 * (size_t)route_chunks((int)S) * (size_t)E;
+  const size_t scratch_bytes = 8 * (size_t)route_chunks((int)S) * (size_t)E;
   if ((rc = get_workspace(st, 256 + scratch_bytes, &ws))) return rc;
   RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr, nullptr};
   int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);

@@ -92,10 +92,10 @@ bool stage_mark(cudaStream_t st, int i);
 cudaError_t note_error(cudaError_t e, const char* stage);
 cudaError_t launch_check(cudaError_t launch_err, cudaStream_t st, const char* stage);
 
-// Routing lists.  With `scratch` (route_chunks(S) * E ints) large slot
+// Routing lists.  With `scratch` (2 * route_chunks(S) * E ints) large slot
 // counts use the three-kernel route; without it one CTA does everything.
 // Adds the number of launches to *launches (if given).
-constexpr int kRouteSingleMax = 16384;   // slots one CTA handles
+constexpr int kRouteSingleMax = 2048;    // slots one CTA handles
 constexpr int kRouteChunk = 1024;        // slots per chunk of the three-kernel route
 constexpr int kRouteMaxChunks = 512;
 int route_chunks(int S);

@@ -50,27 +50,32 @@ __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restr
   if (threadIdx.x == 0 && bad) raise_status(status, MOE_STATUS_BAD_ID);
 }
 
-// One CTA: cnt[c][e] -> first output position of chunk c's slots of expert
-// e; expert-level lists.
-__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ cnt, int G, int S, int E,
+// One CTA: chunk histograms cnt[c][e] -> cbase[c][e], the first output
+// position of chunk c's slots of expert e, and the expert-level lists.  Two
+// read-only passes over cnt (totals, then running prefixes) whose loads do
+// not depend on earlier stores, so each thread keeps many in flight.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ cnt,
+                                                          int32_t* __restrict__ cbase, int G, int S, int E,
                                                           RouteBufs rb) {
   extern __shared__ int eoff[];
   pdl_wait();
   pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-    for (int c = 0; c < G; ++c) {
-      const int v = cnt[(int64_t)c * E + e];
-      cnt[(int64_t)c * E + e] = run;
-      run += v;
-    }
+#pragma unroll 8
+    for (int c = 0; c < G; ++c) run += __ldg(cnt + (int64_t)c * E + e);
     eoff[e] = run;
   }
   __syncthreads();
-  route_expert_scan(eoff, E, S, rb);
+  route_expert_scan(eoff, E, S, rb);   // eoff[e] becomes expert e's first position
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int off = eoff[e];
-    for (int c = 0; c < G; ++c) cnt[(int64_t)c * E + e] += off;
+    int run = eoff[e];
+#pragma unroll 8
+    for (int c = 0; c < G; ++c) {
+      const int v = __ldg(cnt + (int64_t)c * E + e);
+      cbase[(int64_t)c * E + e] = run;
+      run += v;
+    }
   }
 }
 
@@ -131,10 +136,12 @@ cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, 
   if ((err = launch_k(route_count_kernel, dim3(G), dim3(256), (size_t)E * 4, st, false, ids, S, E, chunk, scratch,
                       status)))
     return err;
-  if ((err = launch_k(route_scan_kernel, dim3(1), dim3(1024), (size_t)E * 4, st, true, scratch, G, S, E, rb)))
+  int32_t* cbase = scratch + (int64_t)G * E;
+  if ((err = launch_k(route_scan_kernel, dim3(1), dim3(1024), (size_t)E * 4, st, true, (const int32_t*)scratch,
+                      cbase, G, S, E, rb)))
     return err;
   if ((err = launch_k(route_place_kernel, dim3(G), dim3(nt), psm, st, true, ids, S, E, chunk,
-                      (const int32_t*)scratch, rb)))
+                      (const int32_t*)cbase, rb)))
     return err;
   if (launches) *launches += 3;
   return cudaSuccess;
