@@ -2,13 +2,21 @@
 
 One step = one forward at each batch size of the decode workload with small
 fine-grained experts (E=128, H=2048, I=512, top_k=8, T in {1,2,4,8,16}, down
-scales padded to stride 8), on seeded synthetic inputs resident in HBM, L2
-flushed (256 MiB write) before every forward.  The metric is the decode
-routed-weight HBM bandwidth: bytes of the distinct routed experts' e4m3
-weights and valid bf16 block scales, divided by the device time of the
-forwards (CUDA events on the launching stream).
+scales padded to stride 8), on seeded synthetic inputs resident in HBM.  The
+metric is the decode routed-weight HBM bandwidth: bytes of the distinct
+routed experts' e4m3 weights and valid bf16 block scales, divided by the
+device time of the forwards (CUDA events on the launching stream).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+No forward finds its weights in L2.  Two ways to ensure it (--l2):
+  rotate (default): consecutive forwards read different copies of the weight
+      banks, as the layers of a model do (16 copies, 6.4 GB, far larger
+      than L2); nothing else runs between forwards.
+  flush: one weight bank; a 256 MiB buffer is written before every forward.
+      The written lines sit dirty in L2, so the forward's reads also pay for
+      their write-back to HBM.
+The line reports the chosen mode as `value` and the other one beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--l2 rotate|flush]
 
 --impl reference times the float64 CPU oracle (the only baseline the pages
 allow here) on a bounded sample of the same workload.  Under torchrun
@@ -39,6 +47,7 @@ DECODE_TS = [1, 2, 4, 8, 16]
 SHAPE = syn.DECODE_SMALL
 WORKLOAD = "decode E=128 H=2048 I=512 top_k=8 T={1,2,4,8,16} w2-scale stride 8"
 METRIC = "decode routed-weight HBM GB/s"
+N_LAYERS = 16   # weight-bank copies in --l2 rotate
 
 
 def routed_bytes(shape: syn.MoeShape, ids: torch.Tensor) -> tuple[int, int]:
@@ -229,6 +238,55 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+class Feed:
+    """The inputs of forward number j and what runs before it (--l2)."""
+
+    def __init__(self, probs, mode: str, dev):
+        self.probs, self.mode, self.j = probs, mode, 0
+        self.banks = None
+        if mode == "rotate":
+            p = probs[DECODE_TS[0]]
+            bank0 = (p["w13"], p["w13_scale"], p["w2"], p["w2_scale"])
+            self.banks = [bank0] + [tuple(t.clone() for t in bank0) for _ in range(N_LAYERS - 1)]
+        props = torch.cuda.get_device_properties(dev)
+        self.flush = torch.empty(max(256 << 20, 2 * getattr(props, "L2_cache_size", 128 << 20)),
+                                 dtype=torch.uint8, device=dev) if mode == "flush" else None
+
+    def next(self, T):
+        """Run the pre-forward step (flush mode) and return forward j's problem."""
+        j, self.j = self.j, self.j + 1
+        if self.mode == "flush":
+            self.flush.zero_()
+            return self.probs[T]
+        w = self.banks[j % N_LAYERS]
+        return dict(self.probs[T], w13=w[0], w13_scale=w[1], w2=w[2], w2_scale=w[3])
+
+    def describe(self) -> str:
+        if self.mode == "flush":
+            return "flushed (256 MiB write) before every forward"
+        return f"weights rotated over {N_LAYERS} copies of the banks ({N_LAYERS * bank_bytes() / 1e9:.1f} GB); no flush"
+
+
+def bank_bytes() -> int:
+    E, H, I = SHAPE.E, SHAPE.H, SHAPE.I
+    return E * 3 * H * I
+
+
+def timed_forwards(feed, s, outs, steps):
+    """Median-free device time of `steps` steps: {T: [ms per forward]}."""
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
+          for _ in range(steps)]
+    with torch.cuda.stream(s):
+        for k in range(steps):
+            for i, T in enumerate(DECODE_TS):
+                prob = feed.next(T)
+                ev[k][i][0].record(s)
+                api.forward_problem(prob, out=outs[T], stream=s, force_path="decode")
+                ev[k][i][1].record(s)
+    s.synchronize()
+    return {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)] for i, T in enumerate(DECODE_TS)}
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
@@ -236,16 +294,12 @@ def run_ours(args, world, rank, local):
     probs = make_problems(dev)
     s = torch.cuda.Stream(device=dev)
     api.moe_fp8_block_reserve(max(DECODE_TS), SHAPE.k, SHAPE.H, SHAPE.I, SHAPE.E, stream=s)
-    props = torch.cuda.get_device_properties(dev)
-    flush = torch.empty(max(256 << 20, 2 * getattr(props, "L2_cache_size", 128 << 20)), dtype=torch.uint8,
-                        device=dev)
+    feed = Feed(probs, args.l2, dev)
+    alt = Feed(probs, "flush" if args.l2 == "rotate" else "rotate", dev)
     outs = {T: torch.empty(T, SHAPE.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
     info = {T: routed_bytes(SHAPE, probs[T]["topk_ids"]) for T in DECODE_TS}
     step_bytes = sum(b for _, b in info.values())
     step_tokens = sum(DECODE_TS)
-
-    def fwd(T):
-        api.forward_problem(probs[T], out=outs[T], stream=s, force_path="decode")
 
     clocks = Clocks(local)
     clocks.start()
@@ -254,42 +308,37 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
             for T in DECODE_TS:
-                flush.zero_()
-                fwd(T)
+                api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode")
     s.synchronize()
     launches_per_step = 0
     for T in DECODE_TS:
         with torch.cuda.stream(s):
-            fwd(T)
+            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode")
         launches_per_step += api.moe_fp8_block_last_launches()
     s.synchronize()
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    with torch.cuda.stream(s):
-        for k in range(args.steps):
-            for i, T in enumerate(DECODE_TS):
-                flush.zero_()
-                ev[k][i][0].record(s)
-                fwd(T)
-                ev[k][i][1].record(s)
-    s.synchronize()
+    per_T = timed_forwards(feed, s, outs, args.steps)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     ck = clocks.stop()
-    per_T = {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i, T in enumerate(DECODE_TS)}
     dev_ms = sum(sum(v) for v in per_T.values())
     dev_ms_max = allreduce_max(dev_ms, world)
     total_bytes = allreduce_sum(step_bytes * args.steps, world)
     value = total_bytes / (dev_ms_max / 1e3) / 1e9
     tok_s = allreduce_sum(step_tokens * args.steps, world) / (dev_ms_max / 1e3)
+    # the same measurement with the other way of keeping weights out of L2
+    with torch.cuda.stream(s):
+        for T in DECODE_TS:
+            api.forward_problem(alt.next(T), out=outs[T], stream=s, force_path="decode")
+    alt_T = timed_forwards(alt, s, outs, args.steps)
+    alt_value = step_bytes * args.steps / (sum(sum(v) for v in alt_T.values()) / 1e3) / 1e9
 
     # dominant kernel (decode GEMM1) timed with CUDA events between the stages
-    st_ms = stage_durations(probs, s, flush, args.steps)
+    st_ms = stage_durations(feed, s, args.steps)
     g1_ms = {T: st_ms[T][1] for T in DECODE_TS}
     g1_bytes = {T: info[T][0] * (2 * SHAPE.I * SHAPE.H + 2 * (2 * SHAPE.I // 128) * (SHAPE.H // 128))
                 + T * SHAPE.H * 2 + T * SHAPE.k * SHAPE.I * 4 for T in DECODE_TS}
@@ -297,8 +346,8 @@ def run_ours(args, world, rank, local):
     hbm, _, src = peaks()
 
     # end to end through the host-buffer entry point (pinned host inputs/outputs)
-    e2e_v, h2d, d2h = e2e_hostio(probs, s, flush, args.steps, args.warmup)
-    prefill = prefill_leg(dev, s, flush, max(5, args.steps)) if not args.no_prefill else None
+    e2e_v, h2d, d2h = e2e_hostio(feed, s, args.steps, args.warmup)
+    prefill = prefill_leg(dev, s, max(5, args.steps)) if not args.no_prefill else None
 
     if rank != 0:
         return
@@ -311,9 +360,10 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xbf16->f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every forward",
+        "config": {"workload": WORKLOAD, "l2": feed.describe(),
                    "path": "decode (forced)", "replicas": world},
         "frac_of_hbm_peak": value / hbm, "peak_source": src,
+        "value_other_l2": {"l2": alt.describe(), "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
         "tok_per_s": tok_s,
         "per_T": {str(T): {"distinct_experts": info[T][0], "routed_MB": info[T][1] / 1e6,
                            "us": 1e3 * statistics.median(per_T[T]),
@@ -338,7 +388,7 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def stage_durations(probs, s, flush, steps):
+def stage_durations(feed, s, steps):
     """Median device time of each kernel of the decode path per T, from CUDA
     events the library records between its kernels (stage-timing mode:
     moe_fp8_block_set_stage_events).  Returns {T: [prep, gemm1, gemm2, combine]} in ms."""
@@ -355,20 +405,20 @@ def stage_durations(probs, s, flush, steps):
         times = []
         for _ in range(max(steps, 3)):
             with torch.cuda.stream(s):
-                flush.zero_()
+                prob = feed.next(T)
                 _lib.check(lib.moe_fp8_block_set_stage_events(arr, 5), "set_stage_events")
-                api.forward_problem(probs[T], stream=s, force_path="decode")
+                api.forward_problem(prob, stream=s, force_path="decode")
             s.synchronize()
             times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
         res[T] = [statistics.median(t[i] for t in times) for i in range(4)]
     return res
 
 
-def e2e_hostio(probs, s, flush, steps, warmup):
+def e2e_hostio(feed, s, steps, warmup):
+    probs = feed.probs
     host = {T: (probs[T]["hidden"].cpu().pin_memory(), probs[T]["topk_ids"].cpu().pin_memory(),
                 probs[T]["topk_weights"].cpu().pin_memory(),
                 torch.empty(T, SHAPE.H, dtype=torch.bfloat16).pin_memory()) for T in DECODE_TS}
-    w = probs[1]
     total_b, total_s = 0, 0.0
     h2d = sum(T * SHAPE.H * 2 + T * SHAPE.k * 8 for T in DECODE_TS)
     d2h = sum(T * SHAPE.H * 2 for T in DECODE_TS)
@@ -376,7 +426,7 @@ def e2e_hostio(probs, s, flush, steps, warmup):
         for T in DECODE_TS:
             hx, hi, hw, ho = host[T]
             with torch.cuda.stream(s):
-                flush.zero_()
+                w = feed.next(T)
             s.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
@@ -394,7 +444,7 @@ def e2e_hostio(probs, s, flush, steps, warmup):
 PREFILL_CASES = [(1024, "softmax"), (4096, "softmax"), (4096, "zipf"), (16384, "softmax"), (16384, "zipf")]
 
 
-def prefill_leg(dev, s, flush, reps):
+def prefill_leg(dev, s, reps):
     """Prefill grouped GEMM workload (E=128, H=2048, I=512, top_k=8): FP8
     TFLOPS = 6*T*k*H*I / forward time, per-kernel times from stage events."""
     import ctypes
@@ -402,6 +452,7 @@ def prefill_leg(dev, s, flush, reps):
     lib = _lib.load()
     shp = syn.PREFILL
     w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # prefill reads are compute-bound
     hbm_peak, bf16_peak, src = peaks()
     fp8_peak = 2.0 * bf16_peak
     # the least bytes a prefill forward moves: every expert's weights and valid
@@ -549,6 +600,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
+    ap.add_argument("--l2", choices=("rotate", "flush"), default="rotate",
+                    help="how forwards are kept from finding their weights in L2 (see the module docstring)")
     ap.add_argument("--gate-sweep", choices=tuple(SWEEPS), default=None,
                     help="time decode against prefill for r = T*k/E up to 1.0 on one layer (one JSON object)")
     ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
