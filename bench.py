@@ -272,10 +272,20 @@ def bank_bytes() -> int:
     return E * 3 * H * I
 
 
+def hold_stream(s, ms: float):
+    """Occupy stream s with a bounded spin kernel of about `ms` milliseconds,
+    so that the host queues the launches that follow before the device
+    reaches them: a forward's events then time the device work, not the
+    host's launch overhead (the decode forwards are tens of microseconds)."""
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(int(ms * 2.0e6))
+
+
 def timed_forwards(feed, s, outs, steps):
-    """Median-free device time of `steps` steps: {T: [ms per forward]}."""
+    """Device time of every forward of `steps` steps: {T: [ms per forward]}."""
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
           for _ in range(steps)]
+    hold_stream(s, 2.0 + 0.5 * steps * len(DECODE_TS))
     with torch.cuda.stream(s):
         for k in range(steps):
             for i, T in enumerate(DECODE_TS):
@@ -404,6 +414,7 @@ def stage_durations(feed, s, steps):
         arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
         times = []
         for _ in range(max(steps, 3)):
+            hold_stream(s, 1.0)
             with torch.cuda.stream(s):
                 prob = feed.next(T)
                 _lib.check(lib.moe_fp8_block_set_stage_events(arr, 5), "set_stage_events")
