@@ -15,6 +15,9 @@ No forward finds its weights in L2.  Two ways to ensure it (--l2):
       The written lines sit dirty in L2, so the forward's reads also pay for
       their write-back to HBM.
 The line reports the chosen mode as `value` and the other one beside it.
+Each timed forward is a replay of a CUDA graph captured from the library
+call (one graph per batch size and weight bank), as a serving loop would
+run it; `value_eager` times the same forwards launched eagerly.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--l2 rotate|flush]
 
@@ -252,14 +255,25 @@ class Feed:
         self.flush = torch.empty(max(256 << 20, 2 * getattr(props, "L2_cache_size", 128 << 20)),
                                  dtype=torch.uint8, device=dev) if mode == "flush" else None
 
-    def next(self, T):
-        """Run the pre-forward step (flush mode) and return forward j's problem."""
+    def n_banks(self) -> int:
+        return N_LAYERS if self.mode == "rotate" else 1
+
+    def problem(self, T, bank):
+        if self.mode == "flush":
+            return self.probs[T]
+        w = self.banks[bank]
+        return dict(self.probs[T], w13=w[0], w13_scale=w[1], w2=w[2], w2_scale=w[3])
+
+    def next_bank(self):
+        """Run the pre-forward step (flush mode) and return forward j's weight bank."""
         j, self.j = self.j, self.j + 1
         if self.mode == "flush":
             self.flush.zero_()
-            return self.probs[T]
-        w = self.banks[j % N_LAYERS]
-        return dict(self.probs[T], w13=w[0], w13_scale=w[1], w2=w[2], w2_scale=w[3])
+        return j % self.n_banks()
+
+    def next(self, T):
+        """Run the pre-forward step (flush mode) and return forward j's problem."""
+        return self.problem(T, self.next_bank())
 
     def describe(self) -> str:
         if self.mode == "flush":
@@ -281,17 +295,39 @@ def hold_stream(s, ms: float):
         torch.cuda._sleep(int(ms * 2.0e6))
 
 
-def timed_forwards(feed, s, outs, steps):
-    """Device time of every forward of `steps` steps: {T: [ms per forward]}."""
+def capture_forwards(feed, s, outs):
+    """One CUDA graph per (T, weight bank) of the library's forward, captured
+    on stream s (the library is capture-safe once its workspace is sized):
+    replays launch the forward's kernels without host work in between."""
+    graphs = {}
+    for T in DECODE_TS:
+        for bank in range(feed.n_banks()):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode")
+            graphs[(T, bank)] = g
+    with torch.cuda.stream(s):
+        for g in graphs.values():
+            g.replay()
+    s.synchronize()
+    return graphs
+
+
+def timed_forwards(feed, s, outs, steps, graphs=None):
+    """Device time of every forward of `steps` steps: {T: [ms per forward]}.
+    With `graphs`, each forward is a replay of its captured graph."""
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
           for _ in range(steps)]
     hold_stream(s, 2.0 + 0.5 * steps * len(DECODE_TS))
     with torch.cuda.stream(s):
         for k in range(steps):
             for i, T in enumerate(DECODE_TS):
-                prob = feed.next(T)
+                bank = feed.next_bank()
                 ev[k][i][0].record(s)
-                api.forward_problem(prob, out=outs[T], stream=s, force_path="decode")
+                if graphs is not None:
+                    graphs[(T, bank)].replay()
+                else:
+                    api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode")
                 ev[k][i][1].record(s)
     s.synchronize()
     return {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)] for i, T in enumerate(DECODE_TS)}
@@ -327,10 +363,13 @@ def run_ours(args, world, rank, local):
         launches_per_step += api.moe_fp8_block_last_launches()
     s.synchronize()
 
+    graphs = capture_forwards(feed, s, outs) if not args.no_graph else None
+    alt_graphs = capture_forwards(alt, s, outs) if not args.no_graph else None
+
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    per_T = timed_forwards(feed, s, outs, args.steps)
+    per_T = timed_forwards(feed, s, outs, args.steps, graphs)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
@@ -344,8 +383,11 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(s):
         for T in DECODE_TS:
             api.forward_problem(alt.next(T), out=outs[T], stream=s, force_path="decode")
-    alt_T = timed_forwards(alt, s, outs, args.steps)
+    alt_T = timed_forwards(alt, s, outs, args.steps, alt_graphs)
     alt_value = step_bytes * args.steps / (sum(sum(v) for v in alt_T.values()) / 1e3) / 1e9
+    # and with eager launches instead of graph replays
+    eager_T = timed_forwards(feed, s, outs, args.steps)
+    eager_value = step_bytes * args.steps / (sum(sum(v) for v in eager_T.values()) / 1e3) / 1e9
 
     # dominant kernel (decode GEMM1) timed with CUDA events between the stages
     st_ms = stage_durations(feed, s, args.steps)
@@ -371,9 +413,11 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xbf16->f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": feed.describe(),
+                   "launch": "CUDA graph replay per forward" if graphs is not None else "eager",
                    "path": "decode (forced)", "replicas": world},
         "frac_of_hbm_peak": value / hbm, "peak_source": src,
         "value_other_l2": {"l2": alt.describe(), "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
+        "value_eager": {"launch": "eager (no CUDA graph)", "value": eager_value, "frac_of_hbm_peak": eager_value / hbm},
         "tok_per_s": tok_s,
         "per_T": {str(T): {"distinct_experts": info[T][0], "routed_MB": info[T][1] / 1e6,
                            "us": 1e3 * statistics.median(per_T[T]),
@@ -611,6 +655,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays of each forward")
     ap.add_argument("--l2", choices=("rotate", "flush"), default="rotate",
                     help="how forwards are kept from finding their weights in L2 (see the module docstring)")
     ap.add_argument("--gate-sweep", choices=tuple(SWEEPS), default=None,
