@@ -71,6 +71,11 @@ constexpr int kGW = 4;                 // warps per group (they split K)
 constexpr int kNWC = kGroups * kGW;    // consumer warps
 constexpr int kThreads = 32 * (kNWC + 1);
 constexpr int kSmemLimit = 232448;
+// Weight copies issued before the wait for the previous kernel.  A bulk
+// copy's issue blocks while the SM's copy engine is busy, so copies issued
+// early also delay the activation (x or h) copy behind them, which the first
+// unit needs as much as its weights: only the first two go out early.
+constexpr int kPreIssue = 2;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
@@ -479,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
     if (wk.u < wk.ue) {
       const int d0 = (int)(wk.u / upe);
       const int e0 = expert_select(eb, d0, lane);
-      const long n = min((long)NS, min(wk.ue, (long)(d0 + 1) * upe) - wk.u);
+      const long n = min((long)kPreIssue, min(wk.ue, (long)(d0 + 1) * upe) - wk.u);
       if (lane == 0 && e0 >= 0)
         for (long i = 0; i < n; ++i) {
           const int i0 = (int)((wk.u + i) % upe) * R;
@@ -967,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     {
       Walk w0 = wk;
       if (walk_next_segment(p, w0, SPP)) {
-        const long n = min((long)NS, w0.seg_e - w0.seg_b);
+        const long n = min((long)kPreIssue, w0.seg_e - w0.seg_b);
         if (lane == 0)
           for (long i = 0; i < n; ++i) {
             const int n0 = (int)((w0.seg_b + i) % upe) * R2;
