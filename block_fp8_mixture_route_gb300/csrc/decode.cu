@@ -315,10 +315,12 @@ __device__ __forceinline__ int expert_select(const ExpertBits& eb, int d, int la
   return owner ? __shfl_sync(0xffffffffu, e, __ffs(owner) - 1) : -1;
 }
 
-// Rows per unit after halving until every SM gets enough units to balance
-// (the count of routed experts D is only known on the device).
+// Rows per unit: halved only while there are fewer units than SMs (the
+// count of routed experts D is only known on the device).  Larger units
+// stream better than more SMs each holding small ones: requiring 6 units per
+// SM instead made the decode workload 4% slower, and 25% slower at T=1.
 __device__ __forceinline__ int balanced_rows(int R, int min_rows, int rows_total, int D, int G) {
-  while (R > min_rows && (long)D * (rows_total / R) < 6L * G) R >>= 1;
+  while (R > min_rows && (long)D * (rows_total / R) < (long)G) R >>= 1;
   return R;
 }
 
