@@ -1041,16 +1041,30 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs p) {
   const int t = blockIdx.x;
   const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (n >= a.H) return;
+  // slots in chunks of 8: the chunk's ids, then all its row loads, then the
+  // sums in slot order (the loads are in flight together instead of one
+  // dependent id + row pair after another)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < a.k; ++j) {
-    const int s = t * a.k + j;
-    const int id = a.ids[s];
-    if (id < 0 || id >= a.E) continue;
-    const float4 v = *reinterpret_cast<const float4*>(p.db.ybuf + (int64_t)s * a.H + n);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    const int64_t s0 = (int64_t)t * a.k + j0;
+    bool use[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int id = j0 + q < a.k ? a.ids[s0 + q] : -1;
+      use[q] = id >= 0 && id < a.E;
+    }
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = use[q] ? *reinterpret_cast<const float4*>(p.db.ybuf + (s0 + q) * a.H + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!use[q]) continue;
+      acc.x += v[q].x;
+      acc.y += v[q].y;
+      acc.z += v[q].z;
+      acc.w += v[q].w;
+    }
   }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);

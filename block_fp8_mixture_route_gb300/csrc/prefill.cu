@@ -693,18 +693,31 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillArgs p) {
   const int t = blockIdx.x;
   const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (n >= a.H) return;
+  // slots in chunks of 8: the chunk's rows and weights, then all its row
+  // loads, then the sums in slot order (the loads are in flight together)
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < a.k; ++j) {
-    const int s = t * a.k + j;
-    const int row = p.pb.pinv[s];
-    if (row < 0) continue;
-    const float w = a.wts[s];
-    const uint4 v = *reinterpret_cast<const uint4*>(p.pb.ys + (int64_t)row * a.H + n);
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    const int64_t s0 = (int64_t)t * a.k + j0;
+    int row[8];
+    float w[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(w, bf16_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(w, bf16_to_f32(u[i] >> 16), acc[2 * i + 1]);
+    for (int q = 0; q < 8; ++q) {
+      row[q] = j0 + q < a.k ? p.pb.pinv[s0 + q] : -1;
+      w[q] = j0 + q < a.k ? a.wts[s0 + q] : 0.f;
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = row[q] >= 0 ? *reinterpret_cast<const uint4*>(p.pb.ys + (int64_t)row[q] * a.H + n) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (row[q] < 0) continue;
+      const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w[q], bf16_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w[q], bf16_to_f32(u[i] >> 16), acc[2 * i + 1]);
+      }
     }
   }
   uint32_t o[4];
