@@ -168,6 +168,16 @@ def allreduce_sum(x: float, world: int) -> float:
     return float(t.item())
 
 
+def aggregate(step_bytes: int, step_tokens: int, steps: int, dev_ms: float, world: int):
+    """Whole-job numbers of the replicas: bytes and tokens summed over the
+    ranks, device time the maximum over them.  Returns (GB/s, tokens/s,
+    max ms)."""
+    dev_ms_max = allreduce_max(dev_ms, world)
+    total_bytes = allreduce_sum(step_bytes * steps, world)
+    total_tokens = allreduce_sum(step_tokens * steps, world)
+    return total_bytes / (dev_ms_max / 1e3) / 1e9, total_tokens / (dev_ms_max / 1e3), dev_ms_max
+
+
 # ----------------------------------------------------------------- oracle
 def oracle_sample(problems, budget_s: float = 12.0):
     """Time the float64 oracle (gathered mode) on whole forwards of the
@@ -375,10 +385,7 @@ def run_ours(args, world, rank, local):
     wall = time.perf_counter() - t_wall
     ck = clocks.stop()
     dev_ms = sum(sum(v) for v in per_T.values())
-    dev_ms_max = allreduce_max(dev_ms, world)
-    total_bytes = allreduce_sum(step_bytes * args.steps, world)
-    value = total_bytes / (dev_ms_max / 1e3) / 1e9
-    tok_s = allreduce_sum(step_tokens * args.steps, world) / (dev_ms_max / 1e3)
+    value, tok_s, dev_ms_max = aggregate(step_bytes, step_tokens, args.steps, dev_ms, world)
     # the same measurement with the other way of keeping weights out of L2
     with torch.cuda.stream(s):
         for T in DECODE_TS:
