@@ -33,6 +33,10 @@ What it computes, step by step (float64 unless a step says otherwise):
    y = W2 h (fp8-moe-gather page, "The fix": down projection in fp32; here
    float64).  In W8A8 mode h is itself quantised per 128-group by the rule
    of step 3 (float64 h rounded to fp32 first) before the down projection.
+   The W8A8 decode mode (the Gaudi path of the fp8-moe-gather page, "The
+   fix": dynamic activation scales and an FP8 GEMM for the up/gate
+   projection, the down projection in fp32) quantises the activations by
+   step 3 and keeps h unquantised.
 5. Combine: out_t = sum_j w[t,j] * y_{ids[t,j]}(x_t).  The all-expert
    evaluation (the stock mixture_of_experts op of the fp8-moe-gather page,
    "Problem", reads every expert) computes y_e for every expert and masks
@@ -167,7 +171,8 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 def expert_forward(a: np.ndarray, w13_codes, w13_scale, w2_codes, w2_scale, act: str) -> np.ndarray:
     """y = W2 h(a) for one expert and a batch of activation rows a [n, H]
-    (float64, already dequantised in W8A8 mode)."""
+    (float64, already dequantised in the W8A8 modes).  h is quantised only
+    in act == "e4m3" (prefill W8A8)."""
     I = w13_codes.shape[0] // 2
     W13 = dequant_bank(w13_codes, w13_scale)       # [2I, H]
     gate = a @ W13[:I].T                            # [n, I]
@@ -185,7 +190,7 @@ def activations(hidden_bf16: np.ndarray, act: str) -> np.ndarray:
     x = bf16_bits_to_f64(hidden_bf16)
     if act == "bf16":
         return x
-    if act == "e4m3":
+    if act in ("e4m3", "e4m3_x"):
         codes, scales = quantize_per_128(x.astype(np.float32))
         return dequantize_per_128(codes, scales)
     raise ValueError(act)
@@ -200,7 +205,9 @@ def forward(hidden_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
     [T, k]; w13: uint8 [E, 2I, H]; w13_scale: uint16 [E, 2I/128, >= H/128];
     w2: uint8 [E, H, I]; w2_scale: uint16 [E, H/128, >= I/128].
     mode: "gathered" (routed experts only) or "all" (every expert, masked).
-    act: "bf16" (W8A16) or "e4m3" (W8A8, dynamic per-token-per-128 scales).
+    act: "bf16" (W8A16), "e4m3" (W8A8, dynamic per-token-per-128 scales,
+    h quantised the same way) or "e4m3_x" (W8A8 decode: activations
+    quantised, h kept in float64 for the down projection).
     tokens: optional subset of token indices (all by default).
     """
     E = w13.shape[0]

@@ -254,7 +254,7 @@ def _np_args(prob):
     return out
 
 
-@pytest.mark.parametrize("act", ["bf16", "e4m3"])
+@pytest.mark.parametrize("act", ["bf16", "e4m3", "e4m3_x"])
 def test_gathered_equals_all_expert(act):
     """The gathered path equals the all-expert op (fp8-moe-gather page, The
     fix / VERIFY mode) on the tiny 8-expert, 256-hidden problem."""
@@ -344,7 +344,7 @@ def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act):
     out = [[0.0] * H for _ in range(T)]
     for t in range(T):
         x = [bf(hidden_u16[t, c]) for c in range(H)]
-        if act == "e4m3":
+        if act in ("e4m3", "e4m3_x"):
             x = sum((quant_row(x[c:c + 128]) for c in range(0, H, 128)), [])
         for j in range(ids.shape[1]):
             e = int(ids[t, j])
@@ -363,7 +363,7 @@ def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act):
     return np.array(out)
 
 
-@pytest.mark.parametrize("act", ["bf16", "e4m3"])
+@pytest.mark.parametrize("act", ["bf16", "e4m3", "e4m3_x"])
 def test_brute_force_tiny(act):
     shp = syn.MoeShape(E=3, H=128, I=128, k=2, w2_scale_stride=3)
     prob = syn.make_problem(shp, T=2, seed=11)
@@ -373,6 +373,27 @@ def test_brute_force_tiny(act):
     got = mo.forward(*a, act=act)
     scale = np.max(np.abs(ref), axis=1, keepdims=True)
     assert np.all(np.abs(got - ref) <= 1e-12 * scale)
+
+
+def test_w8a8_decode_equals_w8a16_on_the_e4m3_grid():
+    """Activations that are e4m3 codes times 2^-4, with a 448 (0x7E) code in
+    every 128-group, quantise exactly (scale = 28 / 448 = 2^-4, x / scale =
+    the code's value): the W8A8 decode mode must then equal W8A16 exactly,
+    while the prefill W8A8 mode, which also quantises h, must not."""
+    shp = syn.MoeShape(E=4, H=256, I=128, k=2)
+    prob = syn.make_problem(shp, T=3, seed=5)
+    g = torch.Generator().manual_seed(3)
+    codes = torch.tensor(FINITE, dtype=torch.uint8)[torch.randint(0, len(FINITE), (3, 256), generator=g)]
+    codes[:, ::128] = 0x7E
+    x = (codes.view(torch.float8_e4m3fn).to(torch.float32) * 2.0 ** -4).to(torch.bfloat16)
+    assert torch.equal(x.float(), codes.view(torch.float8_e4m3fn).to(torch.float32) * 2.0 ** -4)
+    a = _np_args(prob)
+    a[0] = bits(x)
+    w8a16 = mo.forward(*a, act="bf16")
+    w8a8_dec = mo.forward(*a, act="e4m3_x")
+    w8a8_pf = mo.forward(*a, act="e4m3")
+    assert np.array_equal(w8a8_dec, w8a16)
+    assert not np.array_equal(w8a8_pf, w8a16)
 
 
 # ------------------------------------------------------- routing lists ---
