@@ -323,7 +323,7 @@ def capture_forwards(feed, s, outs):
     return graphs
 
 
-def timed_forwards(feed, s, outs, steps, graphs=None):
+def timed_forwards(feed, s, outs, steps, graphs=None, decode_act=None):
     """Device time of every forward of `steps` steps: {T: [ms per forward]}.
     With `graphs`, each forward is a replay of its captured graph."""
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
@@ -337,7 +337,8 @@ def timed_forwards(feed, s, outs, steps, graphs=None):
                 if graphs is not None:
                     graphs[(T, bank)].replay()
                 else:
-                    api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode")
+                    api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode",
+                                        decode_act=decode_act)
                 ev[k][i][1].record(s)
     s.synchronize()
     return {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)] for i, T in enumerate(DECODE_TS)}
@@ -395,6 +396,13 @@ def run_ours(args, world, rank, local):
     # and with eager launches instead of graph replays
     eager_T = timed_forwards(feed, s, outs, args.steps)
     eager_value = step_bytes * args.steps / (sum(sum(v) for v in eager_T.values()) / 1e3) / 1e9
+    # the decode path's W8A8 mode (activations quantised per token per 128
+    # columns), eager launches
+    with torch.cuda.stream(s):
+        for T in DECODE_TS:
+            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_act="e4m3")
+    w8a8_T = timed_forwards(feed, s, outs, args.steps, decode_act="e4m3")
+    w8a8_value = step_bytes * args.steps / (sum(sum(v) for v in w8a8_T.values()) / 1e3) / 1e9
 
     # dominant kernel (decode GEMM1) timed with CUDA events between the stages
     st_ms = stage_durations(feed, s, args.steps)
@@ -425,6 +433,8 @@ def run_ours(args, world, rank, local):
         "frac_of_hbm_peak": value / hbm, "peak_source": src,
         "value_other_l2": {"l2": alt.describe(), "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
         "value_eager": {"launch": "eager (no CUDA graph)", "value": eager_value, "frac_of_hbm_peak": eager_value / hbm},
+        "value_w8a8": {"decode_act": "e4m3 (W8A8), eager", "value": w8a8_value, "frac_of_hbm_peak": w8a8_value / hbm,
+                       "us": {str(T): 1e3 * statistics.median(w8a8_T[T]) for T in DECODE_TS}},
         "tok_per_s": tok_s,
         "per_T": {str(T): {"distinct_experts": info[T][0], "routed_MB": info[T][1] / 1e6,
                            "us": 1e3 * statistics.median(per_T[T]),

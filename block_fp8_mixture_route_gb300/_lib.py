@@ -12,7 +12,7 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe_fp8_block.so")
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 MOE_BF16, MOE_F32, MOE_E4M3, MOE_I32 = 1, 2, 3, 4
 MOE_PATH_NONE, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
@@ -49,7 +49,8 @@ class MoeOptions(ctypes.Structure):
     _fields_ = [
         ("gate_ratio", ctypes.c_float),
         ("force_path", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("decode_act", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 

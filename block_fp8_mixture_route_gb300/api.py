@@ -46,19 +46,23 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
-def _options(gate_ratio, force_path) -> Optional[MoeOptions]:
-    if gate_ratio is None and force_path is None:
+def _options(gate_ratio, force_path, decode_act=None) -> Optional[MoeOptions]:
+    if gate_ratio is None and force_path is None and decode_act is None:
         return None
     o = MoeOptions()
     o.gate_ratio = float(gate_ratio) if gate_ratio is not None else 0.0
     fp = {None: 0, "auto": 0, "decode": 1, "prefill": 2}
     o.force_path = fp[force_path] if not isinstance(force_path, int) else force_path
+    da = {None: 0, "bf16": 0, "e4m3": 1}
+    o.decode_act = da[decode_act] if not isinstance(decode_act, int) else decode_act
     return o
 
 
 def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
-                          w2_scale_stride, out=None, stream=None, gate_ratio=None, force_path=None):
-    """Layer forward on device tensors; returns `out` (bf16 [T, H])."""
+                          w2_scale_stride, out=None, stream=None, gate_ratio=None, force_path=None,
+                          decode_act=None):
+    """Layer forward on device tensors; returns `out` (bf16 [T, H]).
+    decode_act: "bf16" (W8A16, default) or "e4m3" (W8A8) for the decode path."""
     lib = _lib.load()
     if out is None:
         out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
@@ -66,7 +70,7 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
     a2 = [desc(w2), desc(w2_scale)]
     o = desc(out)
     P = ctypes.byref
-    opt = _options(gate_ratio, force_path)
+    opt = _options(gate_ratio, force_path, decode_act)
     if opt is None:
         rc = lib.moe_fp8_block_forward(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                        int(w2_scale_stride), P(o), _stream(stream))
@@ -79,7 +83,7 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
 
 def moe_fp8_block_forward_hostio(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
                                  w2_scale, w2_scale_stride, out=None, stream=None, gate_ratio=None,
-                                 force_path=None):
+                                 force_path=None, decode_act=None):
     """Layer forward with HOST hidden/ids/weights/out (pinned for async
     copies) and device weight banks; returns `out` once it is filled."""
     lib = _lib.load()
@@ -89,7 +93,7 @@ def moe_fp8_block_forward_hostio(hidden, topk_ids, topk_weights, w13, w13_scale,
     a2 = [desc(w2), desc(w2_scale)]
     o = desc(out)
     P = ctypes.byref
-    opt = _options(gate_ratio, force_path)
+    opt = _options(gate_ratio, force_path, decode_act)
     rc = lib.moe_fp8_block_forward_hostio(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                           int(w2_scale_stride), P(o), _stream(stream),
                                           P(opt) if opt is not None else None)

@@ -79,7 +79,16 @@ constexpr int kPreIssue = 2;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
+// Two fp32 values -> two e4m3 codes (lo -> low byte), RNE, saturating.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ------------------------------------------------------------- prep ----
+// ACT8: W8A8 activations (per-group e4m3 codes and scales); W8A16 otherwise.
+template <bool ACT8>
 __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
   extern __shared__ int smem_prep[];
   pdl_wait();
@@ -113,6 +122,38 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[c][j]));
     }
+  }
+  if (ACT8) {
+    // W8A8: per 128-column group (16 chunks, held by 16 consecutive
+    // threads) scale = amax / 448 and code = e4m3_rne_satfinite(x / scale),
+    // both IEEE fp32 divisions; the copy holds the codes' values (exact in
+    // f16) and the scales go to xs.  No token-wide exponent: xexp = 0.
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int i0 = (c * (int)blockDim.x + threadIdx.x) * 8;
+      const bool valid = i0 < a.H;
+      float gm = 0.f;
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gm = fmaxf(gm, fabsf(v[c][j]));
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+      if (valid) {
+        const float sc = __fdiv_rn(gm, 448.0f);
+        uint32_t o4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint16_t q = sc != 0.f ? e4m3x2_from_f32(__fdiv_rn(v[c][2 * j], sc), __fdiv_rn(v[c][2 * j + 1], sc))
+                                       : (uint16_t)0;
+          o4[j] = e4m3x2_to_f16x2(q);
+        }
+        *reinterpret_cast<uint4*>(p.db.xh + (int64_t)t * a.H + i0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        if ((threadIdx.x & 15) == 0) p.db.xs[(int64_t)t * (a.H / 128) + i0 / 128] = sc;
+      }
+    }
+    if (threadIdx.x == 0) p.db.xexp[t] = 0;
+    return;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -383,7 +424,9 @@ __device__ __forceinline__ void chunk_mma(float (&b0)[4], float (&b1)[4], const 
   mma_f16_16816(b1, A[3], x1.z, x1.w);
 }
 
-// GEMM1 unit, K slice of KW blocks per warp: the warp first copies all of
+// GEMM1 unit, K slice of KW blocks per warp (sa[j][kk]: the activation
+// scale of the lane's slot 2c + j in K block kb0 + kk, 1 in W8A16 mode, so
+// that the products there are exact): the warp first copies all of
 // its weight bytes of the unit from the ring stage into registers (16 bytes
 // per lane per 64-wide chunk and row) and releases the stage at once, so the
 // stage is held only for those loads, not for the MMAs.  The arrive has
@@ -392,7 +435,8 @@ __device__ __forceinline__ void chunk_mma(float (&b0)[4], float (&b1)[4], const 
 template <int KW>
 __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8_t* brow, const uint8_t* xrow,
                                                 int kb0, bool has_w, bool has_x, float sgl, float sul,
-                                                uint64_t* empty_bar, int lane, float (&acc)[4]) {
+                                                const float (&sa)[2][4], uint64_t* empty_bar, int lane,
+                                                float (&acc)[4]) {
   uint4 wa[2 * KW], wb[2 * KW];
 #pragma unroll
   for (int i = 0; i < 2 * KW; ++i) {
@@ -417,10 +461,10 @@ __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8
     }
     const float sg = __shfl_sync(0xffffffffu, sgl, j);
     const float su = __shfl_sync(0xffffffffu, sul, j);
-    acc[0] = fmaf(sg, b0[0] + b1[0], acc[0]);
-    acc[1] = fmaf(sg, b0[1] + b1[1], acc[1]);
-    acc[2] = fmaf(su, b0[2] + b1[2], acc[2]);
-    acc[3] = fmaf(su, b0[3] + b1[3], acc[3]);
+    acc[0] = fmaf(sg * sa[0][j], b0[0] + b1[0], acc[0]);
+    acc[1] = fmaf(sg * sa[1][j], b0[1] + b1[1], acc[1]);
+    acc[2] = fmaf(su * sa[0][j], b0[2] + b1[2], acc[2]);
+    acc[3] = fmaf(su * sa[1][j], b0[3] + b1[3], acc[3]);
   }
 }
 
@@ -438,6 +482,9 @@ __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8
 // rows as tile rows 8..8+R-1, so each lane ends with gate and up of the same
 // row pair.  The four warps of a group split the unit's K blocks; the
 // group's leader sums the partials and applies silu(gate)*up.
+// ACT8: W8A8 (the activation rows are e4m3 code values with per-group
+// scales); W8A16 otherwise.
+template <bool ACT8>
 __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamCfg& cfg = p.c1;
@@ -569,6 +616,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         for (int j = 0; j < 2; ++j)
           if (2 * c + j < nx) sx[j] = p.db.xexp[p.rb.perm[pos0 + j] / a.k];
       }
+      // W8A8: the activation group scales of slots 2c, 2c+1 over this warp's
+      // K blocks (1 in W8A16 mode and for slots past the pass)
+      float sa[2][4] = {{1.f, 1.f, 1.f, 1.f}, {1.f, 1.f, 1.f, 1.f}};
+      int stok[2] = {-1, -1};
+      if (ACT8) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (2 * c + j < nx) {
+            stok[j] = p.rb.perm[pos0 + j] / a.k;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              if (kb0 + kk < kb1) sa[j][kk] = p.db.xs[(int64_t)stok[j] * nkb + kb0 + kk];
+          }
+        }
+      }
       // this warp's block scales of unit u (lane j: K block kb0 + j).  Loaded a
       // unit ahead: ordinary global loads wait thousands of cycles while the
       // weight stream is in flight, so each group fetches its next unit's
@@ -605,10 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         const int kw = kb1 - kb0;
         if (kw >= 1 && kw <= 4) {
           switch (kw) {
-            case 1: gemm1_unit_regs<1>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
-            case 2: gemm1_unit_regs<2>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
-            case 3: gemm1_unit_regs<3>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
-            default: gemm1_unit_regs<4>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, &S.empty[slot], lane, acc); break;
+            case 1: gemm1_unit_regs<1>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            case 2: gemm1_unit_regs<2>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            case 3: gemm1_unit_regs<3>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            default: gemm1_unit_regs<4>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
           }
         } else {
 #pragma unroll 1
@@ -631,10 +693,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
           // the 128-wide K block is complete: apply its scales once
           const float sg = __shfl_sync(0xffffffffu, sgl, kb - kb0);
           const float su = __shfl_sync(0xffffffffu, sul, kb - kb0);
-          acc[0] = fmaf(sg, b0[0] + b1[0], acc[0]);
-          acc[1] = fmaf(sg, b0[1] + b1[1], acc[1]);
-          acc[2] = fmaf(su, b0[2] + b1[2], acc[2]);
-          acc[3] = fmaf(su, b0[3] + b1[3], acc[3]);
+          float a0 = 1.f, a1 = 1.f;
+          if (ACT8) {
+            if (stok[0] >= 0) a0 = __ldg(p.db.xs + (int64_t)stok[0] * nkb + kb);
+            if (stok[1] >= 0) a1 = __ldg(p.db.xs + (int64_t)stok[1] * nkb + kb);
+          }
+          acc[0] = fmaf(sg * a0, b0[0] + b1[0], acc[0]);
+          acc[1] = fmaf(sg * a1, b0[1] + b1[1], acc[1]);
+          acc[2] = fmaf(su * a0, b0[2] + b1[2], acc[2]);
+          acc[3] = fmaf(su * a1, b0[3] + b1[3], acc[3]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -1178,20 +1245,20 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   const int want = (a.S + 31) / 32 * 32;
   if (want < nt) nt = want < 256 ? 256 : want;   // >= 256 threads: the activation CTAs rely on it
   const size_t rsm = route_smem_bytes(a.E, nt);
-  if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm)))
-    return err;
-  if ((err = cudaFuncSetAttribute(decode_gemm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c1.smem)))
-    return err;
+  auto prep = a.act8 ? decode_prep_kernel<true> : decode_prep_kernel<false>;
+  if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm))) return err;
+  auto gemm1 = a.act8 ? decode_gemm1_kernel<true> : decode_gemm1_kernel<false>;
+  if ((err = cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c1.smem))) return err;
   if ((err = cudaFuncSetAttribute(decode_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c2.smem)))
     return err;
   // prep: route (CTA 0) + f16 activations (CTAs 1..T)
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
-  if ((err = launch_check(launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(nt), rsm, st, false, p), st,
+  if ((err = launch_check(launch_pdl(prep, dim3(1 + a.T), dim3(nt), rsm, st, false, p), st,
                           "decode_prep")))
     return err;
   stage_mark(st, 1);
-  if ((err = launch_check(launch_pdl(decode_gemm1_kernel, dim3(sms), dim3(kThreads), p.c1.smem, st, pdl, p), st,
+  if ((err = launch_check(launch_pdl(gemm1, dim3(sms), dim3(kThreads), p.c1.smem, st, pdl, p), st,
                           "decode_gemm1")))
     return err;
   stage_mark(st, 2);

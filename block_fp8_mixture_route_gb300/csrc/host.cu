@@ -35,7 +35,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Byte layout of one workspace.
 struct Layout {
   size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, mtp2, rcnt;
-  size_t xh, xexp, h, ybuf;                       // decode
+  size_t xh, xexp, xsd, h, ybuf;                  // decode
   size_t xq, xs, hq, hs, ys, pinv, wsc13, wsc2;  // prefill
   int64_t prows;
   size_t hid, tids, twts, outb;                   // host-io staging
@@ -68,6 +68,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
     L.xexp = take(4 * (size_t)T);
     L.h = take(4 * (size_t)(S * I));
     L.ybuf = take(4 * (size_t)(S * H));
+    L.xsd = take(4 * (size_t)T * (size_t)(H / 128));
   } else if (path == MOE_PATH_PREFILL) {
     const int64_t R = prefill_rows(S, E);
     L.prows = R;
@@ -258,15 +259,18 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
   return MOE_OK;
 }
 
-int check_options(const moe_options* opt, float* ratio, int* force) {
+int check_options(const moe_options* opt, float* ratio, int* force, int* act8) {
   *ratio = 0.f;   // the measured default gate (choose_path)
   *force = MOE_PATH_NONE;
+  *act8 = 0;
   if (!opt) return MOE_OK;
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 5; ++i)
     if (opt->reserved[i] != 0) return MOE_ERR_ARG;
   if (opt->force_path < MOE_PATH_NONE || opt->force_path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (opt->decode_act != MOE_DECODE_ACT_BF16 && opt->decode_act != MOE_DECODE_ACT_E4M3) return MOE_ERR_ARG;
   if (opt->gate_ratio > 0.f) *ratio = opt->gate_ratio;
   *force = opt->force_path;
+  *act8 = opt->decode_act == MOE_DECODE_ACT_E4M3;
   return MOE_OK;
 }
 
@@ -304,6 +308,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     DecodeBufs db;
     db.xh = reinterpret_cast<uint16_t*>(w + L.xh);
     db.xexp = reinterpret_cast<int32_t*>(w + L.xexp);
+    db.xs = reinterpret_cast<float*>(w + L.xsd);
     db.h = reinterpret_cast<float*>(w + L.h);
     db.ybuf = reinterpret_cast<float*>(w + L.ybuf);
     err = launch_decode(a, rb, db, status, dev, st, &launches);
@@ -359,8 +364,8 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
                          w2_scale_stride, out, hostio, &c);
   if (rc) return rc;
   float ratio;
-  int force;
-  if ((rc = check_options(opt, &ratio, &force))) return rc;
+  int force, act8;
+  if ((rc = check_options(opt, &ratio, &force, &act8))) return rc;
   if (c.T == 0) {
     g_last_launches = 0;
     return MOE_OK;
@@ -369,6 +374,7 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   if ((rc = device_ok(&dev))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LayerArgs a = c.a;
+  a.act8 = act8;
   const int path = choose_path(a, ratio, force);
   if (path == MOE_PATH_DECODE && !decode_supported(a.H, a.I)) return MOE_ERR_SHAPE;
   const Layout L = make_layout(c.T, a.k, a.H, a.I, a.E, path, hostio);

@@ -24,6 +24,7 @@ struct LayerArgs {
   int64_t s2_row, s2_exp;
   uint16_t* out;               // bf16 [T, H]
   int T, k, H, I, E, S;        // S = T*k
+  int act8 = 0;                // decode: 1 = e4m3 activations (W8A8), 0 = bf16 (W8A16)
 };
 
 // Routing lists produced by the route kernel (device int32 buffers).
@@ -45,6 +46,7 @@ struct RouteBufs {
 struct DecodeBufs {
   uint16_t* xh;       // f16 [T, H]: activations scaled by 2^-xexp[t]
   int32_t* xexp;      // [T]
+  float* xs;          // [T, H/128]: W8A8 activation group scales (decode_act e4m3)
   float* h;           // [S, I] in routed (perm) order
   float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
 };

@@ -51,7 +51,7 @@ cudaError_t scratch_address(int device, void** out) {
 inline size_t al(size_t x) { return (x + 255) / 256 * 256; }
 
 struct NaLayout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta, xh, xexp, h, ybuf, total;
+  size_t status, counts, offsets, perm, inv, glist, nd, meta, xh, xexp, xs, h, ybuf, total;
 };
 
 NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
@@ -76,6 +76,7 @@ NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
   L.xexp = take(4 * (size_t)T);
   L.h = take(4 * (size_t)(S * I));
   L.ybuf = take(4 * (size_t)(S * H));
+  L.xs = take(4 * (size_t)T * (size_t)(H / 128));
   L.total = o;
   return L;
 }
@@ -124,7 +125,8 @@ extern "C" int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, co
                reinterpret_cast<int32_t*>(w + L.glist),  reinterpret_cast<int32_t*>(w + L.nd),
                reinterpret_cast<int4*>(w + L.meta),       nullptr};
   DecodeBufs db{reinterpret_cast<uint16_t*>(w + L.xh), reinterpret_cast<int32_t*>(w + L.xexp),
-                reinterpret_cast<float*>(w + L.h), reinterpret_cast<float*>(w + L.ybuf)};
+                reinterpret_cast<float*>(w + L.xs), reinterpret_cast<float*>(w + L.h),
+                reinterpret_cast<float*>(w + L.ybuf)};
   int launches = 0;
   const cudaError_t e = launch_decode(a, rb, db, status, dev, st, &launches);
   if (e != cudaSuccess) {

@@ -65,7 +65,7 @@ extern "C" {
  * moe_fp8_block_abi_version() differs, so a stale build fails loudly instead
  * of reading the banks with the wrong layout (FreeToken PR #662, PR body: the
  * weight-format ABI probe max_weight_format_id). */
-#define MOE_FP8_BLOCK_ABI_VERSION 1
+#define MOE_FP8_BLOCK_ABI_VERSION 2
 
 /* Element types of moe_tensor.dtype. */
 typedef enum {
@@ -108,11 +108,25 @@ enum {
   MOE_STATUS_TIMEOUT = 2u    /* a bounded pipeline wait gave up; output invalid */
 };
 
+/* Activation formats of the decode path (moe_options.decode_act). */
+enum {
+  /* W8A16: the bf16 activations enter the up/gate projection as they are
+   * (FreeToken PR #662, the CPU and GPU decode kernels). */
+  MOE_DECODE_ACT_BF16 = 0,
+  /* W8A8: each token is quantised per 128-column group to e4m3 with a
+   * dynamic fp32 scale amax/448 (the prefill rule) and the up/gate
+   * projection multiplies e4m3 by e4m3; h stays fp32 for the down projection
+   * (the Gaudi path of the fp8-moe-gather page, "The fix"). */
+  MOE_DECODE_ACT_E4M3 = 1
+};
+
 /* Options of moe_fp8_block_forward_ex.  Zero-initialise, then set fields. */
 typedef struct {
   float gate_ratio;   /* decode while T*k <= E*gate_ratio; <= 0 -> measured rule */
   int32_t force_path; /* MOE_PATH_NONE (gate decides), _DECODE or _PREFILL     */
-  int32_t reserved[6];/* must be zero                                          */
+  int32_t decode_act; /* MOE_DECODE_ACT_BF16 (default) or _E4M3; the prefill  */
+                      /* path always quantises activations (and h)             */
+  int32_t reserved[5];/* must be zero                                          */
 } moe_options;
 
 /*

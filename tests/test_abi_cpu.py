@@ -129,6 +129,9 @@ def test_bad_options(lib, tiny):
     o = _lib.MoeOptions()
     o.reserved[2] = 1
     assert _call(lib, tiny, opt=o) == -9
+    o = _lib.MoeOptions()
+    o.decode_act = 2              # neither MOE_DECODE_ACT_BF16 nor _E4M3
+    assert _call(lib, tiny, opt=o) == -9
 
 
 def test_empty_batch_is_noop(lib):

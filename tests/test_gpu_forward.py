@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from block_fp8_mixture_route_gb300 import api, synthetic as syn
+from block_fp8_mixture_route_gb300 import api, diagnostics, synthetic as syn
 from oracle import moe_oracle as mo
 
 from helpers import TOL, check_per_token, oracle_args
@@ -33,12 +33,15 @@ def problem(shape, T, routing="softmax", seed=0, step=0):
     return dict(hidden=hidden, topk_ids=ids, topk_weights=w, w13=w13, w13_scale=w13s, w2=w2, w2_scale=w2s)
 
 
-def run_and_check(prob, path, tokens=None, mode="gathered"):
-    out = api.forward_problem(prob, force_path=path)
+def run_and_check(prob, path, tokens=None, mode="gathered", decode_act=None):
+    out = api.forward_problem(prob, force_path=path, decode_act=decode_act)
     torch.cuda.synchronize()
     assert api.moe_fp8_block_last_path() == (1 if path == "decode" else 2)
     args, tok = oracle_args(prob, tokens)
-    act = "bf16" if path == "decode" else "e4m3"
+    if path == "decode":
+        act = "e4m3_x" if decode_act == "e4m3" else "bf16"
+    else:
+        act = "e4m3"
     ref = mo.forward(*args, mode=mode, act=act)
     got = out.float().cpu().numpy()[tok]
     return check_per_token(got, ref), out
@@ -253,3 +256,55 @@ def test_prefill_status_and_skipped_slots(cuda_lib):
     api.moe_fp8_block_device_status()
     r, _ = run_and_check(prob, "prefill")
     assert api.moe_fp8_block_device_status() == 1
+
+
+# -------------------------------------------------------- decode (W8A8)
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_decode_w8a8_small_experts(cuda_lib, T):
+    r, _ = run_and_check(problem(syn.DECODE_SMALL, T), "decode", decode_act="e4m3")
+    assert r <= TOL
+
+
+def test_decode_w8a8_padded_skewed(cuda_lib):
+    r, _ = run_and_check(problem(syn.PADDED_SKEWED, 8, routing="hot"), "decode", decode_act="e4m3")
+    assert r <= TOL
+
+
+@pytest.mark.slow
+def test_decode_w8a8_wide_experts(cuda_lib):
+    # H = 7168: 14 K blocks per warp, the kernel's non-register path
+    r, _ = run_and_check(problem(syn.DECODE_WIDE, 2), "decode", tokens=[0, 1], decode_act="e4m3")
+    assert r <= TOL
+
+
+def test_decode_w8a8_exact_grid_equals_w8a16(cuda_lib):
+    """Activations on the e4m3 grid with a 448 code in every group quantise
+    exactly, so W8A8 decode must give the W8A16 output up to summation
+    order."""
+    prob = problem(syn.DECODE_SMALL, 4)
+    g = torch.Generator().manual_seed(3)
+    finite = torch.tensor([b for b in range(256) if b not in (0x7F, 0xFF)], dtype=torch.uint8)
+    codes = finite[torch.randint(0, len(finite), (4, syn.DECODE_SMALL.H), generator=g)]
+    codes[:, ::128] = 0x7E
+    prob["hidden"] = (codes.view(torch.float8_e4m3fn).to(torch.float32) * 2.0 ** -4).to(torch.bfloat16).cuda()
+    a = api.forward_problem(prob, force_path="decode").float()
+    b = api.forward_problem(prob, force_path="decode", decode_act="e4m3").float()
+    torch.cuda.synchronize()
+    scale = a.abs().amax(dim=1, keepdim=True)
+    assert torch.all((a - b).abs() <= 1e-5 * scale)
+
+
+def test_decode_ulp_verify(cuda_lib):
+    """The W8A8-versus-W8A16 diagnostic runs, its statistics are consistent,
+    and its per-token distance agrees with the oracle's own W8A8-versus-W8A16
+    distance: each GPU mode is within the parity tolerance of its oracle, so
+    the two distances differ by at most twice that tolerance."""
+    prob = problem(syn.DECODE_SMALL, 8)
+    st = diagnostics.decode_ulp_verify(prob)
+    assert np.isfinite(st["max_ulp"]) and st["max_ulp"] >= st["mean_ulp"] >= 0.0
+    assert 0.0 <= st["frac_over_2"] <= 1.0
+    args, _ = oracle_args(prob)
+    r16 = mo.forward(*args, act="bf16")
+    r8 = mo.forward(*args, act="e4m3_x")
+    oracle_rel = float(np.max(np.max(np.abs(r16 - r8), axis=1) / np.max(np.abs(r16), axis=1)))
+    assert abs(st["max_rel_row"] - oracle_rel) <= 2 * TOL
