@@ -35,7 +35,8 @@ import torch
 _MASK64 = (1 << 64) - 1
 
 # tensor ids for the per-tensor generator seeds
-_TID_W13, _TID_W13S, _TID_W2, _TID_W2S, _TID_X, _TID_LOGITS, _TID_HOT, _TID_ZIPF = range(1, 9)
+(_TID_W13, _TID_W13S, _TID_W2, _TID_W2S, _TID_X, _TID_LOGITS, _TID_HOT, _TID_ZIPF, _TID_B13,
+ _TID_B2) = range(1, 11)
 
 
 def splitmix64(x: int) -> int:
@@ -125,6 +126,18 @@ def make_weights(shape: MoeShape, seed: int = 0, device="cpu", experts_per_draw:
     w13_scale = _scale_bank(E, -(-2 * I // 128), -(-H // 128), s13, e13, seed, _TID_W13S, device)
     w2_scale = _scale_bank(E, -(-H // 128), -(-I // 128), s2, e2, seed, _TID_W2S, device)
     return w13, w13_scale, w2, w2_scale
+
+
+def make_biases(shape: MoeShape, seed: int = 0, device="cpu", std13: float = 1.0, std2: float = 1.0):
+    """MLP biases, fp32 N(0, std^2): w13_bias [E, 2I] (gate biases in
+    [0, I), up biases in [I, 2I)) and w2_bias [E, H]."""
+    E, H, I = shape.E, shape.H, shape.I
+    b13 = torch.empty((E, 2 * I), dtype=torch.float32, device=device)
+    b2 = torch.empty((E, H), dtype=torch.float32, device=device)
+    for e in range(E):
+        b13[e] = torch.randn((2 * I,), generator=_gen(seed, _TID_B13, e, device), device=device) * std13
+        b2[e] = torch.randn((H,), generator=_gen(seed, _TID_B2, e, device), device=device) * std2
+    return b13, b2
 
 
 def make_hidden(T: int, H: int, seed: int = 0, device="cpu", step: int = 0) -> torch.Tensor:

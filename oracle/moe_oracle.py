@@ -37,6 +37,11 @@ What it computes, step by step (float64 unless a step says otherwise):
    fix": dynamic activation scales and an FP8 GEMM for the up/gate
    projection, the down projection in fp32) quantises the activations by
    step 3 and keeps h unquantised.
+   Optional MLP biases (tpu-inference PR #3040, review of the bias DMA: the
+   up/gate bias row is laid out [gate | up] like the weight rows, the up
+   half at offset I, and the down projection has a bias of its own with no
+   split): gate += b13[0:I], up += b13[I:2I] before silu, y += b2 after the
+   down projection.  The biases are fp32 and enter float64 exactly.
 5. Combine: out_t = sum_j w[t,j] * y_{ids[t,j]}(x_t).  The all-expert
    evaluation (the stock mixture_of_experts op of the fp8-moe-gather page,
    "Problem", reads every expert) computes y_e for every expert and masks
@@ -169,20 +174,30 @@ def silu(z: np.ndarray) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
-def expert_forward(a: np.ndarray, w13_codes, w13_scale, w2_codes, w2_scale, act: str) -> np.ndarray:
-    """y = W2 h(a) for one expert and a batch of activation rows a [n, H]
-    (float64, already dequantised in the W8A8 modes).  h is quantised only
-    in act == "e4m3" (prefill W8A8)."""
+def expert_forward(a: np.ndarray, w13_codes, w13_scale, w2_codes, w2_scale, act: str,
+                   b13=None, b2=None) -> np.ndarray:
+    """y = W2 h(a) (+ b2) for one expert and a batch of activation rows
+    a [n, H] (float64, already dequantised in the W8A8 modes).  h is
+    quantised only in act == "e4m3" (prefill W8A8).  b13: optional fp32 [2I]
+    bias row, gate biases in [0, I) and up biases in [I, 2I); b2: optional
+    fp32 [H] down-projection bias."""
     I = w13_codes.shape[0] // 2
     W13 = dequant_bank(w13_codes, w13_scale)       # [2I, H]
     gate = a @ W13[:I].T                            # [n, I]
     up = a @ W13[I:].T
+    if b13 is not None:
+        b13 = np.asarray(b13, dtype=np.float32).astype(np.float64)
+        gate = gate + b13[:I]
+        up = up + b13[I:2 * I]
     h = silu(gate) * up
     if act == "e4m3":
         hc, hs = quantize_per_128(h.astype(np.float32))
         h = dequantize_per_128(hc, hs)
     W2 = dequant_bank(w2_codes, w2_scale)           # [H, I]
-    return h @ W2.T                                 # [n, H]
+    y = h @ W2.T                                    # [n, H]
+    if b2 is not None:
+        y = y + np.asarray(b2, dtype=np.float32).astype(np.float64)
+    return y
 
 
 def activations(hidden_bf16: np.ndarray, act: str) -> np.ndarray:
@@ -198,7 +213,8 @@ def activations(hidden_bf16: np.ndarray, act: str) -> np.ndarray:
 
 # ---------------------------------------------------------------- step 5 --
 def forward(hidden_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
-            mode: str = "gathered", act: str = "bf16", tokens=None) -> np.ndarray:
+            mode: str = "gathered", act: str = "bf16", tokens=None, w13_bias=None,
+            w2_bias=None) -> np.ndarray:
     """Layer output, float64 [len(tokens), H].
 
     hidden_bf16: uint16 [T, H]; topk_ids: int32 [T, k]; topk_weights: float32
@@ -209,6 +225,8 @@ def forward(hidden_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
     h quantised the same way) or "e4m3_x" (W8A8 decode: activations
     quantised, h kept in float64 for the down projection).
     tokens: optional subset of token indices (all by default).
+    w13_bias: optional fp32 [E, 2I] ([gate | up] per expert); w2_bias:
+    optional fp32 [E, H].
     """
     E = w13.shape[0]
     T, H = hidden_bf16.shape
@@ -220,14 +238,18 @@ def forward(hidden_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
     if mode == "all":
         for e in range(E):
             c = np.where(ids == e, wts, 0.0).sum(axis=1)        # c[t, e]
-            y = expert_forward(a, w13[e], w13_scale[e], w2[e], w2_scale[e], act)
+            y = expert_forward(a, w13[e], w13_scale[e], w2[e], w2_scale[e], act,
+                               None if w13_bias is None else w13_bias[e],
+                               None if w2_bias is None else w2_bias[e])
             out += c[:, None] * y
         return out
     if mode == "gathered":
         valid = (ids >= 0) & (ids < E)
         for e in np.unique(ids[valid]):
             rows, js = np.nonzero(ids == e)
-            y = expert_forward(a[rows], w13[e], w13_scale[e], w2[e], w2_scale[e], act)
+            y = expert_forward(a[rows], w13[e], w13_scale[e], w2[e], w2_scale[e], act,
+                               None if w13_bias is None else w13_bias[e],
+                               None if w2_bias is None else w2_bias[e])
             np.add.at(out, rows, wts[rows, js][:, None] * y)
         return out
     raise ValueError(mode)

@@ -264,6 +264,13 @@ def test_gathered_equals_all_expert(act):
     al = mo.forward(*a, mode="all", act=act)
     scale = np.max(np.abs(al), axis=1, keepdims=True)
     assert np.all(np.abs(g - al) <= 1e-12 * scale)
+    # with MLP biases: an unrouted expert's masked y (which includes its b2)
+    # must still add nothing
+    b13, b2 = (b.numpy() for b in syn.make_biases(syn.TINY, seed=1, std13=30.0, std2=1e5))
+    g = mo.forward(*a, mode="gathered", act=act, w13_bias=b13, w2_bias=b2)
+    al = mo.forward(*a, mode="all", act=act, w13_bias=b13, w2_bias=b2)
+    scale = np.max(np.abs(al), axis=1, keepdims=True)
+    assert np.all(np.abs(g - al) <= 1e-12 * scale)
 
 
 def test_padded_equals_unpadded_scales():
@@ -319,7 +326,7 @@ def test_slot_order_invariance_and_negative_slot():
 
 
 # ------------------------------------------------------- brute force -----
-def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act):
+def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act, b13=None, b2=None):
     """Scalar float64 loops; e4m3 decoded through the fp16 bit trick and
     torch's float8 cast for the activation codes (independent of the oracle)."""
     def dec(b):
@@ -354,11 +361,16 @@ def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act):
             for i in range(I):
                 g = sum(dec(w13[e, i, c]) * bf(w13s[e, i // 128, c // 128]) * x[c] for c in range(H))
                 u = sum(dec(w13[e, I + i, c]) * bf(w13s[e, (I + i) // 128, c // 128]) * x[c] for c in range(H))
+                if b13 is not None:
+                    g += float(b13[e, i])
+                    u += float(b13[e, I + i])
                 h.append(g / (1.0 + math.exp(-g)) * u)
             if act == "e4m3":
                 h = sum((quant_row([float(np.float32(z)) for z in h[c:c + 128]]) for c in range(0, I, 128)), [])
             for n in range(H):
                 y = sum(dec(w2[e, n, i]) * bf(w2s[e, n // 128, i // 128]) * h[i] for i in range(I))
+                if b2 is not None:
+                    y += float(b2[e, n])
                 out[t][n] += float(wts[t, j]) * y
     return np.array(out)
 
@@ -373,6 +385,77 @@ def test_brute_force_tiny(act):
     got = mo.forward(*a, act=act)
     scale = np.max(np.abs(ref), axis=1, keepdims=True)
     assert np.all(np.abs(got - ref) <= 1e-12 * scale)
+
+
+@pytest.mark.parametrize("act", ["bf16", "e4m3"])
+def test_brute_force_tiny_bias(act):
+    """As test_brute_force_tiny, with gate/up and down-projection biases of
+    the size of the projections they are added to."""
+    shp = syn.MoeShape(E=3, H=128, I=128, k=2, w2_scale_stride=3)
+    prob = syn.make_problem(shp, T=2, seed=12)
+    a = _np_args(prob)
+    b13, b2 = (b.numpy() for b in syn.make_biases(shp, seed=12, std13=30.0, std2=1e5))
+    ref = _brute(*a, act=act, b13=b13, b2=b2)
+    got = mo.forward(*a, act=act, w13_bias=b13, w2_bias=b2)
+    scale = np.max(np.abs(ref), axis=1, keepdims=True)
+    assert np.all(np.abs(got - ref) <= 1e-12 * scale)
+    # the biases matter at this size
+    assert np.max(np.abs(mo.forward(*a, act=act) - ref) / scale) > 1e-2
+
+
+def test_bias_zero_weights_gives_weighted_down_bias():
+    """With every weight code 0x00 (+0) both projections vanish, so y = b2
+    exactly whatever the gate/up biases, and out_t = sum_j w[t,j] b2[ids[t,j]]
+    (tpu-inference PR #3040, review of the bias DMA: the down projection's
+    bias is added as it is, with no gate/up split)."""
+    prob = syn.make_problem(syn.TINY, T=4, seed=2)
+    a = _np_args(prob)
+    a[1][3, 0] = -1                                   # a skipped slot adds nothing
+    a[3] = np.zeros_like(a[3])
+    a[5] = np.zeros_like(a[5])
+    b13, b2 = (b.numpy() for b in syn.make_biases(syn.TINY, seed=2))
+    got = mo.forward(*a, w13_bias=b13, w2_bias=b2)
+    exp = np.zeros_like(got)
+    for t in range(a[1].shape[0]):
+        for j in range(a[1].shape[1]):
+            e = int(a[1][t, j])
+            if e >= 0:
+                exp[t] += float(a[2][t, j]) * b2[e].astype(np.float64)
+    assert np.all(np.abs(got - exp) <= 1e-14 * np.max(np.abs(exp)))
+
+
+def test_bias_gate_up_split_closed_form():
+    """One expert, H = 128, I = 256 (two 128-row gate blocks), w13 codes all
+    0x00, gate biases ln 3, up bias of row i equal to i / 256, w2 codes all
+    0x38 (1.0), unit scales.  Then gate = ln 3 and silu(ln 3) = (3/4) ln 3, so
+    h_i = (3/4) ln 3 * i / 256 and y_n = (3/4) ln 3 * 127.5 + b2_n.  An up
+    bias read from the gate half instead (the defect reviewed in
+    tpu-inference PR #3040) would give (3/4) (ln 3)^2 * 256 + b2_n."""
+    H, I = 128, 256
+    one = np.uint16(0x3F80)                           # bf16 1.0
+    w13 = np.zeros((1, 2 * I, H), dtype=np.uint8)
+    w13s = np.full((1, 2 * I // 128, 1), one, dtype=np.uint16)
+    w2 = np.full((1, H, I), 0x38, dtype=np.uint8)
+    w2s = np.full((1, 1, 2), one, dtype=np.uint16)
+    hidden = np.full((1, H), 0x3F80, dtype=np.uint16)
+    ids = np.zeros((1, 1), dtype=np.int32)
+    wts = np.ones((1, 1), dtype=np.float32)
+    ln3 = np.float32(math.log(3.0))
+    b13 = np.concatenate([np.full(I, ln3, dtype=np.float32), np.arange(I, dtype=np.float32) / np.float32(I)])[None]
+    b2 = (np.arange(H, dtype=np.float32) - 64.0)[None] * np.float32(0.25)
+    got = mo.forward(hidden, ids, wts, w13, w13s, w2, w2s, w13_bias=b13, w2_bias=b2)[0]
+    exp = 0.75 * math.log(3.0) * 127.5 + b2[0].astype(np.float64)
+    # fp32 rounding of ln 3 moves silu by about 1e-8 relative
+    assert np.all(np.abs(got - exp) <= 1e-6 * np.max(np.abs(exp)))
+
+
+def test_zero_biases_change_nothing():
+    prob = syn.make_problem(syn.TINY, T=4, seed=0)
+    a = _np_args(prob)
+    z13 = np.zeros((syn.TINY.E, 2 * syn.TINY.I), dtype=np.float32)
+    z2 = np.zeros((syn.TINY.E, syn.TINY.H), dtype=np.float32)
+    for act in ("bf16", "e4m3"):
+        assert np.array_equal(mo.forward(*a, act=act, w13_bias=z13, w2_bias=z2), mo.forward(*a, act=act))
 
 
 def test_w8a8_decode_equals_w8a16_on_the_e4m3_grid():
