@@ -12,7 +12,7 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe_fp8_block.so")
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 MOE_BF16, MOE_F32, MOE_E4M3, MOE_I32 = 1, 2, 3, 4
 MOE_PATH_NONE, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
@@ -26,7 +26,8 @@ ERRORS = {
 
 # every symbol the header declares
 EXPORTS = [
-    "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_hostio",
+    "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_bias",
+    "moe_fp8_block_forward_hostio",
     "moe_fp8_block_forward_decode_noalloc",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
@@ -81,6 +82,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_forward.argtypes = fwd
         lib.moe_fp8_block_forward_ex.argtypes = fwd + [P(MoeOptions)]
         lib.moe_fp8_block_forward_hostio.argtypes = fwd + [P(MoeOptions)]
+        lib.moe_fp8_block_forward_bias.argtypes = fwd[:9] + [T, T] + fwd[9:] + [P(MoeOptions)]
         lib.moe_fp8_block_forward_decode_noalloc.argtypes = fwd
         lib.moe_fp8_block_route.argtypes = [T, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.moe_fp8_block_act_quant.argtypes = [T, vp, vp, vp]

@@ -60,9 +60,15 @@ def _options(gate_ratio, force_path, decode_act=None) -> Optional[MoeOptions]:
 
 def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                           w2_scale_stride, out=None, stream=None, gate_ratio=None, force_path=None,
-                          decode_act=None):
+                          decode_act=None, w13_bias=None, w2_bias=None):
     """Layer forward on device tensors; returns `out` (bf16 [T, H]).
-    decode_act: "bf16" (W8A16, default) or "e4m3" (W8A8) for the decode path."""
+    decode_act: "bf16" (W8A16, default) or "e4m3" (W8A8) for the decode path.
+    w13_bias (fp32 [E, 2I], [gate | up]) and w2_bias (fp32 [E, H]): optional
+    MLP biases, passed to moe_fp8_block_forward_bias."""
+    if w13_bias is not None or w2_bias is not None:
+        return moe_fp8_block_forward_bias(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
+                                          w2_scale, w2_scale_stride, w13_bias, w2_bias, out=out, stream=stream,
+                                          gate_ratio=gate_ratio, force_path=force_path, decode_act=decode_act)
     lib = _lib.load()
     if out is None:
         out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
@@ -78,6 +84,28 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
         rc = lib.moe_fp8_block_forward_ex(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                           int(w2_scale_stride), P(o), _stream(stream), P(opt))
     check(rc, "moe_fp8_block_forward")
+    return out
+
+
+def moe_fp8_block_forward_bias(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                               w2_scale_stride, w13_bias=None, w2_bias=None, out=None, stream=None,
+                               gate_ratio=None, force_path=None, decode_act=None):
+    """Layer forward with optional MLP biases (either may be None)."""
+    lib = _lib.load()
+    if out is None:
+        out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    b13 = desc(w13_bias) if w13_bias is not None else None
+    b2 = desc(w2_bias) if w2_bias is not None else None
+    o = desc(out)
+    P = ctypes.byref
+    opt = _options(gate_ratio, force_path, decode_act)
+    rc = lib.moe_fp8_block_forward_bias(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                        int(w2_scale_stride), P(b13) if b13 is not None else None,
+                                        P(b2) if b2 is not None else None, P(o), _stream(stream),
+                                        P(opt) if opt is not None else None)
+    check(rc, "moe_fp8_block_forward_bias")
     return out
 
 

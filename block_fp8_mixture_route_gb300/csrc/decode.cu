@@ -484,7 +484,7 @@ __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8
 // group's leader sums the partials and applies silu(gate)*up.
 // ACT8: W8A8 (the activation rows are e4m3 code values with per-group
 // scales); W8A16 otherwise.
-template <bool ACT8>
+template <bool ACT8, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamCfg& cfg = p.c1;
@@ -649,6 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
       for (long u = wk.seg_b; u < wk.seg_e; ++u, ++m) {
         if ((m & 1) != gr) continue;   // the other group's unit
         const int i0 = (int)(u % upe) * R;
+        // optional MLP biases of this lane's gate and up row, read now so the
+        // loads complete while the unit computes
+        float bgv = 0.f, buv = 0.f;
+        if (BIAS && wq == 0 && has_w) {
+          const float* br = a.b13 + (int64_t)wk.e * a.b13_ld + i0 + g;
+          bgv = __ldg(br);
+          buv = __ldg(br + a.I);
+        }
         float sgl, sul;
         if (u == next_u) {
           sgl = next_g;
@@ -713,8 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (2 * c + j < nx) {
-              const float gv = ldexpf(tot[j], sx[j]);
-              const float uv = ldexpf(tot[2 + j], sx[j]);
+              float gv = ldexpf(tot[j], sx[j]);
+              float uv = ldexpf(tot[2 + j], sx[j]);
+              if (BIAS) {
+                gv += bgv;
+                uv += buv;
+              }
               p.db.h[(int64_t)(pos0 + j) * a.I + i0 + g] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
           }
@@ -1101,6 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
 }
 
 // ---------------------------------------------------------- combine ----
+template <bool BIAS>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs p) {
   pdl_wait();
   pdl_trigger();
@@ -1115,15 +1128,35 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs p) {
   for (int j0 = 0; j0 < a.k; j0 += 8) {
     const int64_t s0 = (int64_t)t * a.k + j0;
     bool use[8];
+    int id[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const int id = j0 + q < a.k ? a.ids[s0 + q] : -1;
-      use[q] = id >= 0 && id < a.E;
+      id[q] = j0 + q < a.k ? a.ids[s0 + q] : -1;
+      use[q] = id[q] >= 0 && id[q] < a.E;
     }
     float4 v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       v[q] = use[q] ? *reinterpret_cast<const float4*>(p.db.ybuf + (s0 + q) * a.H + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (BIAS) {
+      // optional down-projection bias: slot j adds w[t,j] * b2[e_j] after its
+      // weighted y (the per-slot rows already hold w[t,j] * y)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (!use[q]) continue;
+        const float w = a.wts[s0 + q];
+        const float4 bv = *reinterpret_cast<const float4*>(a.b2 + (int64_t)id[q] * a.b2_ld + n);
+        acc.x += v[q].x;
+        acc.y += v[q].y;
+        acc.z += v[q].z;
+        acc.w += v[q].w;
+        acc.x = fmaf(w, bv.x, acc.x);
+        acc.y = fmaf(w, bv.y, acc.y);
+        acc.z = fmaf(w, bv.z, acc.z);
+        acc.w = fmaf(w, bv.w, acc.w);
+      }
+      continue;
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if (!use[q]) continue;
@@ -1247,7 +1280,11 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   const size_t rsm = route_smem_bytes(a.E, nt);
   auto prep = a.act8 ? decode_prep_kernel<true> : decode_prep_kernel<false>;
   if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm))) return err;
-  auto gemm1 = a.act8 ? decode_gemm1_kernel<true> : decode_gemm1_kernel<false>;
+  // the gate/up projection for the activation format, with the optional
+  // MLP bias compiled in or out
+  auto gemm1 = a.act8 ? (a.b13 ? decode_gemm1_kernel<true, true> : decode_gemm1_kernel<true, false>)
+                      : (a.b13 ? decode_gemm1_kernel<false, true> : decode_gemm1_kernel<false, false>);
+  auto combine = a.b2 ? decode_combine_kernel<true> : decode_combine_kernel<false>;
   if ((err = cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c1.smem))) return err;
   if ((err = cudaFuncSetAttribute(decode_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c2.smem)))
     return err;
@@ -1266,7 +1303,7 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
                           "decode_gemm2")))
     return err;
   stage_mark(st, 3);
-  if ((err = launch_check(launch_pdl(decode_combine_kernel, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, pdl, p),
+  if ((err = launch_check(launch_pdl(combine, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, pdl, p),
                           st, "decode_combine")))
     return err;
   stage_mark(st, 4);

@@ -192,6 +192,18 @@ struct Checked {
   int64_t T;
 };
 
+// An optional MLP bias: fp32 [E, n], stride[1] == 1, expert stride
+// stride[0] >= n and a multiple of 4 elements, 16-byte aligned base.
+int check_bias(const moe_tensor* b, int64_t E, int64_t n) {
+  int rc = check_tensor(b, 2, MOE_F32);
+  if (rc) return rc;
+  if (b->shape[0] != E || b->shape[1] != n) return MOE_ERR_SHAPE;
+  if (b->stride[1] != 1 || (E > 1 && (b->stride[0] < n || b->stride[0] % 4 != 0))) return MOE_ERR_STRIDE;
+  if (!b->data) return MOE_ERR_NULL;
+  if (!aligned16(b->data)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
 int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
                   const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
                   const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride,
@@ -358,11 +370,24 @@ int choose_path(const LayerArgs& a, float ratio, int force) {
 int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
                  const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
                  const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
-                 void* stream, const moe_options* opt, bool hostio) {
+                 void* stream, const moe_options* opt, bool hostio, const moe_tensor* w13_bias = nullptr,
+                 const moe_tensor* w2_bias = nullptr) {
   Checked c{};
   int rc = check_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                          w2_scale_stride, out, hostio, &c);
   if (rc) return rc;
+  if (w13_bias) {
+    if ((rc = check_bias(w13_bias, c.a.E, 2 * (int64_t)c.a.I))) return rc;
+    if (overlap(out, w13_bias)) return MOE_ERR_ALIAS;
+    c.a.b13 = static_cast<const float*>(w13_bias->data);
+    c.a.b13_ld = c.a.E > 1 ? w13_bias->stride[0] : 2 * (int64_t)c.a.I;
+  }
+  if (w2_bias) {
+    if ((rc = check_bias(w2_bias, c.a.E, c.a.H))) return rc;
+    if (overlap(out, w2_bias)) return MOE_ERR_ALIAS;
+    c.a.b2 = static_cast<const float*>(w2_bias->data);
+    c.a.b2_ld = c.a.E > 1 ? w2_bias->stride[0] : c.a.H;
+  }
   float ratio;
   int force, act8;
   if ((rc = check_options(opt, &ratio, &force, &act8))) return rc;
@@ -491,6 +516,15 @@ int moe_fp8_block_forward_ex(const moe_tensor* hidden, const moe_tensor* topk_id
                              void* stream, const moe_options* opt) {
   return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                       w2_scale_stride, out, stream, opt, false);
+}
+
+int moe_fp8_block_forward_bias(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                               const moe_tensor* topk_weights, const moe_tensor* w13,
+                               const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,
+                               const moe_tensor* w2_scale, int64_t w2_scale_stride, const moe_tensor* w13_bias,
+                               const moe_tensor* w2_bias, moe_tensor* out, void* stream, const moe_options* opt) {
+  return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                      w2_scale_stride, out, stream, opt, false, w13_bias, w2_bias);
 }
 
 int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* topk_ids,

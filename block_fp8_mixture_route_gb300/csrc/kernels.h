@@ -25,6 +25,10 @@ struct LayerArgs {
   uint16_t* out;               // bf16 [T, H]
   int T, k, H, I, E, S;        // S = T*k
   int act8 = 0;                // decode: 1 = e4m3 activations (W8A8), 0 = bf16 (W8A16)
+  const float* b13 = nullptr;  // optional fp32 [E, 2I] MLP bias row [gate | up], expert stride b13_ld
+  int64_t b13_ld = 0;
+  const float* b2 = nullptr;   // optional fp32 [E, H] down-projection bias, expert stride b2_ld
+  int64_t b2_ld = 0;
 };
 
 // Routing lists produced by the route kernel (device int32 buffers).

@@ -381,7 +381,7 @@ struct RingPos {
 // the peer's, written by the peer's multicast.  So a stage is free again
 // only when both CTAs' MMAs have read it: each MMA commit arrives on the
 // empty barrier of both CTAs, which therefore count two arrivals.
-template <int MODE>
+template <int MODE, bool BIAS = false>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ PfMaps m, PrefillArgs p, int ns) {
   using namespace pf;
@@ -564,6 +564,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int nb = tl.nb;
       const int p0 = tl.mi * BM;
       const bool has1 = MODE == 1 || nb * BN + 128 < a.H;
+      // optional MLP biases (GEMM1): lane l holds the gate and up biases of
+      // this warp's column pair l, read at the tile start so that the loads
+      // complete during the K loop
+      float2 bg2 = make_float2(0.f, 0.f), bu2 = bg2;
+      if (BIAS) {
+        const float* br = a.b13 + (int64_t)tl.e * a.b13_ld + nb * 128 + hf * 64 + 2 * lane;
+        bg2 = __ldg(reinterpret_cast<const float2*>(br));
+        bu2 = __ldg(reinterpret_cast<const float2*>(br + a.I));
+      }
       // this thread's 64 columns of each 128-column block, as 32 pairs
       uint64_t acc0[32], acc1[32];
 #pragma unroll
@@ -616,9 +625,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float g0 = f2lo(acc0[i]), g1 = f2hi(acc0[i]);
-          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * f2lo(acc1[i]);
-          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * f2hi(acc1[i]);
+          float g0 = f2lo(acc0[i]), g1 = f2hi(acc0[i]);
+          float u0 = f2lo(acc1[i]), u1 = f2hi(acc1[i]);
+          if (BIAS) {
+            g0 += __shfl_sync(0xffffffffu, bg2.x, i);
+            g1 += __shfl_sync(0xffffffffu, bg2.y, i);
+            u0 += __shfl_sync(0xffffffffu, bu2.x, i);
+            u1 += __shfl_sync(0xffffffffu, bu2.y, i);
+          }
+          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
           acc0[i] = f2pack(h0, h1);
           amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
         }
@@ -686,6 +702,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 }
 
 // ------------------------------------------------------------ combine ----
+template <bool BIAS>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillArgs p) {
   pdl_wait();
   pdl_trigger();
@@ -709,6 +726,23 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillArgs p) {
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       v[q] = row[q] >= 0 ? *reinterpret_cast<const uint4*>(p.pb.ys + (int64_t)row[q] * a.H + n) : make_uint4(0, 0, 0, 0);
+    if (BIAS) {
+      // optional down-projection bias: out += w[t,j] * (y + b2[e_j])
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (row[q] < 0) continue;
+        const float* br = a.b2 + (int64_t)a.ids[s0 + q] * a.b2_ld + n;
+        const float4 b0 = *reinterpret_cast<const float4*>(br), b1 = *reinterpret_cast<const float4*>(br + 4);
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(w[q], bf16_to_f32(u[i] & 0xFFFFu) + bb[2 * i], acc[2 * i]);
+          acc[2 * i + 1] = fmaf(w[q], bf16_to_f32(u[i] >> 16) + bb[2 * i + 1], acc[2 * i + 1]);
+        }
+      }
+      continue;
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if (row[q] < 0) continue;
@@ -893,9 +927,11 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
   const int sm1 = (int)pf_layout(1, ns1, a.E).total, sm2 = (int)pf_layout(2, ns2, a.E).total;
+  // the gate/up projection with the optional MLP bias compiled in or out
+  auto gemm1 = a.b13 ? prefill_gemm_kernel<1, true> : prefill_gemm_kernel<1, false>;
   cudaError_t err;
   if ((err = note_error(
-           cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1),
+           cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1),
            "prefill_gemm1 smem attribute")))
     return err;
   if ((err = note_error(
@@ -903,7 +939,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
            "prefill_gemm2 smem attribute")))
     return err;
   const int sms = num_sms(device);
-  int cl1 = resident_pairs(prefill_gemm_kernel<1>, device, 1, (size_t)sm1);
+  int cl1 = resident_pairs(gemm1, device, 1, (size_t)sm1);
   int cl2 = resident_pairs(prefill_gemm_kernel<2>, device, 2, (size_t)sm2);
   cl1 = cl1 < sms / 2 ? cl1 : sms / 2;
   cl2 = cl2 < sms / 2 ? cl2 : sms / 2;
@@ -923,7 +959,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                           st, "act_quant_permute")))
     return err;
   stage_mark(st, 2);
-  if ((err = launch_check(launch_pairs(prefill_gemm_kernel<1>, cl1, (size_t)sm1, st, pdl, g1, p, ns1), st,
+  if ((err = launch_check(launch_pairs(gemm1, cl1, (size_t)sm1, st, pdl, g1, p, ns1), st,
                           "prefill_gemm1")))
     return err;
   stage_mark(st, 3);
@@ -931,9 +967,9 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                           "prefill_gemm2")))
     return err;
   stage_mark(st, 4);
-  if ((err = launch_check(launch_ex(prefill_combine_kernel, dim3(a.T, (a.H + 2047) / 2048), dim3(256), 0, st,
-                                    pdl, p),
-                          st, "prefill_combine")))
+  auto combine = a.b2 ? prefill_combine_kernel<true> : prefill_combine_kernel<false>;
+  if ((err = launch_check(launch_ex(combine, dim3(a.T, (a.H + 2047) / 2048), dim3(256), 0, st, pdl, p), st,
+                          "prefill_combine")))
     return err;
   stage_mark(st, 5);
   *launches += 4 + nl;

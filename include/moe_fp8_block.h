@@ -65,7 +65,7 @@ extern "C" {
  * moe_fp8_block_abi_version() differs, so a stale build fails loudly instead
  * of reading the banks with the wrong layout (FreeToken PR #662, PR body: the
  * weight-format ABI probe max_weight_format_id). */
-#define MOE_FP8_BLOCK_ABI_VERSION 2
+#define MOE_FP8_BLOCK_ABI_VERSION 3
 
 /* Element types of moe_tensor.dtype. */
 typedef enum {
@@ -166,6 +166,31 @@ int moe_fp8_block_forward_ex(const moe_tensor* hidden, const moe_tensor* topk_id
                              const moe_tensor* w2, const moe_tensor* w2_scale,
                              int64_t w2_scale_stride, moe_tensor* out, void* stream,
                              const moe_options* opt);
+
+/*
+ * moe_fp8_block_forward_bias -- moe_fp8_block_forward_ex with MLP biases
+ * (tpu-inference PR #3040, review of the bias DMA: the up/gate bias row is
+ * laid out like the stacked weight rows, gate biases first and the up
+ * biases at offset I; the down projection's bias has no such split):
+ *     gate = Wg . x + w13_bias[e, 0:I]
+ *     up   = Wu . x + w13_bias[e, I:2I]
+ *     y    = W2 . silu(gate) * up + w2_bias[e]
+ *     out_t = sum_j topk_weights[t,j] * y_{t,j}
+ *  w13_bias  fp32 [E, 2I] or NULL (no gate/up bias).
+ *  w2_bias   fp32 [E, H] or NULL (no down-projection bias).
+ * Each bias: stride[1] == 1; expert stride stride[0] >= its row length and a
+ * multiple of 4 elements (when E > 1); 16-byte aligned base; it must not
+ * overlap `out` (MOE_ERR_ALIAS).  Other arguments, the options and the
+ * return codes are those of moe_fp8_block_forward_ex.  With both biases
+ * NULL the call is moe_fp8_block_forward_ex.
+ */
+int moe_fp8_block_forward_bias(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                               const moe_tensor* topk_weights, const moe_tensor* w13,
+                               const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                               const moe_tensor* w2, const moe_tensor* w2_scale,
+                               int64_t w2_scale_stride, const moe_tensor* w13_bias,
+                               const moe_tensor* w2_bias, moe_tensor* out, void* stream,
+                               const moe_options* opt);
 
 /* As moe_fp8_block_forward_ex, but hidden, topk_ids, topk_weights and out
  * are HOST buffers (page-locked memory gives asynchronous copies; pageable

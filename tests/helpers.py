@@ -48,6 +48,27 @@ def oracle_args(prob: dict, tokens=None):
     return args, tok
 
 
+def oracle_biases(prob: dict, tokens=None) -> dict:
+    """The optional MLP biases of a problem (keys w13_bias, w2_bias) as host
+    arrays, with the experts relabelled exactly as oracle_args does; an empty
+    dict when the problem has none."""
+    ids = prob["topk_ids"].cpu().numpy()
+    tok = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    E = prob["w13"].shape[0]
+    sub_ids = ids[tok]
+    if tokens is None and E <= 16:
+        experts = np.arange(E)
+    else:
+        experts = np.unique(sub_ids[(sub_ids >= 0) & (sub_ids < E)])
+    if len(experts) == 0:
+        experts = np.zeros(1, dtype=np.int64)
+    out = {}
+    for name in ("w13_bias", "w2_bias"):
+        if prob.get(name) is not None:
+            out[name] = prob[name].cpu().numpy()[experts]
+    return out
+
+
 def check_per_token(got: np.ndarray, ref: np.ndarray, tol: float = TOL) -> float:
     """Assert the per-token tolerance; return the worst ratio err/(tol*max)."""
     err = np.max(np.abs(got - ref), axis=1)

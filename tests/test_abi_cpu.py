@@ -167,3 +167,35 @@ def test_act_quant_argument_errors(lib):
 def test_reserve_argument_errors(lib):
     assert lib.moe_fp8_block_reserve(16, 0, 2048, 512, 128, None) == -9
     assert lib.moe_fp8_block_reserve(16, 8, 2000, 512, 128, None) == -9
+
+
+def _call_bias(lib, prob, b13, b2, out=None):
+    d = _descs(prob)
+    o = api.desc(out if out is not None else torch.empty(prob["hidden"].shape, dtype=torch.bfloat16))
+    P = ctypes.byref
+    db13 = api.desc(b13) if b13 is not None else None
+    db2 = api.desc(b2) if b2 is not None else None
+    return lib.moe_fp8_block_forward_bias(P(d[0]), P(d[1]), P(d[2]), P(d[3]), P(d[4]), prob["w13_scale"].stride(1),
+                                          P(d[5]), P(d[6]), prob["w2_scale"].stride(1),
+                                          P(db13) if db13 is not None else None,
+                                          P(db2) if db2 is not None else None, P(o), None, None)
+
+
+def test_bias_argument_errors(lib, tiny):
+    E, H, I = syn.TINY.E, syn.TINY.H, syn.TINY.I
+    b13, b2 = syn.make_biases(syn.TINY)
+    if not torch.cuda.is_available():
+        # valid arguments get as far as the device check (host tensors: never
+        # make this call where a GPU could run it)
+        assert _call_bias(lib, tiny, b13, b2) in (-8, -10)
+        assert _call_bias(lib, tiny, None, None) in (-8, -10)
+    assert _call_bias(lib, tiny, b13.to(torch.bfloat16), b2) == -2         # fp32 only
+    assert _call_bias(lib, tiny, b13[:, :I], b2) == -3                     # [E, 2I]
+    assert _call_bias(lib, tiny, b13, b2[:E - 1]) == -3                    # [E, H]
+    assert _call_bias(lib, tiny, b13.t().contiguous().t(), b2) == -5       # stride[1] != 1
+    wide = torch.zeros(E, 2 * I + 2)
+    assert _call_bias(lib, tiny, wide[:, :2 * I], b2) == -5                # expert stride not a multiple of 4
+    big = torch.zeros(E * H + 1)
+    assert _call_bias(lib, tiny, b13, big[1:].view(E, H)) == -4            # 16-byte alignment
+    alias = torch.zeros(E * H, dtype=torch.float32)
+    assert _call_bias(lib, tiny, b13, alias.view(E, H), out=alias.view(torch.bfloat16)[:4 * H].view(4, H)) == -6
