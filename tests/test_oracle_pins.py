@@ -364,7 +364,8 @@ def _brute(hidden_u16, ids, wts, w13, w13s, w2, w2s, act, b13=None, b2=None):
                 if b13 is not None:
                     g += float(b13[e, i])
                     u += float(b13[e, I + i])
-                h.append(g / (1.0 + math.exp(-g)) * u)
+                # e^-g past the double range is +inf, and g / inf the limit 0
+                h.append(g / (1.0 + (math.exp(-g) if g > -709.0 else math.inf)) * u)
             if act == "e4m3":
                 h = sum((quant_row([float(np.float32(z)) for z in h[c:c + 128]]) for c in range(0, I, 128)), [])
             for n in range(H):
@@ -401,6 +402,63 @@ def test_brute_force_tiny_bias(act):
     assert np.all(np.abs(got - ref) <= 1e-12 * scale)
     # the biases matter at this size
     assert np.max(np.abs(mo.forward(*a, act=act) - ref) / scale) > 1e-2
+
+
+@pytest.mark.parametrize("act", ["bf16", "e4m3"])
+def test_brute_force_ragged(act):
+    """Ragged K and N: H = 192 and I = 144 are not multiples of 128, so the
+    last K block of both projections is partial, and the stacked [gate; up]
+    bank's 128-row scale blocks straddle the gate/up boundary (up row i uses
+    scale row (I + i) // 128); the brute force indexes the banks on its own."""
+    shp = syn.MoeShape(E=2, H=192, I=144, k=2)
+    prob = syn.make_problem(shp, T=2, seed=13)
+    a = _np_args(prob)
+    assert a[4].shape[1:] == (3, 2) and a[6].shape[1:] == (2, 2)
+    b13, b2 = (b.numpy() for b in syn.make_biases(shp, seed=13, std13=30.0, std2=1e5))
+    for bias in (False, True):
+        kw = dict(b13=b13, b2=b2) if bias else {}
+        ref = _brute(*a, act=act, **kw)
+        got = mo.forward(*a, act=act, **({"w13_bias": b13, "w2_bias": b2} if bias else {}))
+        scale = np.max(np.abs(ref), axis=1, keepdims=True)
+        assert np.all(np.abs(got - ref) <= 1e-12 * scale)
+
+
+def _pad_problem(a, H2, I2):
+    """The problem's banks and activations zero-padded to H2 >= H columns and
+    I2 >= I intermediate rows (gate and up padded separately); scale banks
+    keep their values, extended by repeating each expert's last scale."""
+    x, ids, wts, w13, w13s, w2, w2s = a
+    E, I2x, H = w13.shape
+    I = I2x // 2
+    xp = np.zeros((x.shape[0], H2), dtype=np.uint16)
+    xp[:, :H] = x
+    w13p = np.zeros((E, 2 * I2, H2), dtype=np.uint8)
+    w13p[:, :I, :H] = w13[:, :I]
+    w13p[:, I2:I2 + I, :H] = w13[:, I:]
+    w2p = np.zeros((E, H2, I2), dtype=np.uint8)
+    w2p[:, :H, :I] = w2
+    s13 = np.repeat(w13s[:, :1, :1], -(-2 * I2 // 128), axis=1).repeat(-(-H2 // 128), axis=2)
+    s2 = np.repeat(w2s[:, :1, :1], -(-H2 // 128), axis=1).repeat(-(-I2 // 128), axis=2)
+    return [xp, ids, wts, w13p, s13, w2p, s2]
+
+
+def test_ragged_equals_zero_padding():
+    """With one scale per expert (so the 128-row blocking cannot matter), a
+    ragged layer (H = 320, I = 176) equals the same layer zero-padded to
+    H = 384, I = 256: the padded activation columns and weight rows add
+    nothing, in both activation modes; the padded outputs are exactly 0."""
+    shp = syn.MoeShape(E=3, H=320, I=176, k=2)
+    prob = syn.make_problem(shp, T=3, seed=14)
+    a = _np_args(prob)
+    a[4] = np.repeat(a[4][:, :1, :1], a[4].shape[1], axis=1).repeat(a[4].shape[2], axis=2)
+    a[6] = np.repeat(a[6][:, :1, :1], a[6].shape[1], axis=1).repeat(a[6].shape[2], axis=2)
+    p = _pad_problem(a, 384, 256)
+    for act in ("bf16", "e4m3"):
+        r = mo.forward(*a, act=act)
+        q = mo.forward(*p, act=act)
+        assert np.all(q[:, 320:] == 0)
+        scale = np.max(np.abs(r), axis=1, keepdims=True)
+        assert np.all(np.abs(q[:, :320] - r) <= 1e-12 * scale)
 
 
 def test_bias_zero_weights_gives_weighted_down_bias():
