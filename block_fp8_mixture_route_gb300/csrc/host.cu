@@ -68,18 +68,18 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
     L.xexp = take(4 * (size_t)T);
     L.h = take(4 * (size_t)(S * I));
     L.ybuf = take(4 * (size_t)(S * H));
-    L.xsd = take(4 * (size_t)T * (size_t)(H / 128));
+    L.xsd = take(4 * (size_t)T * (size_t)((H + 127) / 128));
   } else if (path == MOE_PATH_PREFILL) {
     const int64_t R = prefill_rows(S, E);
     L.prows = R;
     L.xq = take((size_t)(R * H));
-    L.xs = take(4 * (size_t)(R * (H / 128)));
+    L.xs = take(4 * (size_t)(R * ((H + 127) / 128)));
     L.hq = take((size_t)(R * I));
-    L.hs = take(4 * (size_t)(R * (I / 128)));
+    L.hs = take(4 * (size_t)(R * ((I + 127) / 128)));
     L.ys = take(2 * (size_t)(R * H));
     L.pinv = take(4 * (size_t)S);
-    L.wsc13 = take(16 * (size_t)E * (size_t)(H / 128) * (size_t)(I / 128));
-    L.wsc2 = take(16 * (size_t)E * (size_t)(I / 128) * (size_t)((H + 255) / 256));
+    L.wsc13 = take(16 * (size_t)E * (size_t)((H + 127) / 128) * (size_t)((I + 127) / 128));
+    L.wsc2 = take(16 * (size_t)E * (size_t)((I + 127) / 128) * (size_t)((H + 255) / 256));
   }
   if (hostio) {
     L.hid = take(2 * (size_t)(T * H));
@@ -192,6 +192,16 @@ struct Checked {
   int64_t T;
 };
 
+// Layer shapes the library runs.  Multiples of 128 take either path.  A
+// ragged layer (H or I not a multiple of 128) runs on the prefill path,
+// whose tensor-map loads zero-fill the partial last blocks; it needs H a
+// multiple of 64 (the output is stored in 64-column quarters) and I a
+// multiple of 16 (16-byte rows and box coordinates), both at least 128.
+bool layer_shape_ok(int64_t H, int64_t I) {
+  if (H < 128 || I < 128 || H > 8192 || I > 8192) return false;
+  return H % 64 == 0 && I % 16 == 0;
+}
+
 // An optional MLP bias: fp32 [E, n], stride[1] == 1, expert stride
 // stride[0] >= n and a multiple of 4 elements, 16-byte aligned base.
 int check_bias(const moe_tensor* b, int64_t E, int64_t n) {
@@ -224,12 +234,13 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
   if (k < 1 || k > 64 || E < 1 || E > 4096) return MOE_ERR_ARG;
   if (w13->shape[2] != H || I2 % 2 != 0) return MOE_ERR_SHAPE;
   const int64_t I = I2 / 2;
-  if (H <= 0 || I <= 0 || H % 128 != 0 || I % 128 != 0) return MOE_ERR_SHAPE;
+  if (!layer_shape_ok(H, I)) return MOE_ERR_SHAPE;
   if (w2->shape[0] != E || w2->shape[1] != H || w2->shape[2] != I) return MOE_ERR_SHAPE;
   if (H > 8192 || I > 8192) return MOE_ERR_SHAPE;
   if (T > (1 << 24) / k) return MOE_ERR_ARG;
-  if ((rc = check_scale_bank(w13_scale, E, 2 * I / 128, H / 128, w13_scale_stride))) return rc;
-  if ((rc = check_scale_bank(w2_scale, E, H / 128, I / 128, w2_scale_stride))) return rc;
+  const int64_t hb = (H + 127) / 128, ib = (I + 127) / 128, i2b = (2 * I + 127) / 128;
+  if ((rc = check_scale_bank(w13_scale, E, i2b, hb, w13_scale_stride))) return rc;
+  if ((rc = check_scale_bank(w2_scale, E, hb, ib, w2_scale_stride))) return rc;
   if (!contiguous(w13) || !contiguous(w2)) return MOE_ERR_STRIDE;
   if (!contiguous(topk_ids) || !contiguous(topk_weights) || !contiguous(out)) return MOE_ERR_STRIDE;
   if (hidden->stride[1] != 1 || (T > 1 && hidden->stride[0] < H)) return MOE_ERR_STRIDE;
@@ -255,11 +266,11 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
   a.w13 = static_cast<const uint8_t*>(w13->data);
   a.w13s = static_cast<const uint16_t*>(w13_scale->data);
   a.s13_row = w13_scale_stride;
-  a.s13_exp = E > 1 ? w13_scale->stride[0] : (2 * I / 128) * w13_scale_stride;
+  a.s13_exp = E > 1 ? w13_scale->stride[0] : i2b * w13_scale_stride;
   a.w2 = static_cast<const uint8_t*>(w2->data);
   a.w2s = static_cast<const uint16_t*>(w2_scale->data);
   a.s2_row = w2_scale_stride;
-  a.s2_exp = E > 1 ? w2_scale->stride[0] : (H / 128) * w2_scale_stride;
+  a.s2_exp = E > 1 ? w2_scale->stride[0] : hb * w2_scale_stride;
   a.out = static_cast<uint16_t*>(out->data);
   a.T = (int)T;
   a.k = (int)k;
@@ -596,7 +607,7 @@ int moe_fp8_block_widen_e4m3(const uint8_t* codes, int64_t n, float* out, void* 
 }
 
 int moe_fp8_block_reserve(int64_t max_T, int32_t k, int64_t H, int64_t I, int32_t E, void* stream) {
-  if (max_T < 0 || k < 1 || k > 64 || E < 1 || E > 4096 || H <= 0 || I <= 0 || H % 128 || I % 128)
+  if (max_T < 0 || k < 1 || k > 64 || E < 1 || E > 4096 || !layer_shape_ok(H, I))
     return MOE_ERR_ARG;
   int dev, rc;
   if ((rc = device_ok(&dev))) return rc;

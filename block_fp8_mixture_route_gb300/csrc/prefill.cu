@@ -115,15 +115,19 @@ struct PrefillArgs {
   uint32_t* status;
 };
 
-// Weight block scales as fp32 records of four (two used), one per (expert,
-// K block, output tile), so one 16-byte tensor-map load brings the two
-// column-block scales a tile needs for one K block:
-//   wsc13[e][kb][p] = (w13 scale of gate block p, of up block p, 0, 0)
+// Weight block scales as fp32 records of four, one per (expert, K block,
+// output tile), so one 16-byte tensor-map load brings the column-block
+// scales a tile needs for one K block:
+//   wsc13[e][kb][p] = (scale of gate rows p*128.., of the first and of the
+//                      last of up rows p*128.., 0)
 //   wsc2 [e][kb][p] = (w2 scale of row block 2p, of row block 2p+1 or 0, 0, 0)
+// The scale blocks of w13 are 128 rows of the stacked [gate; up] bank, so
+// when I is not a multiple of 128 the up rows of one tile straddle two of
+// them: up row i uses block (I + i) / 128.
 __device__ void repack_weight_scales(const PrefillArgs& p, int64_t idx) {
   const LayerArgs& a = p.a;
-  const int np1 = a.I / 128, nk1 = a.H / 128;
-  const int np2 = (a.H + 255) / 256, nk2 = a.I / 128, nrow2 = a.H / 128;
+  const int np1 = (a.I + 127) / 128, nk1 = (a.H + 127) / 128;
+  const int np2 = (a.H + 255) / 256, nk2 = (a.I + 127) / 128, nrow2 = (a.H + 127) / 128;
   const int64_t n13 = (int64_t)a.E * nk1 * np1;
   const int64_t n2 = (int64_t)a.E * nk2 * np2;
   if (idx < n13) {
@@ -131,9 +135,12 @@ __device__ void repack_weight_scales(const PrefillArgs& p, int64_t idx) {
     const int kb = (int)((idx / np1) % nk1);
     const int e = (int)(idx / ((int64_t)np1 * nk1));
     const uint16_t* s = a.w13s + (int64_t)e * a.s13_exp + kb;
+    const int last = (2 * a.I + 127) / 128 - 1;   // last scale row of the stacked bank
+    const int ua = (a.I + pp * 128) / 128, ub = min((a.I + pp * 128 + 127) / 128, last);
     const float g = bf16_to_f32(s[(int64_t)pp * a.s13_row]);
-    const float u = bf16_to_f32(s[(int64_t)(np1 + pp) * a.s13_row]);
-    reinterpret_cast<float4*>(p.pb.wsc13)[idx] = make_float4(g, u, 0.f, 0.f);
+    const float u0 = bf16_to_f32(s[(int64_t)ua * a.s13_row]);
+    const float u1 = bf16_to_f32(s[(int64_t)ub * a.s13_row]);
+    reinterpret_cast<float4*>(p.pb.wsc13)[idx] = make_float4(g, u0, u1, 0.f);
     return;
   }
   idx -= n13;
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p, i
   pdl_wait();
   pdl_trigger();
   const LayerArgs& a = p.a;
-  const int groups = a.H / 128;
+  const int groups = (a.H + 127) / 128;   // the last one partial when H is not a multiple of 128
   const int nq = (groups + 3) / 4;
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (wid >= (int64_t)a.T * nq) return;
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(256) act_quant_permute_kernel(PrefillArgs p, i
   const int t = (int)(wid / nq);
   const bool first = (wid % nq) == 0;
   const int gi = (int)(wid % nq) * 4 + (lane >> 3);
-  const bool valid = gi < groups;
   const int col = gi * 128 + (lane & 7) * 16;
+  const bool valid = gi < groups && col < a.H;   // H is a multiple of 16
   float v[16];
   float m = 0.f;
   if (valid) {
@@ -381,7 +388,10 @@ struct RingPos {
 // the peer's, written by the peer's multicast.  So a stage is free again
 // only when both CTAs' MMAs have read it: each MMA commit arrives on the
 // empty barrier of both CTAs, which therefore count two arrivals.
-template <int MODE, bool BIAS = false>
+// BIAS: GEMM1 adds the optional MLP gate/up bias.  SPLIT: GEMM1 of a layer
+// whose I is not a multiple of 128, where each up tile's columns take two
+// weight scales (see repack_weight_scales).
+template <int MODE, bool BIAS = false, bool SPLIT = false>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ PfMaps m, PrefillArgs p, int ns) {
   using namespace pf;
@@ -447,9 +457,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int K = MODE == 1 ? a.H : a.I;
-  const int nkb = K / BK;
-  const int ngpt = (nkb + KG - 1) / KG;   // scale groups per tile
-  const int NBT = MODE == 1 ? a.I / 128 : (a.H + BN - 1) / BN;
+  const int nkb = (int)(((unsigned)K + BK - 1) / BK);   // a partial last K block reads zeros past K
+  const int ngpt = (nkb + KG - 1) / KG;                 // scale groups per tile
+  const int NBT = MODE == 1 ? (int)(((unsigned)a.I + 127) / 128) : (a.H + BN - 1) / BN;
   const int total = mtp2_s[E] * NBT;   // pair tiles
   const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // cluster index, clusters
 
@@ -556,6 +566,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int row = eq * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(eq * 32) << 16);
     const bool issuer = ew == 0 && lane == 0;
+    // first up column (within a tile) of the stacked bank's next scale block
+    const int split = SPLIT ? 128 - a.I % 128 : 128;
     int it = 0;
     RingPos gp;
     bool ok = true;
@@ -568,7 +580,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // this warp's column pair l, read at the tile start so that the loads
       // complete during the K loop
       float2 bg2 = make_float2(0.f, 0.f), bu2 = bg2;
-      if (BIAS) {
+      if (BIAS && nb * 128 + hf * 64 + 2 * lane < a.I) {   // columns past I keep h = 0
         const float* br = a.b13 + (int64_t)tl.e * a.b13_ld + nb * 128 + hf * 64 + 2 * lane;
         bg2 = __ldg(reinterpret_cast<const float2*>(br));
         bu2 = __ldg(reinterpret_cast<const float2*>(br + a.I));
@@ -582,11 +594,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         const int sub = kb % KG;
         const int buf = it & 1;
         if (sub == 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[gp.i], gp.ph));
-        float f0 = 0.f, f1 = 0.f;
+        float f0 = 0.f, f1 = 0.f, f1b = 0.f;
         if (ok) {
           const float sa = ring_a[gp.i * (SA_BYTES / 4) + sub * BM + row];
           f0 = sa * ring_w[gp.i * 32 + sub * 4];
           f1 = sa * ring_w[gp.i * 32 + sub * 4 + 1];
+          if (SPLIT) f1b = sa * ring_w[gp.i * 32 + sub * 4 + 2];
         }
         if (sub == KG - 1 || kb == nkb - 1) {
           __syncwarp();
@@ -602,10 +615,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
             tc::tmem_ld16x2_raw(tb + c * 16, tb + 128 + c * 16, r);
+            // up columns from `split` on lie in the next scale block of the stacked bank
+            const uint64_t ffu = SPLIT && hf * 64 + c * 16 >= split ? f2pack(f1b, f1b) : ff1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               ffma2(acc0[c * 8 + i], ff0, r[2 * i], r[2 * i + 1]);
-              ffma2(acc1[c * 8 + i], ff1, r[16 + 2 * i], r[16 + 2 * i + 1]);
+              ffma2(acc1[c * 8 + i], ffu, r[16 + 2 * i], r[16 + 2 * i + 1]);
             }
           }
         }
@@ -908,7 +923,8 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                            uint32_t* status, int device, cudaStream_t st, int* launches) {
   PrefillArgs p{a, rb, pb, status};
   const uint64_t R = (uint64_t)pb.rows;
-  const uint64_t np1 = a.I / 128, nk1 = a.H / 128, np2 = (a.H + 255) / 256, nk2 = a.I / 128;
+  const uint64_t np1 = (a.I + 127) / 128, nk1 = (a.H + 127) / 128, np2 = (a.H + 255) / 256,
+                 nk2 = (a.I + 127) / 128;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
@@ -928,7 +944,9 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
   const int sm1 = (int)pf_layout(1, ns1, a.E).total, sm2 = (int)pf_layout(2, ns2, a.E).total;
   // the gate/up projection with the optional MLP bias compiled in or out
-  auto gemm1 = a.b13 ? prefill_gemm_kernel<1, true> : prefill_gemm_kernel<1, false>;
+  const bool split = a.I % 128 != 0;
+  auto gemm1 = a.b13 ? (split ? prefill_gemm_kernel<1, true, true> : prefill_gemm_kernel<1, true, false>)
+                     : (split ? prefill_gemm_kernel<1, false, true> : prefill_gemm_kernel<1, false, false>);
   cudaError_t err;
   if ((err = note_error(
            cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1),
@@ -950,7 +968,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   if ((err = launch_check(launch_route(a.ids, a.S, a.E, rb, status, route_scratch, st, &nl), st, "route")))
     return err;
   stage_mark(st, 1);
-  const int64_t warps = (int64_t)a.T * ((a.H / 128 + 3) / 4);
+  const int64_t warps = (int64_t)a.T * (((a.H + 127) / 128 + 3) / 4);
   const int qblocks = (int)((warps + 7) / 8);
   const int64_t nrep = (int64_t)a.E * (nk1 * np1 + nk2 * np2);
   const int rblocks = (int)((nrep + 255) / 256);

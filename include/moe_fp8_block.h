@@ -89,7 +89,7 @@ enum {
   MOE_OK = 0,
   MOE_ERR_NULL = -1,          /* a required pointer or descriptor is NULL         */
   MOE_ERR_DTYPE = -2,         /* wrong element type                               */
-  MOE_ERR_SHAPE = -3,         /* inconsistent shapes; H or I not a multiple of 128 */
+  MOE_ERR_SHAPE = -3,         /* inconsistent shapes; unsupported H or I          */
   MOE_ERR_ALIGN = -4,         /* a base pointer is not 16-byte aligned            */
   MOE_ERR_STRIDE = -5,        /* unsupported stride (see each argument)           */
   MOE_ERR_ALIAS = -6,         /* out overlaps an input                            */
@@ -139,17 +139,22 @@ typedef struct {
  *                slot counts.
  *  topk_weights  fp32 [T, k], contiguous; used as given (no renormalisation).
  *  w13           e4m3 [E, 2I, H], contiguous; rows [0,I) gate, [I,2I) up.
- *  w13_scale     bf16 [E, 2I/128, >= H/128]; stride[2] == 1,
- *                stride[1] == w13_scale_stride >= H/128,
- *                stride[0] >= (2I/128) * w13_scale_stride.
+ *  w13_scale     bf16 [E, ceil(2I/128), >= ceil(H/128)]; stride[2] == 1,
+ *                stride[1] == w13_scale_stride >= ceil(H/128),
+ *                stride[0] >= ceil(2I/128) * w13_scale_stride.  The blocks
+ *                are 128 rows of the stacked [gate; up] bank, so when I is
+ *                not a multiple of 128 up row i uses block (I + i) / 128.
  *  w13_scale_stride  row stride of w13_scale in elements (read from the tensor
  *                by the caller; it may be padded).
  *  w2            e4m3 [E, H, I], contiguous.
- *  w2_scale      bf16 [E, H/128, >= I/128]; stride rules as for w13_scale
- *                with w2_scale_stride >= I/128.
+ *  w2_scale      bf16 [E, ceil(H/128), >= ceil(I/128)]; stride rules as for
+ *                w13_scale with w2_scale_stride >= ceil(I/128).
  *  out           bf16 [T, H], contiguous; must not overlap any input.
  *  stream        cudaStream_t.
- * H and I must be multiples of 128 and at most 8192; k in [1, 64];
+ * H and I in [128, 8192], H a multiple of 64 and I of 16.  A layer whose
+ * H or I is not a multiple of 128 ("ragged K", FreeToken PR #662, Tests:
+ * the last 128-wide K block of a projection is partial) runs on the prefill
+ * path; forcing the decode path on it returns MOE_ERR_SHAPE.  k in [1, 64];
  * E in [1, 4096]; T*k <= 2^24.  Every
  * base pointer must be 16-byte aligned.  T == 0 is a no-op returning MOE_OK.
  */

@@ -199,3 +199,19 @@ def test_bias_argument_errors(lib, tiny):
     assert _call_bias(lib, tiny, b13, big[1:].view(E, H)) == -4            # 16-byte alignment
     alias = torch.zeros(E * H, dtype=torch.float32)
     assert _call_bias(lib, tiny, b13, alias.view(E, H), out=alias.view(torch.bfloat16)[:4 * H].view(4, H)) == -6
+
+
+@pytest.mark.parametrize("H,I,ok", [(192, 144, True), (320, 176, True), (2880, 2880, True), (160, 256, False),
+                                    (256, 136, False), (64, 256, False), (256, 112, False)])
+def test_ragged_shape_rules(lib, H, I, ok):
+    """H must be a multiple of 64 and I of 16, both at least 128; multiples
+    of 128 are not required (ragged layers run on the prefill path)."""
+    shp = syn.MoeShape(E=2, H=H, I=I, k=2)
+    prob = syn.make_problem(shp, T=1, seed=0)
+    if ok and torch.cuda.is_available():
+        pytest.skip("host tensors: the valid call is only made without a GPU")
+    rc = _call(lib, prob)
+    if ok:
+        assert rc in (-8, -10)          # past every argument check, then no device
+    else:
+        assert rc == -3
