@@ -1279,14 +1279,14 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   if (want < nt) nt = want < 256 ? 256 : want;   // >= 256 threads: the activation CTAs rely on it
   const size_t rsm = route_smem_bytes(a.E, nt);
   auto prep = a.act8 ? decode_prep_kernel<true> : decode_prep_kernel<false>;
-  if ((err = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm))) return err;
+  if ((err = set_max_smem((const void*)prep, (int)rsm))) return err;
   // the gate/up projection for the activation format, with the optional
   // MLP bias compiled in or out
   auto gemm1 = a.act8 ? (a.b13 ? decode_gemm1_kernel<true, true> : decode_gemm1_kernel<true, false>)
                       : (a.b13 ? decode_gemm1_kernel<false, true> : decode_gemm1_kernel<false, false>);
   auto combine = a.b2 ? decode_combine_kernel<true> : decode_combine_kernel<false>;
-  if ((err = cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c1.smem))) return err;
-  if ((err = cudaFuncSetAttribute(decode_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.c2.smem)))
+  if ((err = set_max_smem((const void*)gemm1, p.c1.smem))) return err;
+  if ((err = set_max_smem((const void*)decode_gemm2_kernel, p.c2.smem)))
     return err;
   // prep: route (CTA 0) + f16 activations (CTAs 1..T)
   const bool timed = stage_mark(st, 0);

@@ -378,6 +378,20 @@ int choose_path(const LayerArgs& a, float ratio, int force) {
   return gathered && decode_ring_stages(a.H, a.I) >= 4 ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
+// Device address of page-locked host memory that kernels can read and write
+// in place (cudaHostAlloc / cudaHostRegister memory, mapped into the unified
+// address space; on GB300 such accesses cross NVLink-C2C), or nullptr for
+// pageable memory.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost) return nullptr;
+  return at.devicePointer;
+}
+
 int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,
                  const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
                  const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
@@ -417,7 +431,25 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   void* ws = nullptr;
   if ((rc = get_workspace(st, L.total, &ws))) return rc;
   char* w = static_cast<char*>(ws);
+  // Page-locked host buffers (all four, not overlapping the output) are
+  // read and written in place by the kernels: no staging copies.
+  bool in_place = false;
   if (hostio) {
+    void* dh = mapped_host(hidden->data);
+    void* di = mapped_host(topk_ids->data);
+    void* dw = mapped_host(topk_weights->data);
+    void* dout = mapped_host(out->data);
+    in_place = dh && di && dw && dout && aligned16(dh) && aligned16(di) && aligned16(dw) && aligned16(dout) &&
+               !overlap(out, hidden) && !overlap(out, topk_ids) && !overlap(out, topk_weights);
+    if (in_place) {
+      a.hidden = static_cast<const uint16_t*>(dh);
+      a.hidden_ld = a.H;
+      a.ids = static_cast<const int32_t*>(di);
+      a.wts = static_cast<const float*>(dw);
+      a.out = static_cast<uint16_t*>(dout);
+    }
+  }
+  if (hostio && !in_place) {
     const size_t xb = 2 * (size_t)a.T * a.H, sb = 4 * (size_t)a.S;
     if (cudaMemcpyAsync(w + L.hid, hidden->data, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(w + L.tids, topk_ids->data, sb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -434,8 +466,8 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   rc = run_forward(a, ratio, path, st, hostio, ws, L, dev);
   if (rc) return rc;
   if (hostio) {
-    if (cudaMemcpyAsync(out->data, w + L.outb, 2 * (size_t)a.T * a.H, cudaMemcpyDeviceToHost, st) !=
-            cudaSuccess ||
+    if ((!in_place &&
+         cudaMemcpyAsync(out->data, w + L.outb, 2 * (size_t)a.T * a.H, cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
         cudaStreamSynchronize(st) != cudaSuccess) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
@@ -491,6 +523,26 @@ int validate_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const
   *args = c.a;
   if (c.T == 0) return MOE_OK;
   return device_ok(device);
+}
+
+static std::mutex g_smem_mu;
+static std::map<std::pair<int, const void*>, int> g_smem_set;
+
+cudaError_t set_max_smem(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_smem_mu);
+  int& cur = g_smem_set[{dev, func}];
+  if (cur >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
+void clear_smem_attributes() {
+  std::lock_guard<std::mutex> lk(g_smem_mu);
+  g_smem_set.clear();
 }
 
 void set_error_detail(const char* text) { snprintf(g_err_detail, sizeof(g_err_detail), "%s", text); }
@@ -681,6 +733,7 @@ void moe_fp8_block_release(void) {
   for (auto& kv : g_ws)
     if (kv.second.base) cudaFree(kv.second.base);
   g_ws.clear();
+  clear_smem_attributes();
 }
 
 }  // extern "C"

@@ -74,6 +74,13 @@ int64_t prefill_rows(int64_t S, int E);
 
 int num_sms(int device);
 
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) on the
+// current device, skipped when an earlier call there already allowed at
+// least `bytes` (it costs host time on every forward otherwise).
+// clear_smem_attributes forgets what was set (moe_fp8_block_release).
+cudaError_t set_max_smem(const void* func, int bytes);
+void clear_smem_attributes();
+
 // Argument checks of moe_fp8_block_forward for other entry points: fills
 // *args and, when T > 0, the current device (which must be sm_103).
 int validate_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe_tensor* topk_weights,

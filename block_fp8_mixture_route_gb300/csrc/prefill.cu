@@ -949,11 +949,11 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
                      : (split ? prefill_gemm_kernel<1, false, true> : prefill_gemm_kernel<1, false, false>);
   cudaError_t err;
   if ((err = note_error(
-           cudaFuncSetAttribute(gemm1, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1),
+           set_max_smem((const void*)gemm1, sm1),
            "prefill_gemm1 smem attribute")))
     return err;
   if ((err = note_error(
-           cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2),
+           set_max_smem((const void*)prefill_gemm_kernel<2>, sm2),
            "prefill_gemm2 smem attribute")))
     return err;
   const int sms = num_sms(device);

@@ -119,19 +119,19 @@ cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, 
   if (G <= 1) {
     const int nt = route_threads(E);
     const size_t sm = route_smem_bytes(E, nt);
-    if ((err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
+    if ((err = set_max_smem((const void*)route_kernel, (int)sm)))
       return err;
     route_kernel<<<1, nt, sm, st>>>(ids, S, E, rb, status);
     if (launches) *launches += 1;
     return cudaGetLastError();
   }
   const int chunk = (S + G - 1) / G;
-  if ((err = cudaFuncSetAttribute(route_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E * 4)))
+  if ((err = set_max_smem((const void*)route_count_kernel, E * 4)))
     return err;
-  if ((err = cudaFuncSetAttribute(route_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, E * 4))) return err;
+  if ((err = set_max_smem((const void*)route_scan_kernel, E * 4))) return err;
   const int nt = route_threads(E);
   const size_t psm = route_smem_bytes(E, nt);
-  if ((err = cudaFuncSetAttribute(route_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm)))
+  if ((err = set_max_smem((const void*)route_place_kernel, (int)psm)))
     return err;
   if ((err = launch_k(route_count_kernel, dim3(G), dim3(256), (size_t)E * 4, st, false, ids, S, E, chunk, scratch,
                       status)))

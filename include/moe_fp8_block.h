@@ -198,11 +198,13 @@ int moe_fp8_block_forward_bias(const moe_tensor* hidden, const moe_tensor* topk_
                                const moe_options* opt);
 
 /* As moe_fp8_block_forward_ex, but hidden, topk_ids, topk_weights and out
- * are HOST buffers (page-locked memory gives asynchronous copies; pageable
- * memory works but copies synchronously).  The weight banks stay device
- * memory.  The inputs are copied to the workspace, the forward runs and the
- * output is copied back, all on `stream`; the call returns after
- * synchronising `stream`, with `out` filled. */
+ * are HOST buffers; the weight banks stay device memory.  When all four are
+ * page-locked (cudaHostAlloc, cudaHostRegister, torch pin_memory), 16-byte
+ * aligned and `out` overlaps no input, the kernels read the inputs and write
+ * the output in place, over the host link, with no staging copies.
+ * Otherwise the inputs are copied to the workspace and the output back (a
+ * pageable buffer copies synchronously).  Everything runs on `stream`; the
+ * call returns after synchronising `stream`, with `out` filled. */
 int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* topk_ids,
                                  const moe_tensor* topk_weights, const moe_tensor* w13,
                                  const moe_tensor* w13_scale, int64_t w13_scale_stride,

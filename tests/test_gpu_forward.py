@@ -177,6 +177,25 @@ def test_hostio_matches_device(cuda_lib):
     assert torch.equal(out, dev_out.cpu())
 
 
+def test_hostio_pageable_and_prefill(cuda_lib):
+    """Host buffers: pageable ones are staged through the workspace, page-locked
+    ones are read and written in place by the kernels; both give the device
+    call's output, on the decode and the prefill path."""
+    for shape, T, path in ((syn.DECODE_SMALL, 4, "decode"), (syn.PREFILL, 64, "prefill")):
+        prob = problem(shape, T)
+        dev_out = api.forward_problem(prob, force_path=path)
+        torch.cuda.synchronize()
+        for pinned in (False, True):
+            h, i, w = (prob[n].cpu() for n in ("hidden", "topk_ids", "topk_weights"))
+            out = torch.full((T, shape.H), float("nan"), dtype=torch.bfloat16)
+            if pinned:
+                h, i, w, out = h.pin_memory(), i.pin_memory(), w.pin_memory(), out.pin_memory()
+            api.moe_fp8_block_forward_hostio(h, i, w, prob["w13"], prob["w13_scale"], prob["w13_scale"].stride(1),
+                                             prob["w2"], prob["w2_scale"], prob["w2_scale"].stride(1), out=out,
+                                             force_path=path)
+            assert torch.equal(out, dev_out.cpu()), (path, pinned)
+
+
 def test_empty_and_all_skipped(cuda_lib):
     prob = problem(syn.TINY, 0)
     out = api.forward_problem(prob)
