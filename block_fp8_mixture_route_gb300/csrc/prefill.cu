@@ -249,7 +249,7 @@ constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 // offsets from a 1024-aligned base; the same function on host and device).
 // Every tensor-copy destination or source is 128-byte aligned.
 struct PfLayout {
-  uint32_t out, ring_a, ring_w, xch, bars, mtp, mtp2, total;
+  uint32_t out, ring_a, ring_w, xch, bars, mtp, total;
 };
 
 __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
@@ -268,8 +268,6 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   o = (o + 15u) & ~15u;
   L.mtp = o;
   o += 4u * (uint32_t)(E + 1);
-  L.mtp2 = o;
-  o += 4u * (uint32_t)(E + 1);
   L.total = o + 1024;   // slack for aligning the dynamic shared memory base
   return L;
 }
@@ -278,7 +276,7 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
 // one load brings a gate block and the matching up block), A scales (K-block
 // major), B scale records, and the output(s).
 struct PfMaps {
-  CUtensorMap a, b, sa, sw, o, os;
+  CUtensorMap a, ah, b, sa, sw, o, os;   // ah: A in 64-row boxes (A-shared pair tiles)
 };
 
 // Largest expert e with mtp[e] <= mi (the expert owning 128-row tile mi).
@@ -344,25 +342,40 @@ __device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const ui
   }
 }
 
-// A tile of a CTA pair: the two CTAs of a cluster take M tiles 2j and 2j+1
-// of the same expert and the same column block nb, so they share the B
-// operand (each loads one half and multicasts it to both).  When the expert
-// has an odd number of M tiles, the second CTA's last tile is a phantom: it
-// loads and multiplies like a real one but stores nothing.
+// A tile of a CTA pair.  Pair tiles come in units of h = ceil(NBT / 2), one
+// unit per 128-row M tile of the padded routed order (mtp[E] units in all):
+//  - M tiles 2i and 2i+1 of an expert (B shared): the two CTAs take one M
+//    tile each and the same column block nb, so each loads its own A rows and
+//    one half of B, multicast to both.  The pair's two units cover column
+//    blocks 0..h-1 and h..2h-1.
+//  - the last M tile of an expert with an odd count (A shared): both CTAs take
+//    that M tile and adjacent column blocks 2w and 2w+1, so each loads one
+//    64-row half of A, multicast to both, and its own whole B.
+// A column block past NBT (odd NBT) is a phantom: it loads zeros past the
+// tensors and multiplies like a real one but stores nothing.
 struct PairTile {
   int mi, nb, e;
   bool real;
+  bool ashared;
 };
 
-__device__ __forceinline__ PairTile pair_tile(const int* mtp, const int* mtp2, int E, int NBT, int pt,
-                                              uint32_t rank) {
+__device__ __forceinline__ PairTile pair_tile(const int* mtp, int E, int NBT, int pt, uint32_t rank) {
   PairTile r;
-  const int mp = pt / NBT;
-  r.nb = pt - mp * NBT;
-  r.e = expert_of_tile(mtp2, E, mp);
-  const int j = 2 * (mp - mtp2[r.e]) + (int)rank;
-  r.mi = mtp[r.e] + j;
-  r.real = j < mtp[r.e + 1] - mtp[r.e];
+  const int h = (NBT + 1) >> 1;
+  const int mt = pt / h;   // unit = M tile of the padded order
+  const int w = pt - mt * h;
+  r.e = expert_of_tile(mtp, E, mt);
+  const int j = mt - mtp[r.e];
+  const int m = mtp[r.e + 1] - mtp[r.e];
+  r.ashared = j >= (m & ~1);
+  if (!r.ashared) {
+    r.mi = mtp[r.e] + (j & ~1) + (int)rank;
+    r.nb = (j & 1) * h + w;
+  } else {
+    r.mi = mtp[r.e] + j;
+    r.nb = 2 * w + (int)rank;
+  }
+  r.real = r.nb < NBT;
   return r;
 }
 
@@ -383,11 +396,11 @@ struct RingPos {
 // Launched in clusters of two CTAs.  10 warps per CTA: warp 0 issues
 // tensor-map loads, warp 1 owns TMEM and issues the MMAs, warps 2..9
 // promote, finish and store.  Cluster c takes pair tiles c, c + clusters,
-// ...; pair tile pt = (tile pair pt / NBT, column block pt % NBT).
-// A stage holds this CTA's A rows and both halves of B: its own half and
-// the peer's, written by the peer's multicast.  So a stage is free again
-// only when both CTAs' MMAs have read it: each MMA commit arrives on the
-// empty barrier of both CTAs, which therefore count two arrivals.
+// ... (pair_tile).  A stage holds a 128-row A tile and a 256-row B tile, part
+// of which the peer writes by multicast (a B half, or an A half).  So a
+// stage is free again only when both CTAs' MMAs have read it: each MMA
+// commit arrives on the empty barrier of both CTAs, which therefore count
+// two arrivals.
 // BIAS: GEMM1 adds the optional MLP gate/up bias.  SPLIT: GEMM1 of a layer
 // whose I is not a multiple of 128, where each up tile's columns take two
 // weight scales (see repack_weight_scales).
@@ -411,7 +424,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   float* ring_w = reinterpret_cast<float*>(base + L.ring_w);
   float* xch = reinterpret_cast<float*>(base + L.xch);
   int* mtp_s = reinterpret_cast<int*>(base + L.mtp);
-  int* mtp2_s = reinterpret_cast<int*>(base + L.mtp2);
   const uint32_t rank = tc::cluster_ctarank();
   constexpr uint16_t kPair = 0x3;
   uint8_t* outs = base + L.out;
@@ -434,6 +446,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     fence_mbar_init();
     abort_flag = 0;
     tc::prefetch_tensormap(&m.a);
+    tc::prefetch_tensormap(&m.ah);
     tc::prefetch_tensormap(&m.b);
     tc::prefetch_tensormap(&m.sa);
     tc::prefetch_tensormap(&m.sw);
@@ -446,7 +459,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // the tile tables, read once before any tensor-map traffic starts
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     mtp_s[i] = __ldg(p.rb.mtp + i);
-    mtp2_s[i] = __ldg(p.rb.mtp2 + i);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -460,7 +472,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const int nkb = (int)(((unsigned)K + BK - 1) / BK);   // a partial last K block reads zeros past K
   const int ngpt = (nkb + KG - 1) / KG;                 // scale groups per tile
   const int NBT = MODE == 1 ? (int)(((unsigned)a.I + 127) / 128) : (a.H + BN - 1) / BN;
-  const int total = mtp2_s[E] * NBT;   // pair tiles
+  const int total = mtp_s[E] * ((NBT + 1) >> 1);   // pair tiles
   const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // cluster index, clusters
 
   if (warp == 0) {
@@ -479,7 +491,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         for (; n_g < upto; ++n_g, gp.next(NSG)) {
           if (n_g >= NSG && !mbar_wait(&sempty[gp.i], gp.ph ^ 1u)) return false;
           const int ti = n_g / ngpt, g = n_g - ti * ngpt;
-          const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, bx + ti * gx, rank);
+          const PairTile tl = pair_tile(mtp_s, E, NBT, bx + ti * gx, rank);
           mbar_arrive_expect_tx(&sfull[gp.i], SA_BYTES + SW_BYTES);
           tc::tma_load_2d(ring_a + gp.i * (SA_BYTES / 4), &m.sa, tl.mi * BM, g * KG, &sfull[gp.i], pol);
           tc::tma_load_2d(ring_w + gp.i * 32, &m.sw, 4 * tl.nb, tl.e * nkb + g * KG, &sfull[gp.i], pol);
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       };
       int ti = 0;
       for (int t = bx; t < total && ok; t += gx, ++ti) {
-        const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, t, rank);
+        const PairTile tl = pair_tile(mtp_s, E, NBT, t, rank);
         const int p0 = tl.mi * BM;
         uint8_t* const bhalf = base + A_BYTES + rank * (B_BYTES / 2);   // + stage offset
         for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(ns)) {
@@ -501,16 +513,33 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             break;
           }
           uint8_t* st = base + sp.i * STAGE;
-          // A of this CTA's rows, 16 KB; B: this CTA's half, 16 KB, to both CTAs;
-          // the peer's half arrives the same way: 48 KB land here in all
+          // 48 KB land in each CTA's stage either way
           mbar_arrive_expect_tx(&full[sp.i], STAGE);
-          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
-          if (MODE == 1)   // rank 0: gate block nb, rank 1: up block nb
-            tc::tma_load_3d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + (int)rank, &full[sp.i],
-                               kPair, pol);
-          else             // rank r: rows 128 r .. 128 r + 127 of the 256-row block
-            tc::tma_load_2d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128 * (int)rank,
-                               &full[sp.i], kPair, pol);
+          if (!tl.ashared) {
+            // A of this CTA's rows, 16 KB; B: this CTA's half, 16 KB, to both
+            // CTAs; the peer's half arrives the same way
+            tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
+            if (MODE == 1)   // rank 0: gate block nb, rank 1: up block nb
+              tc::tma_load_3d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + (int)rank,
+                                 &full[sp.i], kPair, pol);
+            else             // rank r: rows 128 r .. 128 r + 127 of the 256-row block
+              tc::tma_load_2d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128 * (int)rank,
+                                 &full[sp.i], kPair, pol);
+          } else {
+            // A: rows 64 r .. 64 r + 63 of the shared M tile, 8 KB, to both
+            // CTAs (the peer sends the other half); B: this CTA's whole block
+            tc::tma_load_2d_mc(st + rank * (A_BYTES / 2), &m.ah, kb * BK, p0 + 64 * (int)rank, &full[sp.i], kPair,
+                               pol);
+            if (MODE == 1) {
+              tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], pol);
+              tc::tma_load_3d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
+                              pol);
+            } else {
+              tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], pol);
+              tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128,
+                              &full[sp.i], pol);
+            }
+          }
         }
         if (*(volatile int*)&abort_flag) ok = false;
       }
@@ -572,7 +601,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     RingPos gp;
     bool ok = true;
     for (int t = bx; t < total; t += gx) {
-      const PairTile tl = pair_tile(mtp_s, mtp2_s, E, NBT, t, rank);
+      const PairTile tl = pair_tile(mtp_s, E, NBT, t, rank);
       const int nb = tl.nb;
       const int p0 = tl.mi * BM;
       const bool has1 = MODE == 1 || nb * BN + 128 < a.H;
@@ -928,6 +957,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
+            make_map(&g1.ah, U8, 1, pb.xq, R, a.H, a.H, 128, 64, true) &&
             make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
             make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, pf::KG, false) &&
             make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
@@ -939,6 +969,8 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
        make_map_ys(&g2.o, pb.ys, R, a.H);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.a = g1.o;
+  if (!make_map(&g2.ah, U8, 1, pb.hq, R, a.I, a.I, 128, 64, true))
+    return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.os = g2.o;
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
