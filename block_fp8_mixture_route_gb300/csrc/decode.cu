@@ -1,6 +1,6 @@
 // decode.cu -- the decode (W8A16) path of the block-FP8 MoE layer.
 //
-// At small token counts each token routes to only top_k experts, so the
+// With few tokens, only a handful of experts receive any slot, and the
 // layer is bound by reading the routed experts' weights (fp8-moe-gather
 // page, Problem).  This path reads only those experts (the gathered-expert
 // combine, same page, The fix).  Their e4m3 rows are streamed from HBM into

@@ -262,8 +262,8 @@ int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, const moe_ten
  *  inv      int32 [S]     position of slot s in perm, or -1 when skipped
  *  glist    int32 [min(E,S)] distinct routed experts ascending, padded with -1
  *  n_distinct int32 [1]   number of distinct routed experts
- * ("the g = min(local_experts, tokens * top_k) routed experts are gathered",
- * fp8-moe-gather page, The fix.)  All outputs are device int32 buffers of the
+ * (At most g = min(E, T*k) experts are read, the routed ones: fp8-moe-gather
+ * page, The fix.)  All outputs are device int32 buffers of the
  * sizes above, contiguous.  Requires S <= 2^24.
  */
 int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts,

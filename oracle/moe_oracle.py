@@ -9,14 +9,18 @@ What it computes, step by step (float64 unless a step says otherwise):
 1. e4m3 decoding by a 256-entry table built from the format's definition:
    sign s = b>>7, exponent e = (b>>3)&15, mantissa m = b&7; e == 0 is
    subnormal, m * 2^-9; e == 15 and m == 7 is NaN; otherwise
-   (1 + m/8) * 2^(e-7).  ("The normal range rebases the exponent ...;
-   exp == 0 is subnormal (m * 2^-9)", FreeToken PR #662, PR body; "e4m3's
-   whole 2^-9..448 span", same passage.)
+   (1 + m/8) * 2^(e-7).  (FreeToken PR #662, PR body: normal codes take a
+   rebased exponent, a zero exponent field marks a subnormal m * 2^-9, and
+   the finite magnitudes run from 2^-9 to 448.)
 2. Block dequantisation: weight banks are e4m3 row-major [rows, K], K
-   contiguous, with one bf16 scale per 128x128 block (FreeToken PR #662, PR
+   contiguous, with a bf16 scale for each 128 x 128 block (FreeToken PR #662, PR
    body).  The scale of element (n, kk) is scale[n // 128, kk // 128], read
    through the row stride of the scale bank, which may be padded ("honor
-   padded fp8 scale strides" commit of the same PR).
+   padded fp8 scale strides" commit of the same PR).  When K or the row count
+   is not a multiple of 128 the last block is partial (same PR, Tests: the
+   ragged-K case); the stacked [gate; up] bank is blocked over its 2I rows
+   from row 0, so with I not a multiple of 128 one block holds gate and up
+   rows.
 3. Activations: W8A16 mode uses the bf16 activations as they are (the CPU
    and GPU decode kernels of FreeToken PR #662, "Call path" / "Kernels").
    W8A8 mode quantises them per token per 128-column group with a dynamic
@@ -46,8 +50,8 @@ What it computes, step by step (float64 unless a step says otherwise):
    evaluation (the stock mixture_of_experts op of the fp8-moe-gather page,
    "Problem", reads every expert) computes y_e for every expert and masks
    it with c[t,e] = sum_{j: ids[t,j]=e} w[t,j]; the gathered evaluation
-   ("The fix": only the g = min(local_experts, tokens*top_k) routed experts
-   are gathered) visits routed experts only.  Both are the same number up to
+   (section The fix: it reads at most g = min(E_local, T*k) experts, those
+   that are routed) visits routed experts only.  Both are the same number up to
    float64 rounding.
 6. Routing lists: a counting sort of the slots s = t*k + j by expert id,
    stable in s; ids outside [0, E) are skipped.
@@ -290,6 +294,7 @@ def route_lists(topk_ids: np.ndarray, E: int):
 
 
 def gate_takes_gathered_path(T: int, k: int, E: int, ratio: float = 0.4) -> bool:
-    """The path gate: gathered while tokens * top_k <= local_experts * ratio
-    (fp8-moe-gather page, environment-variable table, default ratio 0.4)."""
+    """The path gate: gathered when T*k <= E*ratio (slots against local experts
+    times the ratio; fp8-moe-gather page, environment-variable table,
+    default ratio 0.4)."""
     return T * k <= E * ratio
