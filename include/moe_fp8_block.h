@@ -13,7 +13,7 @@
  *
  * Weight format (FreeToken PR #662, PR body): every expert bank is e4m3
  * (float8 e4m3fn bytes) row-major [rows, K], K contiguous per output row,
- * with one bf16 scale per 128x128 block.  The scale bank's row stride may be
+ * with a bf16 scale for each 128 x 128 block.  The scale bank's row stride may be
  * padded (same PR, commit "honor padded fp8 scale strides"), so it is passed
  * explicitly and never recomputed from K.  w13 stacks the gate and up
  * projections along the output rows: rows [0, I) gate, rows [I, 2I) up

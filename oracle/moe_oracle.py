@@ -7,8 +7,8 @@ library and its Python binding) never calls it and shares no code with it.
 What it computes, step by step (float64 unless a step says otherwise):
 
 1. e4m3 decoding by a 256-entry table built from the format's definition:
-   sign s = b>>7, exponent e = (b>>3)&15, mantissa m = b&7; e == 0 is
-   subnormal, m * 2^-9; e == 15 and m == 7 is NaN; otherwise
+   sign s = b>>7, exponent e = (b>>3)&15, mantissa m = b&7; a zero e gives
+   the subnormal m * 2^-9; e == 15 with m == 7 is NaN; otherwise
    (1 + m/8) * 2^(e-7).  (FreeToken PR #662, PR body: normal codes take a
    rebased exponent, a zero exponent field marks a subnormal m * 2^-9, and
    the finite magnitudes run from 2^-9 to 448.)
