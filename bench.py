@@ -184,8 +184,7 @@ def oracle_sample(problems, budget_s: float = 12.0):
     workload, smallest T first, until ~budget_s of CPU work; returns
     (routed bytes processed, seconds, description)."""
     from oracle import moe_oracle as mo
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from helpers import oracle_args
+    from oracle.host_inputs import oracle_args
     done_bytes, secs, parts = 0, 0.0, []
     for T in DECODE_TS:
         prob = problems[T]

@@ -12,7 +12,7 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe_fp8_block.so")
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 MOE_BF16, MOE_F32, MOE_E4M3, MOE_I32 = 1, 2, 3, 4
 MOE_PATH_NONE, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
@@ -28,7 +28,7 @@ ERRORS = {
 EXPORTS = [
     "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_bias",
     "moe_fp8_block_forward_hostio",
-    "moe_fp8_block_forward_decode_noalloc",
+    "moe_fp8_block_forward_decode_noalloc", "moe_fp8_block_forward_act_codes",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
     "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_last_error_detail", "moe_fp8_block_error_string",
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_forward_hostio.argtypes = fwd + [P(MoeOptions)]
         lib.moe_fp8_block_forward_bias.argtypes = fwd[:9] + [T, T] + fwd[9:] + [P(MoeOptions)]
         lib.moe_fp8_block_forward_decode_noalloc.argtypes = fwd
+        lib.moe_fp8_block_forward_act_codes.argtypes = fwd + [P(MoeOptions), vp, vp]
         lib.moe_fp8_block_route.argtypes = [T, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.moe_fp8_block_act_quant.argtypes = [T, vp, vp, vp]
         lib.moe_fp8_block_widen_e4m3.argtypes = [vp, i64, vp, vp]

@@ -144,6 +144,30 @@ def moe_fp8_block_forward_decode_noalloc(hidden, topk_ids, topk_weights, w13, w1
     return out
 
 
+def moe_fp8_block_forward_act_codes(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
+                                    w2_scale, w2_scale_stride, out=None, stream=None, gate_ratio=None,
+                                    force_path=None, decode_act=None):
+    """Layer forward that also returns the activation codes and group scales
+    its own quantiser produced: (out, codes uint8 [T, H], scales fp32
+    [T, ceil(H/128)])."""
+    lib = _lib.load()
+    T, H = hidden.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    codes = torch.zeros((T, H), dtype=torch.uint8, device=hidden.device)
+    scales = torch.zeros((T, (H + 127) // 128), dtype=torch.float32, device=hidden.device)
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    o = desc(out)
+    P = ctypes.byref
+    opt = _options(gate_ratio, force_path, decode_act) or MoeOptions()
+    rc = lib.moe_fp8_block_forward_act_codes(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                             int(w2_scale_stride), P(o), _stream(stream), P(opt),
+                                             codes.data_ptr(), scales.data_ptr())
+    check(rc, "moe_fp8_block_forward_act_codes")
+    return out, codes, scales
+
+
 def moe_fp8_block_route(topk_ids: torch.Tensor, E: int, stream=None):
     """Routing lists (see the header): dict of int32 device tensors."""
     lib = _lib.load()

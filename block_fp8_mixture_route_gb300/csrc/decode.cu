@@ -141,15 +141,20 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
       for (int o = 1; o < 16; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
       if (valid) {
         const float sc = __fdiv_rn(gm, 448.0f);
-        uint32_t o4[4];
+        uint32_t o4[4], q4[2] = {0u, 0u};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint16_t q = sc != 0.f ? e4m3x2_from_f32(__fdiv_rn(v[c][2 * j], sc), __fdiv_rn(v[c][2 * j + 1], sc))
                                        : (uint16_t)0;
           o4[j] = e4m3x2_to_f16x2(q);
+          q4[j >> 1] |= (uint32_t)q << (16 * (j & 1));
         }
         *reinterpret_cast<uint4*>(p.db.xh + (int64_t)t * a.H + i0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
         if ((threadIdx.x & 15) == 0) p.db.xs[(int64_t)t * (a.H / 128) + i0 / 128] = sc;
+        if (a.dbg_codes) {   // moe_fp8_block_forward_act_codes: the codes and scales as quantised here
+          *reinterpret_cast<uint2*>(a.dbg_codes + (int64_t)t * a.H + i0) = make_uint2(q4[0], q4[1]);
+          if ((threadIdx.x & 15) == 0) a.dbg_scales[(int64_t)t * (a.H / 128) + i0 / 128] = sc;
+        }
       }
     }
     if (threadIdx.x == 0) p.db.xexp[t] = 0;

@@ -347,6 +347,10 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     pb.wsc2 = reinterpret_cast<float*>(w + L.wsc2);
     pb.rows = L.prows;
     err = launch_prefill(a, rb, pb, reinterpret_cast<int32_t*>(w + L.rcnt), status, dev, st, &launches);
+    if (err == cudaSuccess && a.dbg_codes) {
+      err = note_error(launch_prefill_act_codes(a, pb, st), "prefill_act_codes");
+      ++launches;
+    }
   }
   if (err == cudaErrorNotSupported) {
     cudaGetLastError();
@@ -396,7 +400,7 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
                  const moe_tensor* w13, const moe_tensor* w13_scale, int64_t w13_scale_stride,
                  const moe_tensor* w2, const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
                  void* stream, const moe_options* opt, bool hostio, const moe_tensor* w13_bias = nullptr,
-                 const moe_tensor* w2_bias = nullptr) {
+                 const moe_tensor* w2_bias = nullptr, uint8_t* dbg_codes = nullptr, float* dbg_scales = nullptr) {
   Checked c{};
   int rc = check_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                          w2_scale_stride, out, hostio, &c);
@@ -427,6 +431,12 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   a.act8 = act8;
   const int path = choose_path(a, ratio, force);
   if (path == MOE_PATH_DECODE && !decode_supported(a.H, a.I)) return MOE_ERR_SHAPE;
+  if (dbg_codes) {
+    // only a path that quantises its activations has codes to copy
+    if (path == MOE_PATH_DECODE && !act8) return MOE_ERR_ARG;
+    a.dbg_codes = dbg_codes;
+    a.dbg_scales = dbg_scales;
+  }
   const Layout L = make_layout(c.T, a.k, a.H, a.I, a.E, path, hostio);
   void* ws = nullptr;
   if ((rc = get_workspace(st, L.total, &ws))) return rc;
@@ -597,6 +607,17 @@ int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* top
                                  void* stream, const moe_options* opt) {
   return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                       w2_scale_stride, out, stream, opt, true);
+}
+
+int moe_fp8_block_forward_act_codes(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                    const moe_tensor* topk_weights, const moe_tensor* w13,
+                                    const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,
+                                    const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
+                                    void* stream, const moe_options* opt, uint8_t* codes, float* scales) {
+  if (!codes || !scales) return MOE_ERR_NULL;
+  if (!aligned16(codes)) return MOE_ERR_ALIGN;
+  return forward_impl(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                      w2_scale_stride, out, stream, opt, false, nullptr, nullptr, codes, scales);
 }
 
 int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, int32_t* offsets, int32_t* perm,

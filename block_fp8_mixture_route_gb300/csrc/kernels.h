@@ -29,6 +29,11 @@ struct LayerArgs {
   int64_t b13_ld = 0;
   const float* b2 = nullptr;   // optional fp32 [E, H] down-projection bias, expert stride b2_ld
   int64_t b2_ld = 0;
+  // optional copies of the activation codes and group scales the path's own
+  // quantiser produced (moe_fp8_block_forward_act_codes): e4m3 [T, H] and
+  // fp32 [T, ceil(H/128)], both row-contiguous
+  uint8_t* dbg_codes = nullptr;
+  float* dbg_scales = nullptr;
 };
 
 // Routing lists produced by the route kernel (device int32 buffers).
@@ -131,6 +136,10 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t ld, int R, int K, uint8_
                              cudaStream_t st, bool pdl);
 cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const PrefillBufs& pb, int32_t* route_scratch,
                            uint32_t* status, int device, cudaStream_t st, int* launches);
+// After a prefill forward on the same buffers: copy each token's activation
+// codes and scales from the GEMM input rows of one of its routed slots (slot
+// t mod k, else the next valid one) into a.dbg_codes / a.dbg_scales.
+cudaError_t launch_prefill_act_codes(const LayerArgs& a, const PrefillBufs& pb, cudaStream_t st);
 
 // Shared-memory bytes the route kernel needs for E experts with nthreads.
 size_t route_smem_bytes(int E, int nthreads);

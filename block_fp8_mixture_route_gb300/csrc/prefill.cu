@@ -276,7 +276,7 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
 // one load brings a gate block and the matching up block), A scales (K-block
 // major), B scale records, and the output(s).
 struct PfMaps {
-  CUtensorMap a, ah, b, sa, sw, o, os;   // ah: A in 64-row boxes (A-shared pair tiles)
+  CUtensorMap a, b, sa, sw, o, os;
 };
 
 // Largest expert e with mtp[e] <= mi (the expert owning 128-row tile mi).
@@ -342,21 +342,24 @@ __device__ __forceinline__ void stage_bf16_row64(uint8_t* box, int row, const ui
   }
 }
 
-// A tile of a CTA pair.  Pair tiles come in units of h = ceil(NBT / 2), one
-// unit per 128-row M tile of the padded routed order (mtp[E] units in all):
-//  - M tiles 2i and 2i+1 of an expert (B shared): the two CTAs take one M
-//    tile each and the same column block nb, so each loads its own A rows and
-//    one half of B, multicast to both.  The pair's two units cover column
-//    blocks 0..h-1 and h..2h-1.
-//  - the last M tile of an expert with an odd count (A shared): both CTAs take
-//    that M tile and adjacent column blocks 2w and 2w+1, so each loads one
-//    64-row half of A, multicast to both, and its own whole B.
-// A column block past NBT (odd NBT) is a phantom: it loads zeros past the
-// tensors and multiplies like a real one but stores nothing.
+// A tile of a CTA pair (CTAs 2c and 2c + 1 of the grid, rank = the low bit).
+// Pair tiles come in units of h = ceil(NBT / 2), one unit per 128-row M tile
+// of the padded routed order (mtp[E] units in all):
+//  - M tiles 2i and 2i+1 of an expert (same B): the two CTAs take one M tile
+//    each and the same column block nb, so they read the same weight block
+//    at about the same time and the second read finds it in L2.  The pair's
+//    two units cover column blocks 0..h-1 and h..2h-1.
+//  - the last M tile of an expert with an odd count (same A): both CTAs take
+//    that M tile and adjacent column blocks 2w and 2w+1.
+// Each CTA loads all of its own operands (its 128 A rows and its 256 B rows)
+// with plain tensor-map loads into its own shared memory; nothing is written
+// into the other CTA's shared memory.  A column block past NBT (odd NBT) is
+// a phantom: it loads zeros past the tensors and multiplies like a real one
+// but stores nothing.
 struct PairTile {
   int mi, nb, e;
   bool real;
-  bool ashared;
+  bool ashared;   // the last, odd M tile of its expert (both CTAs take it)
 };
 
 __device__ __forceinline__ PairTile pair_tile(const int* mtp, int E, int NBT, int pt, uint32_t rank) {
@@ -393,14 +396,12 @@ struct RingPos {
 
 // MODE 1: gate/up projection, silu(gate)*up, e4m3 h codes + scales.
 // MODE 2: down projection -> bf16 y rows.
-// Launched in clusters of two CTAs.  10 warps per CTA: warp 0 issues
-// tensor-map loads, warp 1 owns TMEM and issues the MMAs, warps 2..9
-// promote, finish and store.  Cluster c takes pair tiles c, c + clusters,
-// ... (pair_tile).  A stage holds a 128-row A tile and a 256-row B tile, part
-// of which the peer writes by multicast (a B half, or an A half).  So a
-// stage is free again only when both CTAs' MMAs have read it: each MMA
-// commit arrives on the empty barrier of both CTAs, which therefore count
-// two arrivals.
+// 10 warps per CTA: warp 0 issues tensor-map loads, warp 1 owns TMEM and
+// issues the MMAs, warps 2..9 promote, finish and store.  CTA pair c (CTAs
+// 2c and 2c + 1) takes pair tiles c, c + pairs, ... (pair_tile).  A stage
+// holds a 128-row A tile and a 256-row B tile, both loaded by the CTA itself;
+// it is free again once this CTA's MMAs have read it (one commit arrives on
+// its empty barrier).
 // BIAS: GEMM1 adds the optional MLP gate/up bias.  SPLIT: GEMM1 of a layer
 // whose I is not a multiple of 128, where each up tile's columns take two
 // weight scales (see repack_weight_scales).
@@ -424,8 +425,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   float* ring_w = reinterpret_cast<float*>(base + L.ring_w);
   float* xch = reinterpret_cast<float*>(base + L.xch);
   int* mtp_s = reinterpret_cast<int*>(base + L.mtp);
-  const uint32_t rank = tc::cluster_ctarank();
-  constexpr uint16_t kPair = 0x3;
+  const uint32_t rank = blockIdx.x & 1u;
   uint8_t* outs = base + L.out;
   __shared__ int abort_flag;
 
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < ns; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 2);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < NSG; ++i) {
       mbar_init(&sfull[i], 1);
@@ -446,7 +446,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     fence_mbar_init();
     abort_flag = 0;
     tc::prefetch_tensormap(&m.a);
-    tc::prefetch_tensormap(&m.ah);
     tc::prefetch_tensormap(&m.b);
     tc::prefetch_tensormap(&m.sa);
     tc::prefetch_tensormap(&m.sw);
@@ -462,8 +461,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  // both CTAs' barriers are initialised before either multicasts into the other
-  tc::cluster_sync();
   tc::fence_after_sync();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
@@ -473,7 +470,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const int ngpt = (nkb + KG - 1) / KG;                 // scale groups per tile
   const int NBT = MODE == 1 ? (int)(((unsigned)a.I + 127) / 128) : (a.H + BN - 1) / BN;
   const int total = mtp_s[E] * ((NBT + 1) >> 1);   // pair tiles
-  const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // cluster index, clusters
+  const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // pair index, pairs
 
   if (warp == 0) {
     // -------------------------------------------------- TMA producer
@@ -502,7 +499,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       for (int t = bx; t < total && ok; t += gx, ++ti) {
         const PairTile tl = pair_tile(mtp_s, E, NBT, t, rank);
         const int p0 = tl.mi * BM;
-        uint8_t* const bhalf = base + A_BYTES + rank * (B_BYTES / 2);   // + stage offset
         for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(ns)) {
           if (!issue_groups(ti * ngpt + kb / KG + 1 + LEAD_G)) {
             ok = false;
@@ -513,32 +509,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             break;
           }
           uint8_t* st = base + sp.i * STAGE;
-          // 48 KB land in each CTA's stage either way
+          // A: the tile's 128 rows, 16 KB; B: the column block's 256 rows, 32 KB
           mbar_arrive_expect_tx(&full[sp.i], STAGE);
-          if (!tl.ashared) {
-            // A of this CTA's rows, 16 KB; B: this CTA's half, 16 KB, to both
-            // CTAs; the peer's half arrives the same way
-            tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
-            if (MODE == 1)   // rank 0: gate block nb, rank 1: up block nb
-              tc::tma_load_3d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + (int)rank,
-                                 &full[sp.i], kPair, pol);
-            else             // rank r: rows 128 r .. 128 r + 127 of the 256-row block
-              tc::tma_load_2d_mc(bhalf + sp.i * STAGE, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128 * (int)rank,
-                                 &full[sp.i], kPair, pol);
-          } else {
-            // A: rows 64 r .. 64 r + 63 of the shared M tile, 8 KB, to both
-            // CTAs (the peer sends the other half); B: this CTA's whole block
-            tc::tma_load_2d_mc(st + rank * (A_BYTES / 2), &m.ah, kb * BK, p0 + 64 * (int)rank, &full[sp.i], kPair,
-                               pol);
-            if (MODE == 1) {
-              tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], pol);
-              tc::tma_load_3d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
-                              pol);
-            } else {
-              tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], pol);
-              tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128,
-                              &full[sp.i], pol);
-            }
+          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
+          if (MODE == 1) {   // gate block nb, then up block nb
+            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], pol);
+            tc::tma_load_3d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
+                            pol);
+          } else {           // rows nb * 256 .. + 255 of the expert's down projection
+            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], pol);
+            tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128, &full[sp.i],
+                            pol);
           }
         }
         if (*(volatile int*)&abort_flag) ok = false;
@@ -573,7 +554,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             tc::mma_f8(d, tc::sw128_desc(st + k * 32), tc::sw128_desc(st + A_BYTES + k * 32), idesc, k > 0);
-          tc::commit_mc(&empty[sp.i], kPair);
+          tc::commit(&empty[sp.i]);
           tc::commit(&tfull[buf]);
         }
         if (*(volatile int*)&abort_flag) ok = false;
@@ -582,8 +563,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         abort_flag = 1;
         raise_status(p.status, MOE_STATUS_TIMEOUT);
       }
-      // the last commits must land before TMEM is released, and the peer's
-      // commits to this CTA's stage barriers before the CTA goes away
+      // the last commits must land before TMEM is released and the CTA goes away
       if (it > 0) mbar_wait(&tfull[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1);
       for (int i = it > ns ? it - ns : 0; i < it; ++i) mbar_wait(&empty[i % ns], (uint32_t)(i / ns) & 1);
     }
@@ -740,7 +720,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // ---------------------------------------------------------- teardown
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync();   // the peer no longer writes into this CTA's shared memory
   tc::fence_after_sync();
   if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -807,6 +786,30 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillArgs p) {
   *reinterpret_cast<uint4*>(a.out + (int64_t)t * a.H + n) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ------------------------------------------------- activation code copy ----
+// Token t's codes and scales as the GEMMs read them: from the row of one of
+// its routed slots (slot t mod k, else the next valid one).  A token with no
+// valid slot has no row and is left untouched.
+__global__ void __launch_bounds__(128) prefill_act_codes_kernel(PrefillArgs p) {
+  const LayerArgs& a = p.a;
+  const int t = blockIdx.x;
+  int64_t row = -1;
+  for (int jj = 0; jj < a.k && row < 0; ++jj) row = p.pb.pinv[(int64_t)t * a.k + (t + jj) % a.k];
+  if (row < 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(p.pb.xq + row * a.H);
+  uint4* dst = reinterpret_cast<uint4*>(a.dbg_codes + (int64_t)t * a.H);
+  for (int i = threadIdx.x; i < a.H / 16; i += blockDim.x) dst[i] = src[i];
+  const int nkb = (a.H + 127) / 128;
+  for (int kb = threadIdx.x; kb < nkb; kb += blockDim.x)
+    a.dbg_scales[(int64_t)t * nkb + kb] = p.pb.xsT[(int64_t)kb * p.pb.rows + row];
+}
+
+cudaError_t launch_prefill_act_codes(const LayerArgs& a, const PrefillBufs& pb, cudaStream_t st) {
+  PrefillArgs p{a, RouteBufs{}, pb, nullptr};
+  prefill_act_codes_kernel<<<a.T, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- launch ----
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -869,54 +872,40 @@ static bool make_map_ys(CUtensorMap* m, const void* base, uint64_t rows, int H) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launch as clusters of two CTAs (the GEMMs' CTA pairs).
+// Launch `pairs` CTA pairs (2 * pairs CTAs; the pair of a CTA is its grid
+// index with the low bit cleared).
 template <typename Kern, typename... Args>
-static cudaError_t launch_pairs(Kern kernel, int clusters, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+static cudaError_t launch_pairs(Kern kernel, int pairs, size_t smem, cudaStream_t st, bool pdl, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters);
+  cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(pf::THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Clusters of two that can be resident at once (the persistent grid), per
-// device and GEMM.
+// CTA pairs that can be resident at once (the persistent grid), per device
+// and GEMM.
 template <typename Kern>
 static int resident_pairs(Kern kernel, int device, int mode, size_t smem) {
   static std::mutex mu;
-  static int cache[64][2][2];   // [device][mode - 1] -> {smem, clusters}
+  static int cache[64][2][2];   // [device][mode - 1] -> {smem, pairs}
   std::lock_guard<std::mutex> lk(mu);
   int* c = cache[device & 63][mode - 1];
   if (c[0] == (int)smem && c[1] > 0) return c[1];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 512);
-  cfg.blockDim = dim3(pf::THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, pf::THREADS, smem) != cudaSuccess) {
     cudaGetLastError();
-    n = 0;
+    per_sm = 0;
   }
   c[0] = (int)smem;
-  c[1] = n;
-  return n;
+  c[1] = per_sm * num_sms(device) / 2;
+  return c[1];
 }
 
 template <typename Kern, typename... Args>
@@ -957,7 +946,6 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
-            make_map(&g1.ah, U8, 1, pb.xq, R, a.H, a.H, 128, 64, true) &&
             make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
             make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, pf::KG, false) &&
             make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
@@ -969,8 +957,6 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
        make_map_ys(&g2.o, pb.ys, R, a.H);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.a = g1.o;
-  if (!make_map(&g2.ah, U8, 1, pb.hq, R, a.I, a.I, 128, 64, true))
-    return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.os = g2.o;
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");

@@ -65,7 +65,7 @@ extern "C" {
  * moe_fp8_block_abi_version() differs, so a stale build fails loudly instead
  * of reading the banks with the wrong layout (FreeToken PR #662, PR body: the
  * weight-format ABI probe max_weight_format_id). */
-#define MOE_FP8_BLOCK_ABI_VERSION 3
+#define MOE_FP8_BLOCK_ABI_VERSION 4
 
 /* Element types of moe_tensor.dtype. */
 typedef enum {
@@ -253,6 +253,30 @@ int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, const moe_ten
                                          int64_t w2_scale_stride, moe_tensor* out, void* stream);
 
 /*
+ * moe_fp8_block_forward_act_codes -- moe_fp8_block_forward_ex, plus a copy
+ * of the e4m3 activation codes and fp32 group scales that the forward's own
+ * quantiser produced in this call, for checking them code by code (the
+ * dynamic per-token, per-128-column activation scales of the fp8-moe-gather
+ * page, "Affects": scale = amax / 448, code = e4m3(x / scale) rounded to
+ * nearest even and saturated).
+ *  codes   device uint8 [T, H], row-contiguous, 16-byte aligned
+ *  scales  device fp32 [T, ceil(H/128)], row-contiguous
+ * Prefill path: the copy is taken from the rows the grouped GEMM reads,
+ * those of one routed slot of each token (slot t mod k, else the next valid
+ * one); a token without a valid slot has no such row and its entries are
+ * left untouched.  Decode path: only with decode_act = MOE_DECODE_ACT_E4M3,
+ * where the gate/up kernel quantises the activations itself and also writes
+ * this copy; the W8A16 decode path quantises nothing (MOE_ERR_ARG).
+ * Everything else, including the return codes, is moe_fp8_block_forward_ex.
+ */
+int moe_fp8_block_forward_act_codes(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                    const moe_tensor* topk_weights, const moe_tensor* w13,
+                                    const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                                    const moe_tensor* w2, const moe_tensor* w2_scale,
+                                    int64_t w2_scale_stride, moe_tensor* out, void* stream,
+                                    const moe_options* opt, uint8_t* codes, float* scales);
+
+/*
  * moe_fp8_block_route -- the routing lists of the gathered path, on their
  * own (the same kernel the forward runs).  For S = T*k slots s = t*k + j:
  *  counts   int32 [E]     slots per expert (valid ids only)
@@ -271,8 +295,10 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts,
                         int32_t* n_distinct, void* stream);
 
 /*
- * moe_fp8_block_act_quant -- the dynamic activation quantisation of the
- * prefill path, on its own (the same kernel the forward runs): for each row r
+ * moe_fp8_block_act_quant -- the dynamic activation quantisation rule of the
+ * prefill path as a standalone kernel (the forward itself quantises inside
+ * its own kernels; moe_fp8_block_forward_act_codes returns those codes): for
+ * each row r
  * of x (bf16 [R, K], stride[1] == 1, K a multiple of 128) and each 128-column
  * group c: amax = max |x|, scale = amax / 448 in IEEE fp32,
  * code = e4m3(x / scale) rounded to nearest even and saturated to +-448
