@@ -1,30 +1,40 @@
 """Benchmark of the block-FP8 MoE layer forward on GB300.
 
-One step = one forward at each batch size of the decode workload with small
-fine-grained experts (E=128, H=2048, I=512, top_k=8, T in {1,2,4,8,16}, down
-scales padded to stride 8), on seeded synthetic inputs resident in HBM.  The
-metric is the decode routed-weight HBM bandwidth: bytes of the distinct
+One step = one decode forward at each batch size of three layers, on
+seeded synthetic inputs resident in HBM:
+  small          E=128 H=2048 I=512 top_k=8, T in {1,2,4,8,16}, down scales
+                 padded to stride 8;
+  padded_skewed  E=256 H=2560 I=640 top_k=8, T in {1,8,32}, down scales
+                 padded to stride 6, router logits +2 on 16 hot experts;
+  wide           E=256 H=7168 I=2048 top_k=8, T in {1,4,16,64} (11.3 GB of
+                 e4m3 weights).
+The metric is the decode routed-weight HBM bandwidth: bytes of the distinct
 routed experts' e4m3 weights and valid bf16 block scales, divided by the
-device time of the forwards (CUDA events on the launching stream).
+device time of the forwards (CUDA events on the launching stream).  The
+headline `value` aggregates every forward of up to 16 tokens (the range the
+decode target is stated for); each layer's numbers, per T, are beside it.
 
-No forward finds its weights in L2.  Two ways to ensure it (--l2):
+No forward finds its weights in L2.  Two ways to ensure it (--l2), for the
+small and skewed layers:
   rotate (default): consecutive forwards read different copies of the weight
-      banks, as the layers of a model do (16 copies, 6.4 GB, far larger
-      than L2); nothing else runs between forwards.
+      banks, as the layers of a model do (16 and 8 copies, far larger than
+      L2); nothing else runs between forwards.
   flush: one weight bank; a 256 MiB buffer is written before every forward.
       The written lines sit dirty in L2, so the forward's reads also pay for
       their write-back to HBM.
-The line reports the chosen mode as `value` and the other one beside it.
-Each timed forward is a replay of a CUDA graph captured from the library
-call (one graph per batch size and weight bank), as a serving loop would
-run it; `value_eager` times the same forwards launched eagerly.
+The wide layer keeps one bank: each of its forwards reads more than twice
+the L2 capacity.  For the small layer the line also reports the other L2
+mode, eager launches and the W8A8 decode option.  Each timed forward is a
+replay of a CUDA graph captured from the library call (one graph per batch
+size and weight bank), as a serving loop would run it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--l2 rotate|flush]
 
 --impl reference times the float64 CPU oracle (the only baseline the pages
-allow here) on a bounded sample of the same workload.  Under torchrun
-(N > 1) every rank runs an independent replica (the layer has no exchange
-step on one GPU per token batch); value = bytes of all ranks / max time.
+allow here) on a bounded sample of the small-expert workload.  Under
+torchrun (N > 1) every rank runs an independent replica (the layer has no
+exchange step on one GPU per token batch); value = bytes of all ranks / max
+time.
 """
 from __future__ import annotations
 
@@ -46,11 +56,12 @@ if ROOT not in sys.path:
 
 from block_fp8_mixture_route_gb300 import api, synthetic as syn  # noqa: E402
 
-DECODE_TS = [1, 2, 4, 8, 16]
+DECODE_TS = [1, 2, 4, 8, 16]   # the small-expert workload (oracle sample, end to end)
 SHAPE = syn.DECODE_SMALL
-WORKLOAD = "decode E=128 H=2048 I=512 top_k=8 T={1,2,4,8,16} w2-scale stride 8"
+WORKLOAD = ("decode, batches of up to 16 tokens of three layers: E=128 H=2048 I=512 (T=1,2,4,8,16); "
+            "E=256 H=2560 I=640 skewed (T=1,8); E=256 H=7168 I=2048 (T=1,4,16); top_k=8")
 METRIC = "decode routed-weight HBM GB/s"
-N_LAYERS = 16   # weight-bank copies in --l2 rotate
+DECODE_KERNEL = "chain"   # --decode-kernel: the chained decode kernels or the single persistent one
 
 
 def routed_bytes(shape: syn.MoeShape, ids: torch.Tensor) -> tuple[int, int]:
@@ -243,7 +254,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * ts / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": "n/a (host)"},
+        "config": {"workload": WORKLOAD, "decode_kernel": DECODE_KERNEL, "l2": "n/a (host)"},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -251,24 +262,31 @@ def run_reference(args, world, rank):
 
 
 class Feed:
-    """The inputs of forward number j and what runs before it (--l2)."""
+    """The inputs of forward number j of one decode workload and what runs
+    before it (--l2).  `banks` copies of the weight banks are rotated when
+    one forward's weights could fit in L2; a workload whose every forward
+    reads far more than L2 (the wide layer) keeps a single bank."""
 
-    def __init__(self, probs, mode: str, dev):
-        self.probs, self.mode, self.j = probs, mode, 0
+    def __init__(self, wl, probs, mode: str, dev, banks: int):
+        """mode: "rotate" (`banks` copies of the banks, read in turn), "flush"
+        (one bank, a 256 MiB write before every forward) or "single" (one
+        bank, nothing in between)."""
+        self.wl, self.probs, self.mode, self.j = wl, probs, mode, 0
+        self.nb = banks if mode == "rotate" else 1
         self.banks = None
         if mode == "rotate":
-            p = probs[DECODE_TS[0]]
+            p = probs[wl.ts[0]]
             bank0 = (p["w13"], p["w13_scale"], p["w2"], p["w2_scale"])
-            self.banks = [bank0] + [tuple(t.clone() for t in bank0) for _ in range(N_LAYERS - 1)]
+            self.banks = [bank0] + [tuple(t.clone() for t in bank0) for _ in range(self.nb - 1)]
         props = torch.cuda.get_device_properties(dev)
         self.flush = torch.empty(max(256 << 20, 2 * getattr(props, "L2_cache_size", 128 << 20)),
                                  dtype=torch.uint8, device=dev) if mode == "flush" else None
 
     def n_banks(self) -> int:
-        return N_LAYERS if self.mode == "rotate" else 1
+        return self.nb
 
     def problem(self, T, bank):
-        if self.mode == "flush":
+        if self.banks is None:
             return self.probs[T]
         w = self.banks[bank]
         return dict(self.probs[T], w13=w[0], w13_scale=w[1], w2=w[2], w2_scale=w[3])
@@ -287,12 +305,14 @@ class Feed:
     def describe(self) -> str:
         if self.mode == "flush":
             return "flushed (256 MiB write) before every forward"
-        return f"weights rotated over {N_LAYERS} copies of the banks ({N_LAYERS * bank_bytes() / 1e9:.1f} GB); no flush"
+        if self.mode == "single":
+            return "one weight bank; every forward reads more than twice the L2 capacity"
+        return (f"weights rotated over {self.nb} copies of the banks "
+                f"({self.nb * bank_bytes(self.wl.shape) / 1e9:.1f} GB); no flush")
 
 
-def bank_bytes() -> int:
-    E, H, I = SHAPE.E, SHAPE.H, SHAPE.I
-    return E * 3 * H * I
+def bank_bytes(shape) -> int:
+    return shape.E * 3 * shape.H * shape.I
 
 
 def hold_stream(s, ms: float):
@@ -304,16 +324,17 @@ def hold_stream(s, ms: float):
         torch.cuda._sleep(int(ms * 2.0e6))
 
 
-def capture_forwards(feed, s, outs):
+def capture_forwards(wl, feed, s, outs):
     """One CUDA graph per (T, weight bank) of the library's forward, captured
     on stream s (the library is capture-safe once its workspace is sized):
     replays launch the forward's kernels without host work in between."""
     graphs = {}
-    for T in DECODE_TS:
+    for T in wl.ts:
         for bank in range(feed.n_banks()):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
-                api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode")
+                api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode",
+                                    decode_kernel=DECODE_KERNEL)
             graphs[(T, bank)] = g
     with torch.cuda.stream(s):
         for g in graphs.values():
@@ -322,103 +343,215 @@ def capture_forwards(feed, s, outs):
     return graphs
 
 
-def timed_forwards(feed, s, outs, steps, graphs=None, decode_act=None):
+def timed_forwards(wl, feed, s, outs, steps, graphs=None, decode_act=None):
     """Device time of every forward of `steps` steps: {T: [ms per forward]}.
     With `graphs`, each forward is a replay of its captured graph."""
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in DECODE_TS]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.ts]
           for _ in range(steps)]
-    hold_stream(s, 2.0 + 0.5 * steps * len(DECODE_TS))
+    hold_stream(s, 2.0 + 0.5 * steps * len(wl.ts) * wl.hold_scale)
     with torch.cuda.stream(s):
         for k in range(steps):
-            for i, T in enumerate(DECODE_TS):
+            for i, T in enumerate(wl.ts):
                 bank = feed.next_bank()
                 ev[k][i][0].record(s)
                 if graphs is not None:
                     graphs[(T, bank)].replay()
                 else:
                     api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode",
-                                        decode_act=decode_act)
+                                        decode_act=decode_act, decode_kernel=DECODE_KERNEL)
                 ev[k][i][1].record(s)
     s.synchronize()
-    return {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)] for i, T in enumerate(DECODE_TS)}
+    return {T: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)] for i, T in enumerate(wl.ts)}
+
+
+class Workload:
+    """One decode workload: a layer shape, its token counts and routing."""
+
+    def __init__(self, name, shape, ts, routing, banks, desc, hold_scale=1.0):
+        self.name, self.shape, self.ts, self.routing, self.banks = name, shape, ts, routing, banks
+        self.desc, self.hold_scale = desc, hold_scale
+
+    def problems(self, dev):
+        w13, w13s, w2, w2s = syn.make_weights(self.shape, 0, dev)
+        probs = {}
+        for T in self.ts:
+            ids, w = syn.make_routing(T, self.shape.E, self.shape.k, 0, dev, self.routing, step=T)
+            probs[T] = dict(hidden=syn.make_hidden(T, self.shape.H, 0, dev, step=T), topk_ids=ids, topk_weights=w,
+                            w13=w13, w13_scale=w13s, w2=w2, w2_scale=w2s)
+        return probs
+
+
+# The decode workloads (small fine-grained experts, padded-scale skewed
+# routing, wide experts); the headline aggregates their batches of up to 16
+# tokens, the range the decode target is stated for.
+WORKLOADS = [
+    Workload("small", syn.DECODE_SMALL, [1, 2, 4, 8, 16], "softmax", 16,
+             "E=128 H=2048 I=512 top_k=8 T={1,2,4,8,16}, w2-scale stride 8"),
+    Workload("padded_skewed", syn.PADDED_SKEWED, [1, 8, 32], "hot", 8,
+             "E=256 H=2560 I=640 top_k=8 T={1,8,32}, w2-scale stride 6, +2 logits on 16 hot experts"),
+    Workload("wide", syn.DECODE_WIDE, [1, 4, 16, 64], "softmax", 1,
+             "E=256 H=7168 I=2048 top_k=8 T={1,4,16,64}, 11.3 GB bank", hold_scale=20.0),
+]
+HEADLINE_T_MAX = 16
+
+
+def algorithmic_bytes(shape, T, D) -> int:
+    """Least bytes a decode forward moves: the routed experts' weights and
+    valid block scales, the activations read and the output written."""
+    return D * routed_per_expert(shape) + 2 * T * shape.H * 2
+
+
+def routed_per_expert(shape) -> int:
+    E, H, I = shape.E, shape.H, shape.I
+    return 2 * I * H + H * I + 2 * ((2 * I // 128) * (H // 128)) + 2 * ((H // 128) * (I // 128))
+
+
+def measure_workload(wl, dev, s, steps, warmup, l2="rotate", graphs_on=True, extras=False):
+    """Time one decode workload; returns a dict of per-T results (and, with
+    extras, the other L2 mode, eager launches and the W8A8 option)."""
+    probs = wl.problems(dev)
+    shp = wl.shape
+    api.moe_fp8_block_reserve(max(wl.ts), shp.k, shp.H, shp.I, shp.E, stream=s)
+    mode = "single" if wl.banks == 1 else l2
+    feed = Feed(wl, probs, mode, dev, wl.banks)
+    outs = {T: torch.empty(T, shp.H, dtype=torch.bfloat16, device=dev) for T in wl.ts}
+    info = {T: routed_bytes(shp, probs[T]["topk_ids"]) for T in wl.ts}
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            for T in wl.ts:
+                api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode",
+                                    decode_kernel=DECODE_KERNEL)
+    s.synchronize()
+    launches = {}
+    for T in wl.ts:
+        with torch.cuda.stream(s):
+            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+        launches[T] = api.moe_fp8_block_last_launches()
+    s.synchronize()
+    graphs = capture_forwards(wl, feed, s, outs) if graphs_on else None
+    per_T = timed_forwards(wl, feed, s, outs, steps, graphs)
+    kern = kernel_durations(wl, feed, s, max(3, steps // 2))
+    res = {"workload": wl.desc, "l2": feed.describe(), "per_T": per_T, "info": info, "kern": kern,
+           "launches": launches}
+    if extras:
+        alt = Feed(wl, probs, "flush" if mode == "rotate" else "rotate", dev, wl.banks)
+        alt_graphs = capture_forwards(wl, alt, s, outs) if graphs_on else None
+        alt_T = timed_forwards(wl, alt, s, outs, steps, alt_graphs)
+        res["alt"] = (alt.describe(), alt_T)
+        res["eager"] = timed_forwards(wl, feed, s, outs, steps)
+        with torch.cuda.stream(s):
+            for T in wl.ts:
+                api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_act="e4m3",
+                                    decode_kernel=DECODE_KERNEL)
+        res["w8a8"] = timed_forwards(wl, feed, s, outs, steps, decode_act="e4m3")
+        res["feed"] = feed
+    else:
+        del feed, probs, graphs
+        torch.cuda.empty_cache()
+    return res
+
+
+def kernel_durations(wl, feed, s, reps):
+    """Median device time of each kernel of a decode forward per T, from CUDA
+    events the library records around its kernels (stage-timing mode:
+    moe_fp8_block_set_stage_events).  Returns {T: [ms per kernel]}."""
+    import ctypes
+    from block_fp8_mixture_route_gb300 import _lib
+    lib = _lib.load()
+    res = {}
+    for T in wl.ts:
+        with torch.cuda.stream(s):
+            api.forward_problem(feed.next(T), stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+        n = api.moe_fp8_block_last_launches()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        for e in evs:          # torch creates the event handle on first record
+            e.record(s)
+        s.synchronize()
+        arr = (ctypes.c_void_p * (n + 1))(*[e.cuda_event for e in evs])
+        times = []
+        for _ in range(reps):
+            hold_stream(s, 1.0 * wl.hold_scale)
+            with torch.cuda.stream(s):
+                prob = feed.next(T)
+                _lib.check(lib.moe_fp8_block_set_stage_events(arr, n + 1), "set_stage_events")
+                api.forward_problem(prob, stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+            s.synchronize()
+            times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(n)])
+        res[T] = [statistics.median(t[i] for t in times) for i in range(n)]
+    return res
 
 
 # ------------------------------------------------------------------ ours
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    probs = make_problems(dev)
     s = torch.cuda.Stream(device=dev)
-    api.moe_fp8_block_reserve(max(DECODE_TS), SHAPE.k, SHAPE.H, SHAPE.I, SHAPE.E, stream=s)
-    feed = Feed(probs, args.l2, dev)
-    alt = Feed(probs, "flush" if args.l2 == "rotate" else "rotate", dev)
-    outs = {T: torch.empty(T, SHAPE.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
-    info = {T: routed_bytes(SHAPE, probs[T]["topk_ids"]) for T in DECODE_TS}
-    step_bytes = sum(b for _, b in info.values())
-    step_tokens = sum(DECODE_TS)
-
+    hbm, _, src = peaks()
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    # warm-up
-    with torch.cuda.stream(s):
-        for _ in range(args.warmup):
-            for T in DECODE_TS:
-                api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode")
-    s.synchronize()
-    launches_per_step = 0
-    for T in DECODE_TS:
-        with torch.cuda.stream(s):
-            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode")
-        launches_per_step += api.moe_fp8_block_last_launches()
-    s.synchronize()
-
-    graphs = capture_forwards(feed, s, outs) if not args.no_graph else None
-    alt_graphs = capture_forwards(alt, s, outs) if not args.no_graph else None
-
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    per_T = timed_forwards(feed, s, outs, args.steps, graphs)
+    results = {}
+    for wl in WORKLOADS:
+        results[wl.name] = measure_workload(wl, dev, s, args.steps, args.warmup, l2=args.l2,
+                                            graphs_on=not args.no_graph, extras=(wl.name == "small"))
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     ck = clocks.stop()
-    dev_ms = sum(sum(v) for v in per_T.values())
+
+    # headline: all decode forwards of up to 16 tokens
+    step_bytes = step_tokens = 0
+    dev_ms = 0.0
+    kern_bytes, kern_ms = 0, 0.0
+    gpu_launches = 0
+    per_wl = {}
+    for wl in WORKLOADS:
+        r = results[wl.name]
+        rows = {}
+        for T in wl.ts:
+            D, nbytes = r["info"][T]
+            med = statistics.median(r["per_T"][T])
+            kms = sum(r["kern"][T])
+            rows[str(T)] = {"distinct_experts": D, "routed_MB": nbytes / 1e6, "us": 1e3 * med,
+                            "GB_s": nbytes / (med / 1e3) / 1e9, "frac_of_hbm_peak": nbytes / (med / 1e3) / 1e9 / hbm,
+                            "kernels_us": [round(1e3 * x, 2) for x in r["kern"][T]],
+                            "launches": r["launches"][T]}
+            if T <= HEADLINE_T_MAX:
+                step_bytes += nbytes
+                step_tokens += T
+                dev_ms += sum(r["per_T"][T])
+                kern_bytes += algorithmic_bytes(wl.shape, T, D)
+                kern_ms += kms
+                gpu_launches += r["launches"][T] * args.steps
+        head = [T for T in wl.ts if T <= HEADLINE_T_MAX]
+        wb = sum(r["info"][T][1] for T in head)
+        wms = sum(statistics.median(r["per_T"][T]) for T in head)
+        per_wl[wl.name] = {"workload": wl.desc, "l2": r["l2"], "GB_s_T_le_16": wb / (wms / 1e3) / 1e9,
+                           "frac_of_hbm_peak_T_le_16": wb / (wms / 1e3) / 1e9 / hbm, "per_T": rows}
     value, tok_s, dev_ms_max = aggregate(step_bytes, step_tokens, args.steps, dev_ms, world)
-    # the same measurement with the other way of keeping weights out of L2
-    with torch.cuda.stream(s):
-        for T in DECODE_TS:
-            api.forward_problem(alt.next(T), out=outs[T], stream=s, force_path="decode")
-    alt_T = timed_forwards(alt, s, outs, args.steps, alt_graphs)
-    alt_value = step_bytes * args.steps / (sum(sum(v) for v in alt_T.values()) / 1e3) / 1e9
-    # and with eager launches instead of graph replays
-    eager_T = timed_forwards(feed, s, outs, args.steps)
-    eager_value = step_bytes * args.steps / (sum(sum(v) for v in eager_T.values()) / 1e3) / 1e9
-    # the decode path's W8A8 mode (activations quantised per token per 128
-    # columns), eager launches
-    with torch.cuda.stream(s):
-        for T in DECODE_TS:
-            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_act="e4m3")
-    w8a8_T = timed_forwards(feed, s, outs, args.steps, decode_act="e4m3")
-    w8a8_value = step_bytes * args.steps / (sum(sum(v) for v in w8a8_T.values()) / 1e3) / 1e9
+    kern_achieved = kern_bytes / (kern_ms / 1e3) / 1e9
 
-    # dominant kernel (decode GEMM1) timed with CUDA events between the stages
-    st_ms = stage_durations(feed, s, args.steps)
-    g1_ms = {T: st_ms[T][1] for T in DECODE_TS}
-    g1_bytes = {T: info[T][0] * (2 * SHAPE.I * SHAPE.H + 2 * (2 * SHAPE.I // 128) * (SHAPE.H // 128))
-                + T * SHAPE.H * 2 + T * SHAPE.k * SHAPE.I * 4 for T in DECODE_TS}
-    g1_achieved = sum(g1_bytes.values()) / (sum(g1_ms.values()) / 1e3) / 1e9
-    hbm, _, src = peaks()
+    small = results["small"]
+    sb = sum(small["info"][T][1] for T in WORKLOADS[0].ts)
+    alt_desc, alt_T = small["alt"]
+    alt_value = sb * args.steps / (sum(sum(v) for v in alt_T.values()) / 1e3) / 1e9
+    eager_value = sb * args.steps / (sum(sum(v) for v in small["eager"].values()) / 1e3) / 1e9
+    w8a8_value = sb * args.steps / (sum(sum(v) for v in small["w8a8"].values()) / 1e3) / 1e9
 
-    # end to end through the host-buffer entry point (pinned host inputs/outputs)
-    e2e_v, h2d, d2h = e2e_hostio(feed, s, args.steps, args.warmup)
-    prefill = prefill_leg(dev, s, max(5, args.steps)) if not args.no_prefill else None
+    # end to end through the host-buffer entry point (pinned host inputs/outputs), small experts
+    e2e_v, h2d, d2h = e2e_hostio(small["feed"], s, args.steps, args.warmup)
+    small.pop("feed")
+    torch.cuda.empty_cache()
+    prefill = prefill_leg(dev, s, max(5, args.steps)) if not args.no_prefill and world == 1 else None
 
     if rank != 0:
         return
     cpu = None
     if world == 1:
+        probs = make_problems(dev)
         b, secs, desc = oracle_sample(probs)
         cpu = {"value": b / secs / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
                "sample": desc}
@@ -426,65 +559,38 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xbf16->f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": feed.describe(),
-                   "launch": "CUDA graph replay per forward" if graphs is not None else "eager",
+        "config": {"workload": WORKLOAD, "decode_kernel": DECODE_KERNEL,
+                   "l2": {n: v["l2"] for n, v in per_wl.items()},
+                   "launch": "CUDA graph replay per forward" if not args.no_graph else "eager",
                    "path": "decode (forced)", "replicas": world},
         "frac_of_hbm_peak": value / hbm, "peak_source": src,
-        "value_other_l2": {"l2": alt.describe(), "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
-        "value_eager": {"launch": "eager (no CUDA graph)", "value": eager_value, "frac_of_hbm_peak": eager_value / hbm},
-        "value_w8a8": {"decode_act": "e4m3 (W8A8), eager", "value": w8a8_value, "frac_of_hbm_peak": w8a8_value / hbm,
-                       "us": {str(T): 1e3 * statistics.median(w8a8_T[T]) for T in DECODE_TS}},
         "tok_per_s": tok_s,
-        "per_T": {str(T): {"distinct_experts": info[T][0], "routed_MB": info[T][1] / 1e6,
-                           "us": 1e3 * statistics.median(per_T[T]),
-                           "GB_s": info[T][1] / (statistics.median(per_T[T]) / 1e3) / 1e9}
-                  for T in DECODE_TS},
-        "stage_us": {str(T): {n: round(1e3 * v, 2) for n, v in zip(("prep", "gemm1", "gemm2", "combine"), st_ms[T])}
-                     for T in DECODE_TS},
-        "roofline": {"kernel": "decode_gemm1", "bound": "hbm", "achieved": g1_achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": g1_achieved / hbm,
-                     "traffic": profile_traffic("decode_gemm1_kernel", "decode_small_T16"),
-                     "traffic_launch": "T=16 launch (ncu capture); achieved aggregates T=1..16",
-                     "algorithmic_bytes_T16": g1_bytes[16],
-                     "achieved_T16": g1_bytes[16] / (g1_ms[16] / 1e3) / 1e9,
+        "workloads": per_wl,
+        "value_small_other_l2": {"l2": alt_desc, "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
+        "value_small_eager": {"launch": "eager (no CUDA graph)", "value": eager_value,
+                              "frac_of_hbm_peak": eager_value / hbm},
+        "value_small_w8a8": {"decode_act": "e4m3 (W8A8), eager", "value": w8a8_value,
+                             "frac_of_hbm_peak": w8a8_value / hbm,
+                             "us": {str(T): 1e3 * statistics.median(small["w8a8"][T]) for T in WORKLOADS[0].ts}},
+        "roofline": {"kernel": "decode forward (all its kernels)" if DECODE_KERNEL == "chain" else "decode_fused",
+                     "bound": "hbm", "achieved": kern_achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": kern_achieved / hbm,
+                     "traffic": profile_traffic("decode_gemm1_kernel" if DECODE_KERNEL == "chain"
+                                                else "decode_fused_kernel", "decode_small_T16"),
+                     "algorithmic_bytes": "per forward: routed experts' e4m3 weights + valid bf16 scales + "
+                                          "activations read (2TH) + output written (2TH), over the summed device "
+                                          "time of the forward's kernels; summed over every headline forward",
                      "peak_source": f"{src} hbm_gbs (copy, burst)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "call": "moe_fp8_block_forward_hostio through the C ABI; page-locked host inputs read and the "
-                        "output written in place by the kernels"},
+                "call": "moe_fp8_block_forward_hostio through the C ABI on the small-expert workload; page-locked "
+                        "host inputs read and the output written in place by the kernels"},
         "prefill": prefill,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": gpu_launches,
         "clocks": ck,
         "wall_s": wall,
     }
     print(json.dumps(line), flush=True)
-
-
-def stage_durations(feed, s, steps):
-    """Median device time of each kernel of the decode path per T, from CUDA
-    events the library records between its kernels (stage-timing mode:
-    moe_fp8_block_set_stage_events).  Returns {T: [prep, gemm1, gemm2, combine]} in ms."""
-    import ctypes
-    from block_fp8_mixture_route_gb300 import _lib
-    lib = _lib.load()
-    res = {}
-    for T in DECODE_TS:
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        for e in evs:          # torch creates the event handle on first record
-            e.record(s)
-        s.synchronize()
-        arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
-        times = []
-        for _ in range(max(steps, 3)):
-            hold_stream(s, 1.0)
-            with torch.cuda.stream(s):
-                prob = feed.next(T)
-                _lib.check(lib.moe_fp8_block_set_stage_events(arr, 5), "set_stage_events")
-                api.forward_problem(prob, stream=s, force_path="decode")
-            s.synchronize()
-            times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
-        res[T] = [statistics.median(t[i] for t in times) for i in range(4)]
-    return res
 
 
 def e2e_hostio(feed, s, steps, warmup):
@@ -502,7 +608,7 @@ def e2e_hostio(feed, s, steps, warmup):
                 torch.empty(T, SHAPE.H, dtype=torch.bfloat16).pin_memory()) for T in DECODE_TS}
     hdesc = {T: [api.desc(x) for x in host[T]] for T in DECODE_TS}
     wdesc = {}
-    opt = api._options(None, "decode")
+    opt = api._options(None, "decode", decode_kernel=DECODE_KERNEL)
     sp = ctypes.c_void_p(s.cuda_stream)
     total_b, total_s = 0, 0.0
     h2d = sum(T * SHAPE.H * 2 + T * SHAPE.k * 8 for T in DECODE_TS)
@@ -696,9 +802,13 @@ def main():
                     help="how forwards are kept from finding their weights in L2 (see the module docstring)")
     ap.add_argument("--gate-sweep", choices=tuple(SWEEPS), default=None,
                     help="time decode against prefill for r = T*k/E up to 1.0 on one layer (one JSON object)")
+    ap.add_argument("--decode-kernel", choices=("chain", "fused"), default="chain",
+                    help="decode kernels: four chained launches (default) or one persistent launch")
     ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
                     help="only run 3 forwards of one case (for ncu captures); prints no bench line")
     args = ap.parse_args()
+    global DECODE_KERNEL
+    DECODE_KERNEL = args.decode_kernel
     if args.profile_case:
         profile_case(args.profile_case)
         return

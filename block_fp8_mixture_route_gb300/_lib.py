@@ -51,7 +51,10 @@ class MoeOptions(ctypes.Structure):
         ("gate_ratio", ctypes.c_float),
         ("force_path", ctypes.c_int32),
         ("decode_act", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("decode_kernel", ctypes.c_int32),
+        ("debug_wait_timeout_us", ctypes.c_int32),
+        ("debug_drop_stage", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 

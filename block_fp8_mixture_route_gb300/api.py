@@ -46,10 +46,16 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
-def _options(gate_ratio, force_path, decode_act=None) -> Optional[MoeOptions]:
-    if gate_ratio is None and force_path is None and decode_act is None:
+def _options(gate_ratio, force_path, decode_act=None, decode_kernel=None, debug_wait_timeout_us=0,
+             debug_drop_stage=0) -> Optional[MoeOptions]:
+    if (gate_ratio is None and force_path is None and decode_act is None and decode_kernel is None
+            and not debug_wait_timeout_us and not debug_drop_stage):
         return None
     o = MoeOptions()
+    dk = {None: 0, "chain": 0, "fused": 1}
+    o.decode_kernel = dk[decode_kernel] if not isinstance(decode_kernel, int) else decode_kernel
+    o.debug_wait_timeout_us = int(debug_wait_timeout_us)
+    o.debug_drop_stage = int(debug_drop_stage)
     o.gate_ratio = float(gate_ratio) if gate_ratio is not None else 0.0
     fp = {None: 0, "auto": 0, "decode": 1, "prefill": 2}
     o.force_path = fp[force_path] if not isinstance(force_path, int) else force_path
@@ -60,7 +66,8 @@ def _options(gate_ratio, force_path, decode_act=None) -> Optional[MoeOptions]:
 
 def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                           w2_scale_stride, out=None, stream=None, gate_ratio=None, force_path=None,
-                          decode_act=None, w13_bias=None, w2_bias=None):
+                          decode_act=None, w13_bias=None, w2_bias=None, decode_kernel=None,
+                          debug_wait_timeout_us=0, debug_drop_stage=0):
     """Layer forward on device tensors; returns `out` (bf16 [T, H]).
     decode_act: "bf16" (W8A16, default) or "e4m3" (W8A8) for the decode path.
     w13_bias (fp32 [E, 2I], [gate | up]) and w2_bias (fp32 [E, H]): optional
@@ -68,7 +75,8 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
     if w13_bias is not None or w2_bias is not None:
         return moe_fp8_block_forward_bias(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
                                           w2_scale, w2_scale_stride, w13_bias, w2_bias, out=out, stream=stream,
-                                          gate_ratio=gate_ratio, force_path=force_path, decode_act=decode_act)
+                                          gate_ratio=gate_ratio, force_path=force_path, decode_act=decode_act,
+                                          decode_kernel=decode_kernel)
     lib = _lib.load()
     if out is None:
         out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
@@ -76,7 +84,7 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
     a2 = [desc(w2), desc(w2_scale)]
     o = desc(out)
     P = ctypes.byref
-    opt = _options(gate_ratio, force_path, decode_act)
+    opt = _options(gate_ratio, force_path, decode_act, decode_kernel, debug_wait_timeout_us, debug_drop_stage)
     if opt is None:
         rc = lib.moe_fp8_block_forward(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                        int(w2_scale_stride), P(o), _stream(stream))
@@ -89,7 +97,7 @@ def moe_fp8_block_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_sc
 
 def moe_fp8_block_forward_bias(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                                w2_scale_stride, w13_bias=None, w2_bias=None, out=None, stream=None,
-                               gate_ratio=None, force_path=None, decode_act=None):
+                               gate_ratio=None, force_path=None, decode_act=None, decode_kernel=None):
     """Layer forward with optional MLP biases (either may be None)."""
     lib = _lib.load()
     if out is None:
@@ -100,7 +108,7 @@ def moe_fp8_block_forward_bias(hidden, topk_ids, topk_weights, w13, w13_scale, w
     b2 = desc(w2_bias) if w2_bias is not None else None
     o = desc(out)
     P = ctypes.byref
-    opt = _options(gate_ratio, force_path, decode_act)
+    opt = _options(gate_ratio, force_path, decode_act, decode_kernel)
     rc = lib.moe_fp8_block_forward_bias(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                         int(w2_scale_stride), P(b13) if b13 is not None else None,
                                         P(b2) if b2 is not None else None, P(o), _stream(stream),
@@ -146,7 +154,7 @@ def moe_fp8_block_forward_decode_noalloc(hidden, topk_ids, topk_weights, w13, w1
 
 def moe_fp8_block_forward_act_codes(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
                                     w2_scale, w2_scale_stride, out=None, stream=None, gate_ratio=None,
-                                    force_path=None, decode_act=None):
+                                    force_path=None, decode_act=None, decode_kernel=None):
     """Layer forward that also returns the activation codes and group scales
     its own quantiser produced: (out, codes uint8 [T, H], scales fp32
     [T, ceil(H/128)])."""
@@ -160,7 +168,7 @@ def moe_fp8_block_forward_act_codes(hidden, topk_ids, topk_weights, w13, w13_sca
     a2 = [desc(w2), desc(w2_scale)]
     o = desc(out)
     P = ctypes.byref
-    opt = _options(gate_ratio, force_path, decode_act) or MoeOptions()
+    opt = _options(gate_ratio, force_path, decode_act, decode_kernel) or MoeOptions()
     rc = lib.moe_fp8_block_forward_act_codes(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
                                              int(w2_scale_stride), P(o), _stream(stream), P(opt),
                                              codes.data_ptr(), scales.data_ptr())

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_fp8_block.so")
-SOURCES = ["host.cu", "route.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["host.cu", "route.cu", "decode.cu", "decode_fused.cu", "prefill.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

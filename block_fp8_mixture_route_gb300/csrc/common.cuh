@@ -18,6 +18,12 @@ namespace moe {
 // winds down instead of spinning forever.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
 
+// The limit the waits of this translation unit's kernels use: kWaitTimeoutNs
+// unless a caller shortened it for one call (moe_options.debug_wait_timeout_us,
+// a failure-detection test aid).  Read only once a wait has already polled
+// for a while.
+static __device__ uint64_t g_wait_limit_ns = kWaitTimeoutNs;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -70,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if ((i & 4095u) == 0) {
       const uint64_t t = globaltimer_ns();
       if (t0 == 0) t0 = t;
-      else if (t - t0 > kWaitTimeoutNs) return false;
+      else if (t - t0 > *(volatile uint64_t*)&g_wait_limit_ns) return false;
     }
   }
 }
@@ -126,6 +132,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
   __half2 h = *reinterpret_cast<__half2*>(&v);
   return __half22float2(h);
+}
+
+// Bits of the lanes below this one in the warp.
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
 // ----------------------------------------------------------- status word --

@@ -37,6 +37,7 @@
 // copy), so every weight copy here is a block of whole rows of 8-32 KiB.
 #include "common.cuh"
 #include "kernels.h"
+#include "decode_mma.cuh"
 #include "route_dev.cuh"
 
 #include <algorithm>
@@ -76,15 +77,6 @@ constexpr int kSmemLimit = 232448;
 // early also delay the activation (x or h) copy behind them, which the first
 // unit needs as much as its weights: only the first two go out early.
 constexpr int kPreIssue = 2;
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
-
-// Two fp32 values -> two e4m3 codes (lo -> low byte), RNE, saturating.
-__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 // ------------------------------------------------------------- prep ----
 // ACT8: W8A8 activations (per-group e4m3 codes and scales); W8A16 otherwise.
@@ -188,39 +180,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
   if (threadIdx.x == 0) p.db.xexp[t] = s;
 }
 
-// ----------------------------------------------------- shared helpers ----
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint4 lds128(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_u32(p)));
-  return v;
-}
-
-__device__ __forceinline__ float4 lds_f4(const void* p) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(smem_u32(p)));
-  return v;
-}
-
 __device__ __forceinline__ int4 ld_meta(const DecodeArgs& p, int d) { return __ldg(p.rb.meta + d); }
-
-// Bounded wait by lane 0 of a warp; the verdict is returned on all lanes.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
-  int ok = 1;
-  if (lane == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 
 // Shared-memory layout common to both streaming kernels.
 struct Smem {
@@ -301,66 +261,6 @@ __device__ __forceinline__ bool walk_next_segment(const DecodeArgs& p, Walk& w, 
   return true;
 }
 
-// The routed experts as a bitmap in shared memory (bit e set when some slot
-// routes to expert e, 0 <= e < E), built by one warp from the ids alone: the
-// same experts, in the same ascending order, as the routing lists, so a
-// kernel can know its first experts before the routing lists exist.  Lane l
-// keeps words 4l .. 4l+3 (E <= 4096) and the exclusive / inclusive counts of
-// set bits before and through them.  Returns the number of routed experts.
-struct ExpertBits {
-  uint32_t w[4];
-  int excl, incl;
-};
-
-__device__ __forceinline__ int expert_bits(const int32_t* __restrict__ ids, int S, int E, uint32_t* bits, int lane,
-                                           ExpertBits& eb) {
-  const int nwords = (E + 31) >> 5;
-  for (int i = lane; i < 128; i += 32) bits[i] = 0;
-  __syncwarp();
-  for (int s = lane; s < S; s += 32) {
-    const int id = __ldg(ids + s);
-    if (id >= 0 && id < E) atomicOr(&bits[id >> 5], 1u << (id & 31));
-  }
-  __syncwarp();
-  int cnt = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int wi = lane * 4 + j;
-    eb.w[j] = wi < nwords ? bits[wi] : 0u;
-    cnt += __popc(eb.w[j]);
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  eb.excl = incl - cnt;
-  eb.incl = incl;
-  return __shfl_sync(0xffffffffu, incl, 31);
-}
-
-// The d-th routed expert (0-based, ascending), on all lanes.
-__device__ __forceinline__ int expert_select(const ExpertBits& eb, int d, int lane) {
-  int e = -1;
-  if (eb.excl <= d && d < eb.incl) {
-    int r = d - eb.excl;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = __popc(eb.w[j]);
-      if (e < 0 && r < c) {
-        uint32_t v = eb.w[j];
-        for (int q = 0; q < r; ++q) v &= v - 1;   // drop the r lowest set bits
-        e = (lane * 4 + j) * 32 + __ffs(v) - 1;
-      } else if (e < 0) {
-        r -= c;
-      }
-    }
-  }
-  const uint32_t owner = __ballot_sync(0xffffffffu, e >= 0);
-  return owner ? __shfl_sync(0xffffffffu, e, __ffs(owner) - 1) : -1;
-}
-
 // Rows per unit: halved only while there are fewer units than SMs (the
 // count of routed experts D is only known on the device).  Larger units
 // stream better than more SMs each holding small ones: requiring 6 units per
@@ -400,33 +300,6 @@ __device__ __forceinline__ bool group_reduce(const Smem& S, int gr, int wq, int 
   __syncwarp();
   if (lane == 0) mbar_arrive(re);
   return true;
-}
-
-// Widen one 64-wide K chunk of two weight rows (tile rows g and g+8) into
-// the A fragments of four m16n8k16 MMAs.  Physical element 16c + 4m + v of
-// the chunk (c = lane % 4) plays logical k {2c, 2c+1, 2c+8, 2c+9}[v] of MMA
-// m; the B fragment uses the same map, so the four MMAs together sum over
-// exactly the chunk's 64 elements.
-__device__ __forceinline__ void afrag(const uint4& wa, const uint4& wb, uint32_t (&A)[4][4]) {
-  const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w};
-  const uint32_t wb_[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    e4m3x4_to_f16x4(wa_[m], A[m][0], A[m][2]);
-    e4m3x4_to_f16x4(wb_[m], A[m][1], A[m][3]);
-  }
-}
-
-// One 64-wide K chunk: four MMAs on two independent accumulators (shorter
-// dependency chains).
-__device__ __forceinline__ void chunk_mma(float (&b0)[4], float (&b1)[4], const uint4& wa, const uint4& wb,
-                                          const uint4& x0, const uint4& x1) {
-  uint32_t A[4][4];
-  afrag(wa, wb, A);
-  mma_f16_16816(b0, A[0], x0.x, x0.y);
-  mma_f16_16816(b1, A[1], x0.z, x0.w);
-  mma_f16_16816(b0, A[2], x1.x, x1.y);
-  mma_f16_16816(b1, A[3], x1.z, x1.w);
 }
 
 // GEMM1 unit, K slice of KW blocks per warp (sa[j][kk]: the activation
@@ -541,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
       const long n = min((long)kPreIssue, min(wk.ue, (long)(d0 + 1) * upe) - wk.u);
       if (lane == 0 && e0 >= 0)
         for (long i = 0; i < n; ++i) {
+          if (i == a.dbg_drop_stage - 1) continue;   // failure-detection test: this stage never comes
           const int i0 = (int)((wk.u + i) % upe) * R;
           const uint8_t* gsrc = a.w13 + ((int64_t)e0 * 2 * a.I + i0) * a.H;
           mbar_arrive_expect_tx(&S.full[i], 2 * rowb);
@@ -574,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
           if (m >= pre) {
           if (m >= NS) ok = warp_wait(&S.empty[slot], ((m / NS) - 1) & 1, lane);
           if (!ok) break;
-          if (lane == 0) {
+          if (lane == 0 && m != a.dbg_drop_stage - 1) {   // (the failure-detection test drops one)
             const int i0 = (int)(u % upe) * R;
             const uint8_t* gsrc = a.w13 + ((int64_t)wk.e * 2 * a.I + i0) * a.H;
             mbar_arrive_expect_tx(&S.full[slot], 2 * rowb);
@@ -1273,6 +1147,8 @@ bool decode_supported(int H, int I) {
 
 cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeBufs& db, uint32_t* status,
                           int device, cudaStream_t st, int* launches) {
+  if (a.decode_kernel == MOE_DECODE_KERNEL_FUSED && db.counters && fused_decode_ok(a.T, a.k, a.H, a.I, a.E))
+    return launch_decode_fused(a, db.h, db.ybuf, db.counters, status, device, st, launches);
   DecodeArgs p{a, rb, db, status, {}, {}};
   if (!config_gemm1(a.H, p.c1) || !config_gemm2(a.H, a.I, p.c2)) return cudaErrorNotSupported;
   const int sms = num_sms(device);
@@ -1293,6 +1169,13 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   if ((err = set_max_smem((const void*)gemm1, p.c1.smem))) return err;
   if ((err = set_max_smem((const void*)decode_gemm2_kernel, p.c2.smem)))
     return err;
+  // a shortened wait limit for this call (failure-detection test aid)
+  if (a.dbg_wait_ns) {
+    const uint64_t v = a.dbg_wait_ns;
+    if ((err = note_error(cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st),
+                          "decode wait limit")))
+      return err;
+  }
   // prep: route (CTA 0) + f16 activations (CTAs 1..T)
   const bool timed = stage_mark(st, 0);
   const bool pdl = !timed;
@@ -1313,6 +1196,12 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
     return err;
   stage_mark(st, 4);
   *launches += 4;
+  if (a.dbg_wait_ns) {
+    const uint64_t v = kWaitTimeoutNs;
+    if ((err = note_error(cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st),
+                          "decode wait limit")))
+      return err;
+  }
   return cudaSuccess;
 }
 

@@ -31,10 +31,12 @@ std::map<int, int> g_sms;
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+// bytes of the status word and the fused decode counters at the start of a workspace
+const size_t kCountersEnd = align_up(16) + align_up(4 * (size_t)kFusedCounterWords);
 
 // Byte layout of one workspace.
 struct Layout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta, mtp, mtp2, rcnt;
+  size_t status, fctr, counts, offsets, perm, inv, glist, nd, meta, mtp, mtp2, rcnt;
   size_t xh, xexp, xsd, h, ybuf;                  // decode
   size_t xq, xs, hq, hs, ys, pinv, wsc13, wsc2;  // prefill
   int64_t prows;
@@ -53,6 +55,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
   const int64_t S = T * k;
   const int64_t g = S < E ? S : E;
   L.status = take(16);
+  L.fctr = take(4 * (size_t)kFusedCounterWords);   // same offset in every layout
   L.counts = take(4 * (size_t)E);
   L.offsets = take(4 * (size_t)(E + 1));
   L.perm = take(4 * (size_t)S);
@@ -122,8 +125,9 @@ int get_workspace(cudaStream_t st, size_t bytes, void** out) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
-  // the status word must start cleared
-  if (cudaMemsetAsync(ws.base, 0, 16, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // the status word and the fused decode kernel's counters must start cleared
+  // (they sit at the same offsets in every layout, before any other buffer)
+  if (cudaMemsetAsync(ws.base, 0, kCountersEnd, st) != cudaSuccess) return MOE_ERR_CUDA;
   ws.bytes = want;
   *out = ws.base;
   return MOE_OK;
@@ -282,18 +286,25 @@ int check_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const mo
   return MOE_OK;
 }
 
-int check_options(const moe_options* opt, float* ratio, int* force, int* act8) {
+int check_options(const moe_options* opt, float* ratio, int* force, LayerArgs* a) {
   *ratio = 0.f;   // the measured default gate (choose_path)
   *force = MOE_PATH_NONE;
-  *act8 = 0;
+  a->act8 = 0;
   if (!opt) return MOE_OK;
-  for (int i = 0; i < 5; ++i)
+  for (int i = 0; i < 2; ++i)
     if (opt->reserved[i] != 0) return MOE_ERR_ARG;
   if (opt->force_path < MOE_PATH_NONE || opt->force_path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
   if (opt->decode_act != MOE_DECODE_ACT_BF16 && opt->decode_act != MOE_DECODE_ACT_E4M3) return MOE_ERR_ARG;
+  if (opt->decode_kernel != MOE_DECODE_KERNEL_CHAIN && opt->decode_kernel != MOE_DECODE_KERNEL_FUSED)
+    return MOE_ERR_ARG;
+  if (opt->debug_wait_timeout_us < 0 || opt->debug_wait_timeout_us > 1000000 || opt->debug_drop_stage < 0)
+    return MOE_ERR_ARG;
   if (opt->gate_ratio > 0.f) *ratio = opt->gate_ratio;
   *force = opt->force_path;
-  *act8 = opt->decode_act == MOE_DECODE_ACT_E4M3;
+  a->act8 = opt->decode_act == MOE_DECODE_ACT_E4M3;
+  a->decode_kernel = opt->decode_kernel;
+  a->dbg_wait_ns = 1000ull * (uint64_t)opt->debug_wait_timeout_us;
+  a->dbg_drop_stage = opt->debug_drop_stage;
   return MOE_OK;
 }
 
@@ -334,6 +345,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     db.xs = reinterpret_cast<float*>(w + L.xsd);
     db.h = reinterpret_cast<float*>(w + L.h);
     db.ybuf = reinterpret_cast<float*>(w + L.ybuf);
+    db.counters = reinterpret_cast<uint32_t*>(w + L.fctr);
     err = launch_decode(a, rb, db, status, dev, st, &launches);
   } else {
     PrefillBufs pb;
@@ -418,8 +430,9 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
     c.a.b2_ld = c.a.E > 1 ? w2_bias->stride[0] : c.a.H;
   }
   float ratio;
-  int force, act8;
-  if ((rc = check_options(opt, &ratio, &force, &act8))) return rc;
+  int force;
+  if ((rc = check_options(opt, &ratio, &force, &c.a))) return rc;
+  const int act8 = c.a.act8;
   if (c.T == 0) {
     g_last_launches = 0;
     return MOE_OK;
@@ -428,7 +441,6 @@ int forward_impl(const moe_tensor* hidden, const moe_tensor* topk_ids, const moe
   if ((rc = device_ok(&dev))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LayerArgs a = c.a;
-  a.act8 = act8;
   const int path = choose_path(a, ratio, force);
   if (path == MOE_PATH_DECODE && !decode_supported(a.H, a.I)) return MOE_ERR_SHAPE;
   if (dbg_codes) {
@@ -635,9 +647,11 @@ int moe_fp8_block_route(const moe_tensor* topk_ids, int32_t E, int32_t* counts, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   const size_t scratch_bytes = 8 * (size_t)route_chunks((int)S) * (size_t)E;
-  if ((rc = get_workspace(st, 256 + scratch_bytes, &ws))) return rc;
+  if ((rc = get_workspace(st, kCountersEnd + scratch_bytes, &ws))) return rc;
   RouteBufs rb{counts, offsets, perm, inv, glist, n_distinct, nullptr, nullptr};
-  int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
+  // after the status word and the decode counters, which other calls on this
+  // stream rely on
+  int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kCountersEnd);
   if (note_error(launch_route(static_cast<const int32_t*>(topk_ids->data), (int)S, E, rb,
                               static_cast<uint32_t*>(ws), scratch, st, nullptr),
                  "route") != cudaSuccess) {

@@ -34,6 +34,9 @@ struct LayerArgs {
   // fp32 [T, ceil(H/128)], both row-contiguous
   uint8_t* dbg_codes = nullptr;
   float* dbg_scales = nullptr;
+  int decode_kernel = MOE_DECODE_KERNEL_CHAIN;   // moe_options.decode_kernel
+  uint64_t dbg_wait_ns = 0;    // moe_options.debug_wait_timeout_us (0 = the default limit)
+  int dbg_drop_stage = 0;      // moe_options.debug_drop_stage (0 = none)
 };
 
 // Routing lists produced by the route kernel (device int32 buffers).
@@ -58,6 +61,7 @@ struct DecodeBufs {
   float* xs;          // [T, H/128]: W8A8 activation group scales (decode_act e4m3)
   float* h;           // [S, I] in routed (perm) order
   float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
+  uint32_t* counters = nullptr;   // fused kernel: kFusedCounterWords words, zero between forwards
 };
 
 // Scratch of the prefill path.  Per-row buffers hold `rows` rows in the
@@ -126,8 +130,19 @@ bool decode_supported(int H, int I);
 // Ring stages the decode gate/up stream gets for this shape (0 if unsupported).
 int decode_ring_stages(int H, int I);
 
-// Decode (W8A16) path: prep (route + f16 activations), GEMM1+silu*up,
-// GEMM2, combine.  Adds the number of launches to *launches.
+// The fused decode kernel (one launch per forward) handles up to this many
+// slots, when its shared-memory layout fits; larger slot counts take the
+// chained kernels.  It keeps 2 + min(E, S) counters in global memory.
+constexpr int kFusedMaxSlots = 4096;
+constexpr int kFusedCounterWords = 2 + 4096;
+bool fused_decode_ok(int T, int k, int H, int I, int E);
+size_t fused_counter_words(int S, int E);
+cudaError_t launch_decode_fused(const LayerArgs& a, float* h, float* ybuf, uint32_t* counters, uint32_t* status,
+                                int device, cudaStream_t st, int* launches);
+
+// Decode (W8A16) path: the fused kernel when it applies (and db.counters is
+// set), else prep (route + f16 activations), GEMM1+silu*up, GEMM2, combine.
+// Adds the number of launches to *launches.
 cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeBufs& db, uint32_t* status,
                           int device, cudaStream_t st, int* launches);
 

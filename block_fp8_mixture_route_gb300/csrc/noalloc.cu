@@ -51,7 +51,7 @@ cudaError_t scratch_address(int device, void** out) {
 inline size_t al(size_t x) { return (x + 255) / 256 * 256; }
 
 struct NaLayout {
-  size_t status, counts, offsets, perm, inv, glist, nd, meta, xh, xexp, xs, h, ybuf, total;
+  size_t status, fctr, counts, offsets, perm, inv, glist, nd, meta, xh, xexp, xs, h, ybuf, total;
 };
 
 NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
@@ -65,6 +65,7 @@ NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
   const int64_t S = T * k;
   const int64_t g = S < E ? S : E;
   L.status = take(16);
+  L.fctr = take(4 * (size_t)kFusedCounterWords);   // same offset in every call; kept zero between calls
   L.counts = take(4 * (size_t)E);
   L.offsets = take(4 * (size_t)(E + 1));
   L.perm = take(4 * (size_t)S);
@@ -126,7 +127,7 @@ extern "C" int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, co
                reinterpret_cast<int4*>(w + L.meta),       nullptr};
   DecodeBufs db{reinterpret_cast<uint16_t*>(w + L.xh), reinterpret_cast<int32_t*>(w + L.xexp),
                 reinterpret_cast<float*>(w + L.xs), reinterpret_cast<float*>(w + L.h),
-                reinterpret_cast<float*>(w + L.ybuf)};
+                reinterpret_cast<float*>(w + L.ybuf), reinterpret_cast<uint32_t*>(w + L.fctr)};
   int launches = 0;
   const cudaError_t e = launch_decode(a, rb, db, status, dev, st, &launches);
   if (e != cudaSuccess) {

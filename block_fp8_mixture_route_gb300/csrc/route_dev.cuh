@@ -24,12 +24,6 @@
 
 namespace moe {
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
 // Block-wide exclusive scan of one int per thread; returns the exclusive
 // prefix and writes the total to *total (all threads).
 static __device__ int block_exclusive_scan(int v, int* red /*[33]*/, int* total) {

@@ -120,13 +120,39 @@ enum {
   MOE_DECODE_ACT_E4M3 = 1
 };
 
+/* Kernels of the decode path (moe_options.decode_kernel). */
+enum {
+  /* Four chained launches: routing and activation prep, gate/up projection,
+   * down projection, combine (programmatic dependent launch between them). */
+  MOE_DECODE_KERNEL_CHAIN = 0,
+  /* One persistent launch for the whole forward (routing in every CTA's
+   * shared memory, per-expert hand-off of h between the projections, a
+   * grid-wide count before the combine).  Slot counts it cannot stage in
+   * shared memory fall back to the chain. */
+  MOE_DECODE_KERNEL_FUSED = 1
+};
+
 /* Options of moe_fp8_block_forward_ex.  Zero-initialise, then set fields. */
 typedef struct {
   float gate_ratio;   /* decode while T*k <= E*gate_ratio; <= 0 -> measured rule */
   int32_t force_path; /* MOE_PATH_NONE (gate decides), _DECODE or _PREFILL     */
   int32_t decode_act; /* MOE_DECODE_ACT_BF16 (default) or _E4M3; the prefill  */
                       /* path always quantises activations (and h)             */
-  int32_t reserved[5];/* must be zero                                          */
+  int32_t decode_kernel;         /* MOE_DECODE_KERNEL_CHAIN (default) or _FUSED */
+  /* Failure-detection test aids of the decode path (0 = off).  Every
+   * pipeline wait of the decode kernels gives up after a bounded time (1 s
+   * by default) and raises MOE_STATUS_TIMEOUT; debug_wait_timeout_us
+   * shortens that limit for this call (1..1000000 us).  debug_drop_stage = n
+   * makes the gate/up weight producer of the chained decode kernels skip
+   * its n-th ring stage (1-based): it neither copies the stage nor arrives
+   * on the stage's barrier, so the consumers' wait for it runs out.  The
+   * kernels then wind down (every copy already issued lands first) and the
+   * call's output is invalid; moe_fp8_block_device_status reports
+   * MOE_STATUS_TIMEOUT.  Calls on other streams that overlap a call with a
+   * shortened limit may use it too. */
+  int32_t debug_wait_timeout_us;
+  int32_t debug_drop_stage;
+  int32_t reserved[2];           /* must be zero                                */
 } moe_options;
 
 /*

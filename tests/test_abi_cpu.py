@@ -127,11 +127,16 @@ def test_bad_options(lib, tiny):
     o.force_path = 7
     assert _call(lib, tiny, opt=o) == -9
     o = _lib.MoeOptions()
-    o.reserved[2] = 1
+    o.reserved[1] = 1
     assert _call(lib, tiny, opt=o) == -9
     o = _lib.MoeOptions()
     o.decode_act = 2              # neither MOE_DECODE_ACT_BF16 nor _E4M3
     assert _call(lib, tiny, opt=o) == -9
+    for field, bad in (("decode_kernel", 2), ("decode_kernel", -1), ("debug_wait_timeout_us", -5),
+                       ("debug_wait_timeout_us", 1000001), ("debug_drop_stage", -1)):
+        o = _lib.MoeOptions()
+        setattr(o, field, bad)
+        assert _call(lib, tiny, opt=o) == -9, (field, bad)
 
 
 def test_empty_batch_is_noop(lib):
