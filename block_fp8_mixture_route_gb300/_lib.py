@@ -29,6 +29,7 @@ EXPORTS = [
     "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_bias",
     "moe_fp8_block_forward_hostio",
     "moe_fp8_block_forward_decode_noalloc", "moe_fp8_block_forward_act_codes",
+    "moe_fp8_block_forward_host_experts",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
     "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_last_error_detail", "moe_fp8_block_error_string",
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_forward_bias.argtypes = fwd[:9] + [T, T] + fwd[9:] + [P(MoeOptions)]
         lib.moe_fp8_block_forward_decode_noalloc.argtypes = fwd
         lib.moe_fp8_block_forward_act_codes.argtypes = fwd + [P(MoeOptions), vp, vp]
+        lib.moe_fp8_block_forward_host_experts.argtypes = fwd + [P(MoeOptions)]
         lib.moe_fp8_block_route.argtypes = [T, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.moe_fp8_block_act_quant.argtypes = [T, vp, vp, vp]
         lib.moe_fp8_block_widen_e4m3.argtypes = [vp, i64, vp, vp]

@@ -137,6 +137,25 @@ def moe_fp8_block_forward_hostio(hidden, topk_ids, topk_weights, w13, w13_scale,
     return out
 
 
+def moe_fp8_block_forward_host_experts(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
+                                       w2_scale, w2_scale_stride, out=None, stream=None, decode_act=None):
+    """Decode forward with the expert banks (w13, w13_scale, w2, w2_scale)
+    in page-locked host memory; activations, routing and output on the
+    device.  Returns `out` (bf16 [T, H], device)."""
+    lib = _lib.load()
+    if out is None:
+        out = torch.empty(hidden.shape, dtype=torch.bfloat16, device=hidden.device)
+    args = [desc(hidden), desc(topk_ids), desc(topk_weights), desc(w13), desc(w13_scale)]
+    a2 = [desc(w2), desc(w2_scale)]
+    o = desc(out)
+    P = ctypes.byref
+    opt = _options(None, None, decode_act) or MoeOptions()
+    rc = lib.moe_fp8_block_forward_host_experts(*[P(x) for x in args], int(w13_scale_stride), *[P(x) for x in a2],
+                                                int(w2_scale_stride), P(o), _stream(stream), P(opt))
+    check(rc, "moe_fp8_block_forward_host_experts")
+    return out
+
+
 def moe_fp8_block_forward_decode_noalloc(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2,
                                          w2_scale, w2_scale_stride, out, stream=None):
     """The decode path without any device allocation (scratch in a fixed

@@ -1,52 +1,57 @@
 // decode_fused.cu -- the decode path of the block-FP8 MoE layer as one
-// persistent kernel.
+// persistent kernel (moe_options.decode_kernel = MOE_DECODE_KERNEL_FUSED).
 //
 // At decode sizes the layer is bound by reading the routed experts' e4m3
 // weights (fp8-moe-gather page, Problem), and only the routed experts are
-// read (same page, The fix).  A forward of a few microseconds of HBM traffic
-// cannot afford a chain of kernels (each launch and drain costs several
-// microseconds on this part), so every step runs in one launch of one CTA
-// per SM:
+// read (same page, The fix).  Every step runs in one launch of one CTA per
+// SM:
 //
 //   routing     each CTA builds the routing lists of all slots in its own
 //               shared memory (warp ballots and matches, identical in every
-//               CTA), so no kernel and no global list precede the weights
-//   gate/up     units of (routed expert, RU gate rows + the matching RU up
-//               rows); CTA c takes units [c*U1/G, (c+1)*U1/G).  The
-//               activation rows of a pass (up to SPP1 slots of one expert)
-//               are copied raw (bf16) into shared memory and converted
-//               there to f16 scaled by a power of two per token (W8A16) or
-//               quantised per 128-column group (W8A8).  e4m3 weights are
-//               widened exactly (FreeToken PR #662, PR body), multiplied on
-//               mma.sync m16n8k16 with fp32 accumulation, and each bf16
-//               block scale is applied once per 128-wide K block.  The
-//               eight consumer warps split K; one of them (rotating) sums
-//               the partials and writes h = silu(gate) * up in fp32.
-//   hand-off    when a CTA has finished its gate/up units it adds, per
-//               routed expert, the (unit, pass) count it completed to a
-//               counter in global memory (after a fence: one per warp per
-//               forward); a down-projection pass of that expert waits until
-//               the counter is complete (acquire).  The down-projection
-//               weights do not depend on h, so the ring streams them right
-//               after the gate/up weights and only the h copies wait.
-//   down        units of (routed expert, R2 rows of w2); h enters the MMA
-//               as two f16 terms (hi + lo, about 22 significant bits) after
-//               a per-slot power of two ("the down projection in fp32",
-//               fp8-moe-gather page, The fix); y * topk_weight goes to a
-//               per-slot fp32 buffer.
-//   combine     once every CTA has counted its down units as done (one
+//               CTA); no kernel and no global list precede the weights
+//   gate/up     items of (routed expert, 8 gate rows + the matching 8 up
+//               rows, one K round of up to 16 128-wide K blocks); CTA c
+//               takes the tiles [c*U1/G, (c+1)*U1/G) with all their K
+//               rounds.  The activation rows of a pass (up to SPP1 slots of
+//               one expert) are copied raw (bf16) into shared memory and
+//               converted there to f16 scaled by a power of two per token
+//               (W8A16) or quantised per 128-column group (W8A8).  Each of
+//               the eight consumer warps takes two K blocks of an item: its
+//               e4m3 weights come straight from memory into registers with
+//               16-byte non-allocating vector loads, one item ahead (device
+//               banks: after a bulk prefetch has brought them from HBM into
+//               L2 eight items ahead); they are widened exactly (FreeToken PR #662,
+//               PR body) and multiplied on mma.sync m16n8k16 with fp32
+//               accumulation; each bf16 block scale is applied once per
+//               128-wide K block.
+//   hand-off    when a CTA has finished its gate/up tiles it adds, per routed
+//               expert, the (tile, pass) count it completed to a counter in
+//               global memory (after a fence); a down-projection pass of that
+//               expert waits until the counter is complete (acquire).  The
+//               down-projection weights do not depend on h, so their loads
+//               are issued as soon as a warp's gate/up items are loaded.
+//   down        items of (routed expert, 16 * NT2 rows of w2); h enters the
+//               MMA as two f16 terms (hi + lo, about 22 significant bits)
+//               after a per-slot power of two ("the down projection in
+//               fp32", fp8-moe-gather page, The fix); y * topk_weight goes
+//               to a per-slot fp32 buffer.
+//   combine     once every CTA has counted its down items as done (one
 //               grid-wide counter), each CTA sums a share of the output
 //               rows: out[t] = sum_j ybuf[t*k + j] in slot order (fixed
 //               order, no atomics on the data) -> bf16.
 //
-// Warp roles: warps 0-7 consume ring stages (each unit: every warp takes
-// one K slice or row tile and deposits its partial sums in shared memory),
-// warp 8 streams the weights (bulk copies of whole-row blocks of 16-64 KiB:
-// smaller copies leave one SM's copy engine far below its rate), warp 9
-// routes and prepares the activation rows, warp 10 finishes every unit
-// (sums the partials, applies silu * up or the top-k weight and stores), so
-// that no consumer ever waits for another unit's epilogue.  Every wait is bounded (MOE_STATUS_TIMEOUT); the last
-// CTA to finish resets the global counters for the next forward.
+// Warp roles: warps 0-7 compute (each item: every warp deposits its partial
+// sums in shared memory), warp 8 routes and prepares the activation and h
+// rows, warp 9 finishes every item (sums the partials over the warps and
+// the K rounds, applies silu * up or the top-k weight and stores), so that
+// no compute warp waits for another item's epilogue.  The weights never
+// pass through shared memory and every weight access is an ordinary load,
+// so the same kernel streams banks that live in page-locked host memory
+// (read over the host link; moe_fp8_block_forward_host_experts), where bulk
+// copies and prefetches are not used.  Registers bound how far ahead the
+// loads run (three warps share each SM sub-partition's register file).  Every wait is bounded
+// (MOE_STATUS_TIMEOUT); the last CTA to finish resets the global counters
+// for the next forward.
 #include "decode_mma.cuh"
 
 #include <cstdlib>
@@ -57,29 +62,29 @@ namespace moe {
 
 namespace {
 
-constexpr int kCons = 8;                 // consumer warps
-constexpr int kProd = 8;                 // producer warp index
-constexpr int kAct = 9;                  // activation warp index
-constexpr int kFin = 10;                 // finisher warp index
-constexpr int kFThreads = 32 * 11;
+constexpr int kCons = 8;                 // compute warps
+constexpr int kAct = 8;                  // activation warp index
+constexpr int kFin = 9;                  // finisher warp index
+constexpr int kFThreads = 32 * 10;
+constexpr int kPD = 2;                   // items whose weights a compute warp holds or has in flight
+constexpr int kPF = 8;                   // items ahead whose weights are prefetched into L2
 constexpr int kFSmemLimit = 232448 - 1024;   // dynamic shared memory (static arrays take the rest)
 
 // Global counters of one forward, in the workspace (zero between forwards;
 // the last CTA to finish clears them).
 struct Counters {
   uint32_t* done;     // [1] CTAs finished
-  uint32_t* d2;       // [1] CTAs whose down units are all written
-  uint32_t* c1;       // [DMAX] per routed expert: gate/up (unit, pass) completions
+  uint32_t* d2;       // [1] CTAs whose down items are all written
+  uint32_t* c1;       // [DMAX] per routed expert: gate/up (tile, pass) completions
 };
 
 struct FusedCfg {
-  int RU, RT;          // gate/up row pairs per unit; MMA row tiles (ceil(RU / 8))
-  int R2;              // down-projection rows per unit
-  int NS, SB;          // ring stages, stage bytes
+  int NKR1;            // K rounds of a gate/up tile (16 K blocks each)
+  int NT2, KS2;        // down: 16-row tiles per item, K splits per tile (2 K blocks each)
   int SPP1, SPP2;      // slots per gate/up pass (<= 8), per down pass (<= 4)
   int XP, HP;          // f16 activation row pitch, converted-h row pitch (bytes)
   int S, DMAX;         // slots, min(E, S)
-  int o_ids, o_wts, o_perm, o_meta, o_words, o_wbase, o_cnt, o_red, o_xaux, o_act, o_ring, smem;
+  int o_ids, o_wts, o_perm, o_meta, o_words, o_wbase, o_cnt, o_red, o_xaux, o_act, smem;
 };
 
 struct FusedArgs {
@@ -93,7 +98,6 @@ struct FusedArgs {
 
 // Barrier block at the start of dynamic shared memory.
 struct FBars {
-  uint64_t full[8], empty[8];   // ring
   uint64_t xfull[2], xempty[2]; // activation (x) buffers
   uint64_t hfull[2], hempty[2]; // converted-h buffers
   uint64_t rfull[2], rempty[2]; // cross-warp partial sums
@@ -111,9 +115,24 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
-// Barrier among the eight consumer warps and the finisher (named barrier 1;
-// warps 0-7 and 10).
+// Barrier among the eight compute warps and the finisher (named barrier 1;
+// warps 0-7 and 9).
 __device__ __forceinline__ void finish_sync() { asm volatile("bar.sync 1, 288;" ::: "memory"); }
+
+// Start streaming `bytes` (a multiple of 16, 16-byte aligned) of global
+// memory into L2; no completion, no shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 16 bytes of weights that are read once: not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 // Bounded spin until *p >= target (acquire).  False on timeout.
 __device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target) {
@@ -130,25 +149,15 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target)
   }
 }
 
-// The units of one phase that CTA `cta` of `G` takes: [u0, u1) of D * upe.
+// The range of a phase's work that CTA `cta` of `G` takes: [u0, u1) of
+// D * per (per = tiles or items per routed expert).
 struct Range {
   long u0, u1;
-  int upe;
 };
 
-__device__ __forceinline__ Range cta_range(int D, int upe, int cta, int G) {
-  const long U = (long)D * upe;
-  Range r;
-  r.u0 = U * cta / G;
-  r.u1 = U * (cta + 1) / G;
-  r.upe = upe;
-  return r;
-}
-
-// Rows per unit, halved while fewer units than CTAs (small D), never below lo.
-__device__ __forceinline__ int halve_rows(int R, int lo, int rows_total, int D, int G) {
-  while (R > lo && (long)D * (rows_total / R) < (long)G) R >>= 1;
-  return R;
+__device__ __forceinline__ Range cta_range(int D, int per, int cta, int G) {
+  const long U = (long)D * per;
+  return Range{U * cta / G, U * (cta + 1) / G};
 }
 
 // ------------------------------------------------------------ routing ----
@@ -318,115 +327,119 @@ __device__ void quantize_row_w8a8(uint8_t* row, int H, float* xs, uint8_t* codes
 }
 
 
-// ------------------------------------------------------- warp slices ----
-// A warp's K slice of one 16-row MMA tile, KW 128-wide K blocks from K block
-// kb0: rows g (p0) and g + 8 (p1) of the tile, 16 bytes per lane per 64-wide
-// chunk (the fragment layout of afrag), copied out of the ring stage into
-// registers so that the stage can be released before the MMAs.
-template <int KW>
-__device__ __forceinline__ void load_slice(const uint8_t* p0, const uint8_t* p1, int kb0, bool has,
-                                           uint4 (&wa)[2 * KW], uint4 (&wb)[2 * KW]) {
-#pragma unroll
-  for (int i = 0; i < 2 * KW; ++i) {
-    const int kk = (kb0 + (i >> 1)) * 128 + (i & 1) * 64;
-    wa[i] = has ? lds128(p0 + kk) : make_uint4(0, 0, 0, 0);
-    wb[i] = has ? lds128(p1 + kk) : make_uint4(0, 0, 0, 0);
-  }
-}
+// ------------------------------------------------------------ the walk ----
+// The sequence of items a CTA works through, identical for the compute
+// warps (twice: one walk issues loads kPD items ahead of the other), the
+// finisher and, by segments and passes, the activation warp.  Phase 1: for
+// each routed expert d in the CTA's range of gate/up tiles, each pass of up
+// to SPP1 of the expert's slots, each tile, each K round.  Phase 2: for each
+// expert in the range of down row blocks, each pass of up to SPP2 slots,
+// each row block.  gen counts the passes of the current phase.
+struct Walker {
+  const int4* meta;
+  Range r1, r2;
+  int tpe1, upe2, NKR1, SPP1, SPP2;
+  int phase;   // 1, 2, or 0 when done
+  long u, se, uu;
+  int d, passes, pass, kr, gen;
+  int4 md;
 
-// The slice's MMAs against the activation columns at xrow (f16, 16 bytes per
-// lane per 64-wide chunk, 32 per 128 bytes of K).  Each K block's partial is
-// scaled once: rows g (C[0], C[1]) by slo, rows g + 8 (C[2], C[3]) by shi,
-// times the column scales a0[j] (column 2c) and a1[j] (column 2c + 1); slo
-// and shi of K block kb0 + j come from lane j.
-template <int KW>
-__device__ __forceinline__ void mma_slice(const uint4 (&wa)[2 * KW], const uint4 (&wb)[2 * KW], const uint8_t* xrow,
-                                          int kb0, bool has_x, float slo, float shi, const float (&a0)[8],
-                                          const float (&a1)[8], float (&acc)[4]) {
+  __device__ __forceinline__ void seg_begin() {
+    for (;;) {
+      if (phase == 0) return;
+      const long end = phase == 1 ? r1.u1 : r2.u1;
+      if (u < end) {
+        const int per = phase == 1 ? tpe1 : upe2;
+        d = (int)(u / per);
+        se = min(end, (long)(d + 1) * per);
+        md = meta[d];
+        const int spp = phase == 1 ? SPP1 : SPP2;
+        passes = (md.z + spp - 1) / spp;
+        pass = 0;
+        uu = u;
+        kr = 0;
+        return;
+      }
+      if (phase == 1) {
+        phase = 2;
+        u = r2.u0;
+        gen = 0;
+      } else {
+        phase = 0;
+      }
+    }
+  }
+  __device__ __forceinline__ void init(const int4* m, Range a, Range b, int t1, int u2, int nkr, int s1, int s2) {
+    meta = m;
+    r1 = a;
+    r2 = b;
+    tpe1 = t1;
+    upe2 = u2;
+    NKR1 = nkr;
+    SPP1 = s1;
+    SPP2 = s2;
+    phase = 1;
+    u = r1.u0;
+    gen = 0;
+    seg_begin();
+  }
+  __device__ __forceinline__ void next() {
+    if (phase == 1 && ++kr < NKR1) return;
+    kr = 0;
+    if (++uu < se) return;
+    ++gen;
+    if (++pass < passes) {
+      uu = u;
+      return;
+    }
+    u = se;
+    seg_begin();
+  }
+  __device__ __forceinline__ bool done() const { return phase == 0; }
+  __device__ __forceinline__ int pos0() const { return md.y + pass * (phase == 1 ? SPP1 : SPP2); }
+  __device__ __forceinline__ int nslots() const {
+    const int spp = phase == 1 ? SPP1 : SPP2;
+    return min(spp, md.z - pass * spp);
+  }
+};
+
+// ------------------------------------------------------- warp slices ----
+// The MMAs of one item's two K blocks (nvb of them valid) of one 16-row tile
+// against 8 activation columns at col (f16, 32 bytes per lane per 64-wide
+// chunk): weights wa (rows g) and wb (rows g + 8), 16 bytes per lane per
+// chunk in the fragment order of afrag.  K block j's partial is scaled once:
+// rows g by slo(j) * colscale, rows g + 8 by shi(j) * colscale, where
+// slo(j), shi(j) come from lane j (slo) and lane j (shi).
+__device__ __forceinline__ void mma_item(const uint4 (&wa)[4], const uint4 (&wb)[4], const uint8_t* col, int kb0,
+                                         int nvb, bool has_col, float slo, float shi, const float (&c0)[2],
+                                         const float (&c1)[2], float (&acc)[4]) {
 #pragma unroll
-  for (int j = 0; j < KW; ++j) {
+  for (int j = 0; j < 2; ++j) {
+    if (j >= nvb) break;
     float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       const int kk = (kb0 + j) * 128 + ch * 64;
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-      if (has_x) {
-        x0 = lds128(xrow + 2 * kk);
-        x1 = lds128(xrow + 2 * kk + 16);
+      if (has_col) {
+        x0 = lds128(col + 2 * kk);
+        x1 = lds128(col + 2 * kk + 16);
       }
       chunk_mma(b0, b1, wa[2 * j + ch], wb[2 * j + ch], x0, x1);
     }
     const float sl = __shfl_sync(0xffffffffu, slo, j);
     const float sh = __shfl_sync(0xffffffffu, shi, j);
-    acc[0] = fmaf(sl * a0[j], b0[0] + b1[0], acc[0]);
-    acc[1] = fmaf(sl * a1[j], b0[1] + b1[1], acc[1]);
-    acc[2] = fmaf(sh * a0[j], b0[2] + b1[2], acc[2]);
-    acc[3] = fmaf(sh * a1[j], b0[3] + b1[3], acc[3]);
+    acc[0] = fmaf(sl * c0[j], b0[0] + b1[0], acc[0]);
+    acc[1] = fmaf(sl * c1[j], b0[1] + b1[1], acc[1]);
+    acc[2] = fmaf(sh * c0[j], b0[2] + b1[2], acc[2]);
+    acc[3] = fmaf(sh * c1[j], b0[3] + b1[3], acc[3]);
   }
 }
-
-// The same reading the weights from the ring stage inside the loop (K
-// slices too long for registers); any KW.  Column scales from shared memory
-// (a0[j], a1[j]) or 1 where a0 / a1 is null.
-__device__ __forceinline__ void mma_slice_smem(const uint8_t* p0, const uint8_t* p1, int kb0, int kw, bool has,
-                                               const uint8_t* xrow, bool has_x, float slo, float shi,
-                                               const float* a0, const float* a1, float (&acc)[4]) {
-#pragma unroll 1
-  for (int j = 0; j < kw; ++j) {
-    float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      const int kk = (kb0 + j) * 128 + ch * 64;
-      uint4 wa = make_uint4(0, 0, 0, 0), wb = wa, x0 = wa, x1 = wa;
-      if (has) {
-        wa = lds128(p0 + kk);
-        wb = lds128(p1 + kk);
-      }
-      if (has_x) {
-        x0 = lds128(xrow + 2 * kk);
-        x1 = lds128(xrow + 2 * kk + 16);
-      }
-      chunk_mma(b0, b1, wa, wb, x0, x1);
-    }
-    const float sl = __shfl_sync(0xffffffffu, slo, j);
-    const float sh = __shfl_sync(0xffffffffu, shi, j);
-    const float c0 = a0 ? a0[j] : 1.f, c1 = a1 ? a1[j] : 1.f;
-    acc[0] = fmaf(sl * c0, b0[0] + b1[0], acc[0]);
-    acc[1] = fmaf(sl * c1, b0[1] + b1[1], acc[1]);
-    acc[2] = fmaf(sh * c0, b0[2] + b1[2], acc[2]);
-    acc[3] = fmaf(sh * c1, b0[3] + b1[3], acc[3]);
-  }
-}
-
-// One warp's block scales of a 128-row block (lane j: K block kb0 + j, for
-// j < kw), kept while consecutive units stay in the block, with the next
-// block of the same bank loaded ahead.  Ordinary loads issued while the
-// SM's bulk copies stream take microseconds to return, so a unit must never
-// wait on its own scale load.
-struct ScaleCache {
-  const uint16_t* cur_row = nullptr;   // scale row the current values belong to
-  const uint16_t* nxt_row = nullptr;
-  float cur = 0.f, nxt = 0.f;
-  __device__ __forceinline__ float get(const uint16_t* row, const uint16_t* next_row, int kb0, int kw, int lane) {
-    if (row != cur_row) {
-      if (row == nxt_row) {
-        cur = nxt;
-      } else {
-        cur = lane < kw ? bf16_bits_to_f32(__ldg(row + kb0 + lane)) : 0.f;
-      }
-      cur_row = row;
-      nxt_row = next_row;
-      if (next_row) nxt = lane < kw ? bf16_bits_to_f32(__ldg(next_row + kb0 + lane)) : 0.f;
-    }
-    return cur;
-  }
-};
 
 // ------------------------------------------------------------ the kernel --
 template <bool ACT8, bool BIAS>
 __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid_constant__ FusedArgs p) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  __shared__ uint32_t ebits[128];
   const LayerArgs& a = p.a;
   const FusedCfg& c = p.c;
   FBars& B = *reinterpret_cast<FBars*>(sm);
@@ -438,9 +451,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
   const int4* meta_s = reinterpret_cast<const int4*>(sm + c.o_meta);
   float* red = reinterpret_cast<float*>(sm + c.o_red);
   uint8_t* act = sm + c.o_act;
-  uint8_t* ring = sm + c.o_ring;
-  // per x buffer: token exponents [SPP1] then W8A8 group scales [SPP1][nkb]
   const int nkb1 = a.H >> 7, nkb2 = a.I >> 7;
+  // per x buffer: token exponents [SPP1] then W8A8 group scales [SPP1][nkb1]
   int* xaux = reinterpret_cast<int*>(sm + c.o_xaux);
   auto xexp = [&](int b) { return xaux + b * (c.SPP1 * (1 + nkb1)); };
   auto xsc = [&](int b) { return reinterpret_cast<float*>(xaux + b * (c.SPP1 * (1 + nkb1)) + c.SPP1); };
@@ -450,10 +462,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
   uint8_t* hconv0 = act + c.SPP2 * 4 * a.I;          // phase 2: [2][8][HP]
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < c.NS; ++i) {
-      mbar_init(&B.full[i], 1);
-      mbar_init(&B.empty[i], kCons);
-    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.xfull[i], 1);
       mbar_init(&B.xempty[i], kCons + 1);
@@ -477,90 +485,16 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
     raise_status(p.status, MOE_STATUS_TIMEOUT);
   };
   auto aborted = [&]() { return *(volatile int*)&B.abort != 0; };
+  const int tpe1 = a.I >> 3;                        // gate/up tiles of 8 row pairs per expert
+  const int upe2 = a.H / (16 * c.NT2);              // down row blocks per expert
 
-  if (warp == kProd) {
-    // ============================================== weight producer ====
-    ExpertBits eb;
-    const int D = expert_bits(a.ids, a.S, a.E, ebits, lane, eb);
-    const int RU = halve_rows(c.RU, 1, a.I, D, G);
-    const int R2 = halve_rows(c.R2, 16, a.H, D, G);
-    const Range r1 = cta_range(D, a.I / RU, cta, G), r2 = cta_range(D, a.H / R2, cta, G);
-    const uint64_t pol = l2_policy_evict_first();
-    const int rowb = RU * a.H, tileb = R2 * a.I;
-    int m = 0, pre = 0;
-    bool ok = true;
-    auto issue1 = [&](int slot, int e, int i0) {
-      const uint8_t* g = a.w13 + ((int64_t)e * 2 * a.I + i0) * a.H;
-      mbar_arrive_expect_tx(&B.full[slot], 2 * rowb);
-      bulk_g2s(ring + slot * c.SB, g, rowb, &B.full[slot], pol);
-      bulk_g2s(ring + slot * c.SB + rowb, g + (int64_t)a.I * a.H, rowb, &B.full[slot], pol);
-    };
-    // the first stages (pass 0 of the first expert) go out before the routing lists exist
-    if (r1.u0 < r1.u1) {
-      const int d0 = (int)(r1.u0 / r1.upe);
-      const int e0 = expert_select(eb, d0, lane);
-      const long n = min((long)c.NS, min(r1.u1, (long)(d0 + 1) * r1.upe) - r1.u0);
-      if (lane == 0)
-        for (long i = 0; i < n; ++i) issue1((int)i, e0, (int)((r1.u0 + i) % r1.upe) * RU);
-      pre = (int)n;
-    }
-    __syncwarp();
-    ok = warp_wait(&B.route, 0, lane);
-    // phase 1: gate/up units, pass by pass
-    for (long u = r1.u0; ok && u < r1.u1;) {
-      const int d = (int)(u / r1.upe);
-      const long se = min(r1.u1, (long)(d + 1) * r1.upe);
-      const int4 md = meta_s[d];
-      const int passes = (md.z + c.SPP1 - 1) / c.SPP1;
-      for (int ps = 0; ps < passes && ok; ++ps)
-        for (long uu = u; uu < se && ok; ++uu, ++m) {
-          if (m < pre) continue;
-          const int slot = m % c.NS;
-          if (m >= c.NS) ok = warp_wait(&B.empty[slot], ((m / c.NS) - 1) & 1, lane);
-          if (ok && lane == 0) issue1(slot, md.x, (int)(uu % r1.upe) * RU);
-          __syncwarp();
-          if (aborted()) ok = false;
-        }
-      u = se;
-    }
-    // phase 2: down-projection units (no dependency on h)
-    for (long u = r2.u0; ok && u < r2.u1;) {
-      const int d = (int)(u / r2.upe);
-      const long se = min(r2.u1, (long)(d + 1) * r2.upe);
-      const int4 md = meta_s[d];
-      const int passes = (md.z + c.SPP2 - 1) / c.SPP2;
-      for (int ps = 0; ps < passes && ok; ++ps)
-        for (long uu = u; uu < se && ok; ++uu, ++m) {
-          const int slot = m % c.NS;
-          if (m >= c.NS) ok = warp_wait(&B.empty[slot], ((m / c.NS) - 1) & 1, lane);
-          if (ok && lane == 0) {
-            const int n0 = (int)(uu % r2.upe) * R2;
-            mbar_arrive_expect_tx(&B.full[slot], tileb);
-            bulk_g2s(ring + slot * c.SB, a.w2 + ((int64_t)md.x * a.H + n0) * a.I, tileb, &B.full[slot], pol);
-          }
-          __syncwarp();
-          if (aborted()) ok = false;
-        }
-      u = se;
-    }
-    if (!ok) {
-      if (lane == 0) {
-        fail();
-        // copies already issued must land before the CTA exits
-        const int issued = max(m, pre);
-        for (int mm = max(0, issued - c.NS); mm < issued; ++mm) mbar_wait(&B.full[mm % c.NS], (mm / c.NS) & 1);
-      }
-      __syncwarp();
-    }
-  } else if (warp == kAct) {
+  if (warp == kAct) {
     // ============================================ activation warp ====
     const int D = route_smem(a, c, sm, p.status, lane);
     if (lane == 0) B.D = D;
     __syncwarp();
     if (lane == 0) mbar_arrive(&B.route);
-    const int RU = halve_rows(c.RU, 1, a.I, D, G);
-    const int R2 = halve_rows(c.R2, 16, a.H, D, G);
-    const Range r1 = cta_range(D, a.I / RU, cta, G), r2 = cta_range(D, a.H / R2, cta, G);
+    const Range r1 = cta_range(D, tpe1, cta, G), r2 = cta_range(D, upe2, cta, G);
     const uint64_t pol = l2_policy_evict_last();
     uint32_t aph = 0;   // phase of abar
     bool ok = true;
@@ -586,8 +520,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
     // phase 1: the x rows of every gate/up pass
     int gx = 0;
     for (long u = r1.u0; ok && u < r1.u1;) {
-      const int d = (int)(u / r1.upe);
-      const long se = min(r1.u1, (long)(d + 1) * r1.upe);
+      const int d = (int)(u / tpe1);
+      const long se = min(r1.u1, (long)(d + 1) * tpe1);
       const int4 md = meta_s[d];
       const int passes = (md.z + c.SPP1 - 1) / c.SPP1;
       for (int ps = 0; ps < passes && ok; ++ps, ++gx) {
@@ -617,14 +551,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
     // the h buffers share the x buffers' bytes: wait until both are released
     for (int g = max(0, gx - 2); ok && g < gx; ++g) ok = warp_wait(&B.xempty[g & 1], (g >> 1) & 1, lane);
     // phase 2: the h rows of every down pass, once the expert's h is complete
-    const int upe1 = a.I / RU;
     int gh = 0;
     for (long u = r2.u0; ok && u < r2.u1;) {
-      const int d = (int)(u / r2.upe);
-      const long se = min(r2.u1, (long)(d + 1) * r2.upe);
+      const int d = (int)(u / upe2);
+      const long se = min(r2.u1, (long)(d + 1) * upe2);
       const int4 md = meta_s[d];
       const int passes = (md.z + c.SPP2 - 1) / c.SPP2;
-      const uint32_t target = (uint32_t)(upe1 * ((md.z + c.SPP1 - 1) / c.SPP1));
+      const uint32_t target = (uint32_t)(tpe1 * ((md.z + c.SPP1 - 1) / c.SPP1));
       if (lane == 0) ok = wait_counter(p.ctr.c1 + d, target);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int ps = 0; ps < passes && ok; ++ps, ++gh) {
@@ -670,347 +603,272 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const __grid
     if (!ok && lane == 0) fail();
     __syncwarp();
   } else {
-    // ======================================= consumers 0-7, finisher 10 ====
+    // ================================== compute warps 0-7, finisher 9 ====
     const bool fin = warp == kFin;
     const int w = fin ? 0 : warp;
     const int g = lane >> 2, cq = lane & 3;
     bool ok = warp_wait(&B.route, 0, lane);
     const int D = ok ? *(volatile int*)&B.D : 0;
-    const int RU = halve_rows(c.RU, 1, a.I, D, G);
-    const int RT = (RU + 7) >> 3;
-    const int R2 = halve_rows(c.R2, 16, a.H, D, G);
-    const Range r1 = cta_range(D, a.I / RU, cta, G), r2 = cta_range(D, a.H / R2, cta, G);
-    const int kb0 = w * nkb1 / kCons, kb1 = (w + 1) * nkb1 / kCons, kw = kb1 - kb0;
-    int m = 0;   // ring stage sequence (as the producer's) = reduction step
-    // Reduction steps, double-buffered: every consumer deposits 8 floats per
-    // lane for step m and arrives on rfull[m & 1]; the finisher waits for all
-    // eight, sums, finishes the unit and arrives on rempty[m & 1], which a
-    // deposit two steps later waits for.  (Compile-time indexes only: the
-    // partial sums stay in registers.)
-    auto deposit = [&](const float (&part)[8]) -> bool {
-      const int rb = m & 1;
-      if (m >= 2 && !warp_wait(&B.rempty[rb], ((m >> 1) - 1) & 1, lane)) return false;
-      float4* dst = reinterpret_cast<float4*>(red + ((rb * kCons + w) * 32 + lane) * 8);
-      dst[0] = make_float4(part[0], part[1], part[2], part[3]);
-      dst[1] = make_float4(part[4], part[5], part[6], part[7]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.rfull[rb]);
-      return true;
-    };
-    // the finisher: the partials of step m from warps w0, w0 + stride, ... (nw of them)
-    auto gather = [&](float (&tot)[8], int w0, int nw, int stride) {
-      const int rb = m & 1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) tot[i] = 0.f;
-      for (int j = 0; j < nw; ++j) {
-        const float4* src = reinterpret_cast<const float4*>(red + ((rb * kCons + w0 + j * stride) * 32 + lane) * 8);
-        const float4 x = src[0], y = src[1];
-        tot[0] += x.x; tot[1] += x.y; tot[2] += x.z; tot[3] += x.w;
-        tot[4] += y.x; tot[5] += y.y; tot[6] += y.z; tot[7] += y.w;
+    const Range r1 = cta_range(D, tpe1, cta, G), r2 = cta_range(D, upe2, cta, G);
+    const int NT2 = c.NT2, KS2 = c.KS2;
+    const int tt = w % NT2, ks = w / NT2;   // this warp's down tile and K split
+    // the buffer (x or h) of the pass the walk is in: wait for it when a pass
+    // starts, release the previous one
+    int cur_phase = 0, cur_gen = -1;
+    auto enter_pass = [&](const Walker& W) -> bool {
+      if (W.phase == cur_phase && W.gen == cur_gen) return true;
+      if (cur_phase != 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cur_phase == 1 ? &B.xempty[cur_gen & 1] : &B.hempty[cur_gen & 1]);
       }
+      cur_phase = W.phase;
+      cur_gen = W.gen;
+      if (cur_phase == 0) return true;
+      uint64_t* full = cur_phase == 1 ? &B.xfull[cur_gen & 1] : &B.hfull[cur_gen & 1];
+      return warp_wait(full, (cur_gen >> 1) & 1, lane);
     };
+    int m = 0;   // item sequence = reduction step (double-buffered)
 
-    // ---------------------------------------------- gate/up units
-    ScaleCache scg, scu;   // this warp's gate and up block scales
-    int gx = 0;
-    for (long u = r1.u0; ok && u < r1.u1;) {
-      const int d = (int)(u / r1.upe);
-      const long se = min(r1.u1, (long)(d + 1) * r1.upe);
-      const int4 md = meta_s[d];
-      const int e = md.x;
-      const int passes = (md.z + c.SPP1 - 1) / c.SPP1;
-      for (int ps = 0; ps < passes && ok; ++ps, ++gx) {
-        const int b = gx & 1, nx = min(c.SPP1, md.z - ps * c.SPP1);
-        const int pos0 = md.y + ps * c.SPP1;
-        if (!warp_wait(&B.xfull[b], (gx >> 1) & 1, lane)) {
+    if (!fin) {
+      // ------------------------------------------ compute warps
+      // one item's weights for this warp: two K blocks of rows g and g + 8
+      // of its 16-row tile, loaded straight from global memory, and the
+      // block scales (gate/up: lanes 0, 1 gate, lanes 2, 3 up; down: lanes 0, 1)
+      auto issue = [&](const Walker& L, uint4 (&wa)[4], uint4 (&wb)[4], float& sv) {
+        const int e = L.md.x;
+        if (L.phase == 1) {
+          const int i0 = (int)(L.uu % tpe1) * 8;
+          const int kbA = 16 * L.kr + 2 * w;
+          const uint8_t* pa = a.w13 + ((int64_t)e * 2 * a.I + i0 + g) * a.H + cq * 16;
+          const uint8_t* pb = pa + (int64_t)a.I * a.H;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kb = kbA + (i >> 1);
+            const int kk = kb * 128 + (i & 1) * 64;
+            wa[i] = kb < nkb1 ? ldg_stream(pa + kk) : make_uint4(0, 0, 0, 0);
+            wb[i] = kb < nkb1 ? ldg_stream(pb + kk) : make_uint4(0, 0, 0, 0);
+          }
+          const int kb = kbA + (lane & 1);
+          const int rb = lane < 2 ? (i0 >> 7) : ((a.I + i0) >> 7);
+          sv = lane < 4 && kb < nkb1 ? bf16_bits_to_f32(__ldg(a.w13s + (int64_t)e * a.s13_exp + (int64_t)rb * a.s13_row + kb))
+                                     : 0.f;
+        } else {
+          const int n0 = (int)(L.uu % upe2) * 16 * NT2 + tt * 16;
+          const int kbA = 2 * ks;
+          const uint8_t* pa = a.w2 + ((int64_t)e * a.H + n0 + g) * a.I + cq * 16;
+          const uint8_t* pb = pa + 8 * (int64_t)a.I;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kb = kbA + (i >> 1);
+            const int kk = kb * 128 + (i & 1) * 64;
+            wa[i] = kb < nkb2 ? ldg_stream(pa + kk) : make_uint4(0, 0, 0, 0);
+            wb[i] = kb < nkb2 ? ldg_stream(pb + kk) : make_uint4(0, 0, 0, 0);
+          }
+          const int kb = kbA + lane;
+          sv = lane < 2 && kb < nkb2
+                   ? bf16_bits_to_f32(__ldg(a.w2s + (int64_t)e * a.s2_exp + (int64_t)(n0 >> 7) * a.s2_row + kb))
+                   : 0.f;
+        }
+      };
+      // one item: the MMAs, then this warp's partial sums to the finisher
+      auto compute = [&](const Walker& W, const uint4 (&wa)[4], const uint4 (&wb)[4], float sv) -> bool {
+        if (!enter_pass(W)) return false;
+        const int b = W.gen & 1;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (W.phase == 1) {
+          const int nx = W.nslots();
+          const int kbA = 16 * W.kr + 2 * w;
+          const int nvb = max(0, min(2, nkb1 - kbA));
+          float c0[2] = {1.f, 1.f}, c1[2] = {1.f, 1.f};
+          if (ACT8) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              if (kbA + j >= nkb1) break;
+              if (2 * cq < nx) c0[j] = xsc(b)[(2 * cq) * nkb1 + kbA + j];
+              if (2 * cq + 1 < nx) c1[j] = xsc(b)[(2 * cq + 1) * nkb1 + kbA + j];
+            }
+          }
+          const float shi = __shfl_sync(0xffffffffu, sv, (lane & 1) + 2);
+          mma_item(wa, wb, xbuf0 + b * c.SPP1 * c.XP + g * c.XP + cq * 32, kbA, nvb, g < nx, sv, shi, c0, c1, acc);
+        } else {
+          const int nh = W.nslots();
+          const int kbA = 2 * ks;
+          const int nvb = max(0, min(2, nkb2 - kbA));
+          const float one[2] = {1.f, 1.f};
+          mma_item(wa, wb, hconv0 + b * 8 * c.HP + g * c.HP + cq * 32, kbA, nvb, (g & 3) < nh, sv, sv, one, one,
+                   acc);
+        }
+        const int rb = m & 1;
+        if (m >= 2 && !warp_wait(&B.rempty[rb], ((m >> 1) - 1) & 1, lane)) return false;
+        *reinterpret_cast<float4*>(red + ((rb * kCons + w) * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.rfull[rb]);
+        ++m;
+        return !aborted();
+      };
+      // warp 0, lane 0: bulk prefetches into L2, kPF items ahead of the loads
+      // (a gate/up tile once, at its first K round of its first pass; a down
+      // item's rows at its first pass); not for banks in host memory
+      Walker P;
+      P.init(meta_s, r1, r2, tpe1, upe2, c.NKR1, c.SPP1, c.SPP2);
+      auto prefetch_next = [&]() {
+        if (P.done()) return;
+        if (!a.host_weights && w == 0 && lane == 0 && P.pass == 0) {
+          const int e = P.md.x;
+          if (P.phase == 1 && P.kr == 0) {
+            const int i0 = (int)(P.uu % tpe1) * 8;
+            const uint8_t* pa = a.w13 + ((int64_t)e * 2 * a.I + i0) * a.H;
+            prefetch_l2(pa, (uint32_t)(8 * a.H));
+            prefetch_l2(pa + (int64_t)a.I * a.H, (uint32_t)(8 * a.H));
+          } else if (P.phase == 2) {
+            const int nb = (int)(P.uu % upe2) * 16 * NT2;
+            prefetch_l2(a.w2 + ((int64_t)e * a.H + nb) * a.I, (uint32_t)(16 * NT2 * a.I));
+          }
+        }
+        P.next();
+      };
+      for (int j = 0; j < kPF; ++j) prefetch_next();
+      Walker L, W;
+      L.init(meta_s, r1, r2, tpe1, upe2, c.NKR1, c.SPP1, c.SPP2);
+      W = L;
+      uint4 wa[kPD][4], wb[kPD][4];
+      float sv[kPD];
+#pragma unroll
+      for (int j = 0; j < kPD; ++j) {
+        if (!L.done()) {
+          issue(L, wa[j], wb[j], sv[j]);
+          L.next();
+        }
+      }
+      while (ok && !W.done()) {
+#pragma unroll
+        for (int j = 0; j < kPD; ++j) {
+          if (!ok || W.done()) break;
+          prefetch_next();
+          ok = compute(W, wa[j], wb[j], sv[j]);
+          W.next();
+          if (!L.done()) {
+            issue(L, wa[j], wb[j], sv[j]);
+            L.next();
+          }
+        }
+      }
+      if (ok) enter_pass(W);   // release the last pass's buffer
+    } else {
+      // ------------------------------------------ finisher
+      Walker W;
+      W.init(meta_s, r1, r2, tpe1, upe2, c.NKR1, c.SPP1, c.SPP2);
+      float tacc[4] = {0.f, 0.f, 0.f, 0.f};   // a gate/up tile's sums over its K rounds
+      bool signalled = false;
+      // after the last gate/up tile: this CTA's (tile, pass) counts per routed
+      // expert, once its h rows are visible
+      auto signal_h = [&]() {
+        signalled = true;
+        __threadfence();
+        __syncwarp();
+        if (aborted()) return;
+        const int dlo = (int)(r1.u0 / tpe1), dhi = r1.u1 > r1.u0 ? (int)((r1.u1 - 1) / tpe1) : dlo - 1;
+        for (int d = dlo + lane; d <= dhi; d += 32) {
+          const long ua = max(r1.u0, (long)d * tpe1), ub = min(r1.u1, (long)(d + 1) * tpe1);
+          const int passes = (meta_s[d].z + c.SPP1 - 1) / c.SPP1;
+          atomicAdd(p.ctr.c1 + d, (uint32_t)((ub - ua) * passes));
+        }
+      };
+      while (ok && !W.done()) {
+        if (W.phase == 2 && !signalled) signal_h();
+        if (!enter_pass(W)) {
           ok = false;
           break;
         }
-        if (fin) {
-          // ------------------------------------------ finisher, gate/up
-          int sx[2] = {0, 0};
+        const int b = W.gen & 1;
+        const int rb = m & 1;
+        if (!warp_wait(&B.rfull[rb], (m >> 1) & 1, lane)) {
+          ok = false;
+          break;
+        }
+        const int e = W.md.x;
+        const int pos0 = W.pos0(), ns = W.nslots();
+        if (W.phase == 1) {
+#pragma unroll 4
+          for (int j = 0; j < kCons; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(red + ((rb * kCons + j) * 32 + lane) * 4);
+            tacc[0] += v.x;
+            tacc[1] += v.y;
+            tacc[2] += v.z;
+            tacc[3] += v.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.rempty[rb]);
+          if (W.kr == c.NKR1 - 1) {
+            const int i0 = (int)(W.uu % tpe1) * 8;
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            if (2 * cq + j < nx) sx[j] = xexp(b)[2 * cq + j];
-          for (long uu = u; uu < se; ++uu, ++m) {
-            const int i0 = (int)(uu % r1.upe) * RU;
-            if (!warp_wait(&B.rfull[m & 1], (m >> 1) & 1, lane)) {
-              ok = false;
-              break;
-            }
-            float tot[8];
-            gather(tot, 0, kCons, 1);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.rempty[m & 1]);
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int r = t * 8 + g;
-              if (t >= RT || r >= RU) continue;
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (2 * cq + j >= nx) continue;
-                float gv = ldexpf(tot[4 * t + j], sx[j]);
-                float uv = ldexpf(tot[4 * t + 2 + j], sx[j]);
-                if (BIAS && a.b13) {   // either bias may be absent
-                  const float* br = a.b13 + (int64_t)e * a.b13_ld + i0 + r;
-                  gv += __ldg(br);
-                  uv += __ldg(br + a.I);
-                }
-                p.h[(int64_t)(pos0 + 2 * cq + j) * a.I + i0 + r] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+            for (int j = 0; j < 2; ++j) {
+              if (2 * cq + j >= ns) continue;
+              const int sx = xexp(b)[2 * cq + j];
+              float gv = ldexpf(tacc[j], sx);
+              float uv = ldexpf(tacc[2 + j], sx);
+              if (BIAS && a.b13) {   // either bias may be absent
+                const float* br = a.b13 + (int64_t)e * a.b13_ld + i0 + g;
+                gv += __ldg(br);
+                uv += __ldg(br + a.I);
               }
+              p.h[(int64_t)(pos0 + 2 * cq + j) * a.I + i0 + g] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
-            if (aborted()) {
-              ok = false;
-              break;
-            }
+            tacc[0] = tacc[1] = tacc[2] = tacc[3] = 0.f;
           }
         } else {
-          // ------------------------------------------ consumer, gate/up
-          const uint8_t* xrow = xbuf0 + b * c.SPP1 * c.XP + g * c.XP + cq * 32;
-          const bool has_x = g < nx;
-          // W8A8 activation scales of slots 2cq, 2cq + 1 over this warp's K blocks
-          float sa[2][8];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              sa[j][kk] = (ACT8 && 2 * cq + j < nx && kk < kw) ? xsc(b)[(2 * cq + j) * nkb1 + kb0 + kk] : 1.f;
-          for (long uu = u; uu < se; ++uu, ++m) {
-            const int i0 = (int)(uu % r1.upe) * RU;
-            // this warp's block scales (lane j: K block kb0 + j) of the unit's
-            // gate and up rows; the up rows' 128-row block is I/128 blocks on
-            const int rb = i0 >> 7, nrb = a.I >> 7;
-            const uint16_t* sbase = a.w13s + (int64_t)e * a.s13_exp;
-            const bool more = rb + 1 < nrb && (int)((se - 1) % r1.upe) * RU >= (rb + 1) * 128;
-            const float sgl = scg.get(sbase + (int64_t)rb * a.s13_row,
-                                      more ? sbase + (int64_t)(rb + 1) * a.s13_row : nullptr, kb0, kw, lane);
-            const float sul = scu.get(sbase + (int64_t)(nrb + rb) * a.s13_row,
-                                      more ? sbase + (int64_t)(nrb + rb + 1) * a.s13_row : nullptr, kb0, kw, lane);
-            const int slot = m % c.NS;
-            if (!warp_wait(&B.full[slot], (m / c.NS) & 1, lane)) {
-              ok = false;
-              break;
-            }
-            const uint8_t* st = ring + slot * c.SB;
-            float part[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) part[i] = 0.f;
-            // W8A8 group scales of columns 2cq, 2cq + 1 in shared memory (smem path)
-            const float* xs0 = ACT8 && 2 * cq < nx ? xsc(b) + (2 * cq) * nkb1 + kb0 : nullptr;
-            const float* xs1 = ACT8 && 2 * cq + 1 < nx ? xsc(b) + (2 * cq + 1) * nkb1 + kb0 : nullptr;
-            const uint8_t* ar0 = st + g * a.H + cq * 16;   // tile 0: gate row g, up row g
-            const uint8_t* ar1 = ar0 + 8 * a.H;             // tile 1: gate row 8 + g
-            const bool hw0 = g < RU, hw1 = 8 + g < RU;
-            bool released = true;
-            if (RT == 1 && kw == 2) {
-              uint4 wa[4], wb[4];
-              load_slice<2>(ar0, ar0 + RU * a.H, kb0, hw0, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_slice<2>(wa, wb, xrow, kb0, has_x, sgl, sul, sa[0], sa[1], acc);
-              part[0] = acc[0]; part[1] = acc[1]; part[2] = acc[2]; part[3] = acc[3];
-            } else if (RT == 1 && kw == 3) {
-              uint4 wa[6], wb[6];
-              load_slice<3>(ar0, ar0 + RU * a.H, kb0, hw0, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_slice<3>(wa, wb, xrow, kb0, has_x, sgl, sul, sa[0], sa[1], acc);
-              part[0] = acc[0]; part[1] = acc[1]; part[2] = acc[2]; part[3] = acc[3];
-            } else if (RT == 1 && kw == 1) {
-              uint4 wa[2], wb[2];
-              load_slice<1>(ar0, ar0 + RU * a.H, kb0, hw0, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_slice<1>(wa, wb, xrow, kb0, has_x, sgl, sul, sa[0], sa[1], acc);
-              part[0] = acc[0]; part[1] = acc[1]; part[2] = acc[2]; part[3] = acc[3];
-            } else if (RT == 2 && kw == 2) {
-              uint4 wa0[4], wb0[4], wa1[4], wb1[4];
-              load_slice<2>(ar0, ar0 + RU * a.H, kb0, hw0, wa0, wb0);
-              load_slice<2>(ar1, ar1 + RU * a.H, kb0, hw1, wa1, wb1);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_slice<2>(wa0, wb0, xrow, kb0, has_x, sgl, sul, sa[0], sa[1], acc0);
-              mma_slice<2>(wa1, wb1, xrow, kb0, has_x, sgl, sul, sa[0], sa[1], acc1);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                part[i] = acc0[i];
-                part[4 + i] = acc1[i];
-              }
-            } else {
-              released = false;
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                if (t >= RT) break;
-                const uint8_t* arow = t ? ar1 : ar0;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_slice_smem(arow, arow + RU * a.H, kb0, kw, t ? hw1 : hw0, xrow, has_x, sgl, sul, xs0, xs1, acc);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) part[4 * t + i] = acc[i];
-              }
-            }
-            if (!released) {
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-            }
-            if (!deposit(part)) {
-              ok = false;
-              break;
-            }
-            if (aborted()) {
-              ok = false;
-              break;
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.xempty[b]);
-      }
-      u = se;
-    }
-
-    // every h row the finisher wrote is visible before this CTA's counts are
-    __threadfence();
-    finish_sync();
-    if (fin && !aborted()) {
-      // per routed expert: the (unit, pass) count this CTA completed
-      const int dlo = (int)(r1.u0 / r1.upe), dhi = r1.u1 > r1.u0 ? (int)((r1.u1 - 1) / r1.upe) : dlo - 1;
-      for (int d = dlo + lane; d <= dhi; d += 32) {
-        const long ua = max(r1.u0, (long)d * r1.upe), ub = min(r1.u1, (long)(d + 1) * r1.upe);
-        const int passes = (meta_s[d].z + c.SPP1 - 1) / c.SPP1;
-        atomicAdd(p.ctr.c1 + d, (uint32_t)((ub - ua) * passes));
-      }
-    }
-
-    // ---------------------------------------------- down units
-    ScaleCache sc2;   // this warp's down-projection block scales
-    const float ones[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-    const int NT2 = R2 >> 4, KS2 = kCons / NT2;
-    const int tt = w % NT2, ks = w / NT2;
-    const int k2a = ks * nkb2 / KS2, k2b = (ks + 1) * nkb2 / KS2;
-    int gh = 0;
-    for (long u = r2.u0; ok && u < r2.u1;) {
-      const int d = (int)(u / r2.upe);
-      const long se = min(r2.u1, (long)(d + 1) * r2.upe);
-      const int4 md = meta_s[d];
-      const int e = md.x;
-      const int passes = (md.z + c.SPP2 - 1) / c.SPP2;
-      for (int ps = 0; ps < passes && ok; ++ps, ++gh) {
-        const int b = gh & 1, nh = min(c.SPP2, md.z - ps * c.SPP2);
-        const int pos0 = md.y + ps * c.SPP2;
-        if (!warp_wait(&B.hfull[b], (gh >> 1) & 1, lane)) {
-          ok = false;
-          break;
-        }
-        if (fin) {
-          // ------------------------------------------ finisher, down
-          // output slots of this lane (lanes cq < 2: slots 2cq, 2cq + 1),
-          // their top-k weights and h exponents
+          // output slots of this lane (lanes cq < 2: slots 2cq, 2cq + 1)
           int so[2] = {-1, -1}, es[2] = {0, 0};
           float wo[2] = {0.f, 0.f};
           if (cq < 2) {
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              if (2 * cq + j < nh) {
+              if (2 * cq + j < ns) {
                 so[j] = perm_s[pos0 + 2 * cq + j];
                 wo[j] = wts_s[so[j]];
                 es[j] = hexp[b * 4 + 2 * cq + j];
               }
           }
-          for (long uu = u; uu < se; ++uu, ++m) {
-            const int nb = (int)(uu % r2.upe) * R2;
-            if (!warp_wait(&B.rfull[m & 1], (m >> 1) & 1, lane)) {
-              ok = false;
-              break;
+          const int nb = (int)(W.uu % upe2) * 16 * NT2;
+          for (int t2 = 0; t2 < NT2; ++t2) {
+            float tot[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k2 = 0; k2 < KS2; ++k2) {
+              const float4 v =
+                  *reinterpret_cast<const float4*>(red + ((rb * kCons + t2 + k2 * NT2) * 32 + lane) * 4);
+              tot[0] += v.x;
+              tot[1] += v.y;
+              tot[2] += v.z;
+              tot[3] += v.w;
             }
-            for (int t2 = 0; t2 < NT2; ++t2) {
-              float tot[8];
-              gather(tot, t2, KS2, NT2);
-              // columns 2cq, 2cq + 1: hi terms on lanes cq < 2, lo terms on lanes cq >= 2
+            // columns 2cq, 2cq + 1: hi terms on lanes cq < 2, lo terms on lanes cq >= 2
 #pragma unroll
-              for (int i = 0; i < 4; ++i) tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], 2);
-              const int n0 = nb + t2 * 16;
+            for (int i = 0; i < 4; ++i) tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], 2);
+            const int n0 = nb + t2 * 16;
 #pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (so[j] < 0) continue;
-                float y0 = ldexpf(tot[j], es[j]) * wo[j];
-                float y1 = ldexpf(tot[2 + j], es[j]) * wo[j];
-                if (BIAS && a.b2) {
-                  const float* br = a.b2 + (int64_t)e * a.b2_ld + n0 + g;
-                  y0 = fmaf(wo[j], __ldg(br), y0);
-                  y1 = fmaf(wo[j], __ldg(br + 8), y1);
-                }
-                p.ybuf[(int64_t)so[j] * a.H + n0 + g] = y0;
-                p.ybuf[(int64_t)so[j] * a.H + n0 + g + 8] = y1;
+            for (int j = 0; j < 2; ++j) {
+              if (so[j] < 0) continue;
+              float y0 = ldexpf(tot[j], es[j]) * wo[j];
+              float y1 = ldexpf(tot[2 + j], es[j]) * wo[j];
+              if (BIAS && a.b2) {
+                const float* br = a.b2 + (int64_t)e * a.b2_ld + n0 + g;
+                y0 = fmaf(wo[j], __ldg(br), y0);
+                y1 = fmaf(wo[j], __ldg(br + 8), y1);
               }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.rempty[m & 1]);
-            if (aborted()) {
-              ok = false;
-              break;
+              p.ybuf[(int64_t)so[j] * a.H + n0 + g] = y0;
+              p.ybuf[(int64_t)so[j] * a.H + n0 + g + 8] = y1;
             }
           }
-        } else {
-          // ------------------------------------------ consumer, down
-          const uint8_t* hbrow = hconv0 + b * 8 * c.HP + g * c.HP + cq * 32;
-          const bool has_b = (g & 3) < nh;
-          for (long uu = u; uu < se; ++uu, ++m) {
-            const int n0 = (int)(uu % r2.upe) * R2 + tt * 16;   // this warp's 16 rows
-            const int rb = n0 >> 7;
-            const uint16_t* sbase = a.w2s + (int64_t)e * a.s2_exp;
-            const bool more = rb + 1 < (a.H >> 7) && (int)((se - 1) % r2.upe) * R2 + tt * 16 >= (rb + 1) * 128;
-            const float sl = sc2.get(sbase + (int64_t)rb * a.s2_row,
-                                     more ? sbase + (int64_t)(rb + 1) * a.s2_row : nullptr, k2a, k2b - k2a, lane);
-            const int slot = m % c.NS;
-            if (!warp_wait(&B.full[slot], (m / c.NS) & 1, lane)) {
-              ok = false;
-              break;
-            }
-            const uint8_t* st = ring + slot * c.SB + (tt * 16) * a.I + g * a.I + cq * 16;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            const int kw2 = k2b - k2a;
-            if (kw2 == 2) {
-              uint4 wa[4], wb[4];
-              load_slice<2>(st, st + 8 * a.I, k2a, true, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              mma_slice<2>(wa, wb, hbrow, k2a, has_b, sl, sl, ones, ones, acc);
-            } else if (kw2 == 1) {
-              uint4 wa[2], wb[2];
-              load_slice<1>(st, st + 8 * a.I, k2a, true, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              mma_slice<1>(wa, wb, hbrow, k2a, has_b, sl, sl, ones, ones, acc);
-            } else if (kw2 == 3) {
-              uint4 wa[6], wb[6];
-              load_slice<3>(st, st + 8 * a.I, k2a, true, wa, wb);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-              mma_slice<3>(wa, wb, hbrow, k2a, has_b, sl, sl, ones, ones, acc);
-            } else {
-              mma_slice_smem(st, st + 8 * a.I, k2a, kw2, true, hbrow, has_b, sl, sl, nullptr, nullptr, acc);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&B.empty[slot]);
-            }
-            const float part[8] = {acc[0], acc[1], acc[2], acc[3], 0.f, 0.f, 0.f, 0.f};
-            if (!deposit(part)) {
-              ok = false;
-              break;
-            }
-            if (aborted()) {
-              ok = false;
-              break;
-            }
-          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.rempty[rb]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.hempty[b]);
+        ++m;
+        W.next();
+        if (aborted()) ok = false;
       }
-      u = se;
+      if (ok) {
+        if (!signalled) signal_h();
+        enter_pass(W);   // release the last pass's buffer
+      }
     }
     if (!ok && lane == 0) fail();
     __syncwarp();
@@ -1082,62 +940,36 @@ bool place(FusedCfg& c, int H, int I) {
   c.o_cnt = o;
   o += al128(4 * c.DMAX);
   c.o_red = o;
-  o += 2 * kCons * 32 * 8 * 4;
+  o += 2 * kCons * 32 * 4 * 4;
   c.o_xaux = o;
   o += al128(4 * (2 * c.SPP1 * (1 + H / 128) + 8));
   c.o_act = o;
   const int xb = 2 * c.SPP1 * c.XP;
   const int hb = c.SPP2 * 4 * I + 2 * 8 * c.HP;
   o += al128(xb > hb ? xb : hb);
-  c.o_ring = o;
-  o += c.NS * c.SB;
   c.smem = o;
   return o <= kFSmemLimit;
 }
 
-// Candidate shapes, best first: gate/up units whose two copies are as large
-// as possible up to 32 KiB each, down units of at least the same stage,
-// at least 3 ring stages (about 100-200 KiB in flight per SM), then passes
-// of as many slots as still fit.
+// K rounds of 16 blocks for the gate/up tiles; for the down items two K
+// blocks per warp, as many 16-row tiles as the eight warps then cover
+// (the down projection's K, I, up to 2048); passes of as many slots as fit.
 bool choose_cfg(int H, int I, int S, int E, FusedCfg& c) {
+  const int nkb2 = I / 128;
+  if (nkb2 > 16) return false;
   c.S = S;
   c.DMAX = S < E ? S : E;
   c.XP = 2 * H + 16;   // == 16 mod 128: conflict-free fragment loads
   c.HP = 2 * I + 16;
-  const char* env = getenv("MOE_FP8_BLOCK_DECODE_CFG");   // tuning aid: "RU,R2,SPP1,NS"
-  if (env) {
-    int ru, r2, spp, ns;
-    if (sscanf(env, "%d,%d,%d,%d", &ru, &r2, &spp, &ns) == 4 && ru >= 1 && ru <= 16 && I % ru == 0 &&
-        (r2 == 16 || r2 == 32 || r2 == 64 || r2 == 128) && H % r2 == 0 && spp >= 1 && spp <= 8 && ns >= 2 &&
-        ns <= 8) {
-      c.RU = ru;
-      c.RT = (ru + 7) / 8;
-      c.R2 = r2;
-      c.SPP1 = spp;
-      c.SPP2 = 4;
-      c.SB = al128(2 * ru * H > r2 * I ? 2 * ru * H : r2 * I);
-      c.NS = ns;
-      if (place(c, H, I)) return true;
-    }
+  c.NKR1 = (H / 128 + 15) / 16;
+  c.KS2 = 1;
+  while (2 * c.KS2 < nkb2) c.KS2 <<= 1;
+  c.NT2 = kCons / c.KS2;
+  c.SPP2 = 4;
+  for (int spp = 8; spp >= 1; --spp) {
+    c.SPP1 = spp;
+    if (place(c, H, I)) return true;
   }
-  for (int ns_min = 3; ns_min >= 2; --ns_min)
-    for (int ru = 16; ru >= 1; ru >>= 1) {
-      if (I % ru || 128 % ru || (ru * H > 32768 && ru > 1)) continue;
-      c.RU = ru;
-      c.RT = (ru + 7) / 8;
-      for (int r2 = 128; r2 >= 16; r2 >>= 1) {
-        if (H % r2 || (r2 * I > 2 * ru * H && r2 > 16)) continue;
-        c.R2 = r2;
-        c.SB = al128(2 * ru * H > r2 * I ? 2 * ru * H : r2 * I);
-        for (int spp = 8; spp >= 2; --spp) {
-          c.SPP1 = spp;
-          c.SPP2 = I <= 1024 ? 4 : 2;
-          for (c.NS = 8; c.NS >= ns_min; --c.NS)
-            if (place(c, H, I)) return true;
-        }
-        break;
-      }
-    }
   return false;
 }
 
@@ -1171,6 +1003,12 @@ cudaError_t launch_decode_fused(const LayerArgs& a, float* h, float* ybuf, uint3
                      : (a.b13 || a.b2 ? decode_fused_kernel<false, true> : decode_fused_kernel<false, false>);
   cudaError_t err = set_max_smem((const void*)kern, p.c.smem);
   if (err != cudaSuccess) return note_error(err, "decode_fused smem attribute");
+  if (a.dbg_wait_ns) {
+    const uint64_t v = a.dbg_wait_ns;
+    if ((err = note_error(cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st),
+                          "decode wait limit")))
+      return err;
+  }
   const bool timed = stage_mark(st, 0);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms(device));
@@ -1185,6 +1023,12 @@ cudaError_t launch_decode_fused(const LayerArgs& a, float* h, float* ybuf, uint3
   if ((err = launch_check(cudaLaunchKernelEx(&cfg, kern, p), st, "decode_fused"))) return err;
   stage_mark(st, 1);
   *launches += 1;
+  if (a.dbg_wait_ns) {
+    const uint64_t v = kWaitTimeoutNs;
+    if ((err = note_error(cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st),
+                          "decode wait limit")))
+      return err;
+  }
   return cudaSuccess;
 }
 

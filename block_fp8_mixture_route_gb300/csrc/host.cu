@@ -621,6 +621,47 @@ int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* top
                       w2_scale_stride, out, stream, opt, true);
 }
 
+int moe_fp8_block_forward_host_experts(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                       const moe_tensor* topk_weights, const moe_tensor* w13,
+                                       const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,
+                                       const moe_tensor* w2_scale, int64_t w2_scale_stride, moe_tensor* out,
+                                       void* stream, const moe_options* opt) {
+  Checked c{};
+  int rc = check_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
+                         w2_scale_stride, out, false, &c);
+  if (rc) return rc;
+  float ratio;
+  int force;
+  if ((rc = check_options(opt, &ratio, &force, &c.a))) return rc;
+  if (force == MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (c.T == 0) {
+    g_last_launches = 0;
+    return MOE_OK;
+  }
+  int dev;
+  if ((rc = device_ok(&dev))) return rc;
+  LayerArgs a = c.a;
+  if (!fused_decode_ok(a.T, a.k, a.H, a.I, a.E)) return MOE_ERR_SHAPE;
+  // the banks must be page-locked host memory the device can address
+  void* d13 = mapped_host(w13->data);
+  void* d13s = mapped_host(w13_scale->data);
+  void* d2 = mapped_host(w2->data);
+  void* d2s = mapped_host(w2_scale->data);
+  if (!d13 || !d13s || !d2 || !d2s) return MOE_ERR_ARG;
+  if (!aligned16(d13) || !aligned16(d2)) return MOE_ERR_ALIGN;
+  a.w13 = static_cast<const uint8_t*>(d13);
+  a.w13s = static_cast<const uint16_t*>(d13s);
+  a.w2 = static_cast<const uint8_t*>(d2);
+  a.w2s = static_cast<const uint16_t*>(d2s);
+  a.host_weights = 1;
+  a.decode_kernel = MOE_DECODE_KERNEL_FUSED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = make_layout(c.T, a.k, a.H, a.I, a.E, MOE_PATH_DECODE, false);
+  void* ws = nullptr;
+  if ((rc = get_workspace(st, L.total, &ws))) return rc;
+  return run_forward(a, ratio, MOE_PATH_DECODE, st, false, ws, L, dev);
+}
+
 int moe_fp8_block_forward_act_codes(const moe_tensor* hidden, const moe_tensor* topk_ids,
                                     const moe_tensor* topk_weights, const moe_tensor* w13,
                                     const moe_tensor* w13_scale, int64_t w13_scale_stride, const moe_tensor* w2,

@@ -35,6 +35,7 @@ struct LayerArgs {
   uint8_t* dbg_codes = nullptr;
   float* dbg_scales = nullptr;
   int decode_kernel = MOE_DECODE_KERNEL_CHAIN;   // moe_options.decode_kernel
+  int host_weights = 0;        // w13, w2 and their scales are mapped page-locked host memory
   uint64_t dbg_wait_ns = 0;    // moe_options.debug_wait_timeout_us (0 = the default limit)
   int dbg_drop_stage = 0;      // moe_options.debug_drop_stage (0 = none)
 };

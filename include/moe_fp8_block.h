@@ -238,6 +238,34 @@ int moe_fp8_block_forward_hostio(const moe_tensor* hidden, const moe_tensor* top
                                  int64_t w2_scale_stride, moe_tensor* out, void* stream,
                                  const moe_options* opt);
 
+/*
+ * moe_fp8_block_forward_host_experts -- the decode forward with the expert
+ * banks held in HOST memory: the layer of moe_fp8_block_forward, where
+ * w13, w13_scale, w2 and w2_scale (same shapes, strides and rules) are
+ * page-locked host buffers (cudaHostAlloc, cudaHostRegister, torch
+ * pin_memory) that the device can address, and hidden, topk_ids,
+ * topk_weights and out stay device memory.  Serving block-fp8 experts
+ * that do not fit, or are not kept, in device memory is the offload case of
+ * FreeToken PR #662 (PR body: the cpu and hybrid backends); on GB300 the GPU
+ * reads the host-resident banks itself over NVLink-C2C, with ordinary
+ * 16-byte loads only (no bulk or tensor-map copies, no prefetches, of host
+ * memory), so only the routed experts' weights cross the link.
+ * The path is the single-launch decode kernel (W8A16, or W8A8 with
+ * decode_act = MOE_DECODE_ACT_E4M3); options are those of
+ * moe_fp8_block_forward_ex, and force_path = MOE_PATH_PREFILL is refused
+ * (MOE_ERR_ARG).  Returns MOE_ERR_ARG when a bank is not page-locked host
+ * memory, MOE_ERR_SHAPE when the layer or the slot count is outside what the
+ * single-launch decode kernel handles (H and I multiples of 128, I <= 2048,
+ * T*k <= 4096 within its shared-memory budget); otherwise as
+ * moe_fp8_block_forward_ex.  Asynchronous on `stream`.
+ */
+int moe_fp8_block_forward_host_experts(const moe_tensor* hidden, const moe_tensor* topk_ids,
+                                       const moe_tensor* topk_weights, const moe_tensor* w13,
+                                       const moe_tensor* w13_scale, int64_t w13_scale_stride,
+                                       const moe_tensor* w2, const moe_tensor* w2_scale,
+                                       int64_t w2_scale_stride, moe_tensor* out, void* stream,
+                                       const moe_options* opt);
+
 /* Size in bytes of the fixed device array behind
  * moe_fp8_block_forward_decode_noalloc. */
 #define MOE_FP8_BLOCK_NOALLOC_BYTES (8u << 20)
