@@ -10,10 +10,14 @@ from .api import (  # noqa: F401
     moe_fp8_block_act_quant,
     moe_fp8_block_device_status,
     moe_fp8_block_forward,
+    moe_fp8_block_forward_act_codes,
+    moe_fp8_block_forward_bias,
     moe_fp8_block_forward_decode_noalloc,
+    moe_fp8_block_forward_host_experts,
     moe_fp8_block_forward_hostio,
     moe_fp8_block_last_launches,
     moe_fp8_block_last_path,
+    moe_fp8_block_noalloc_status,
     moe_fp8_block_release,
     moe_fp8_block_reserve,
     moe_fp8_block_route,

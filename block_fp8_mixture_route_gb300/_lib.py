@@ -28,7 +28,7 @@ ERRORS = {
 EXPORTS = [
     "moe_fp8_block_forward", "moe_fp8_block_forward_ex", "moe_fp8_block_forward_bias",
     "moe_fp8_block_forward_hostio",
-    "moe_fp8_block_forward_decode_noalloc", "moe_fp8_block_forward_act_codes",
+    "moe_fp8_block_forward_decode_noalloc", "moe_fp8_block_noalloc_status", "moe_fp8_block_forward_act_codes",
     "moe_fp8_block_forward_host_experts",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
     "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
@@ -95,6 +95,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_widen_e4m3.argtypes = [vp, i64, vp, vp]
         lib.moe_fp8_block_reserve.argtypes = [i64, i32, i64, i64, i32, vp]
         lib.moe_fp8_block_device_status.argtypes = [vp, P(ctypes.c_uint32)]
+        lib.moe_fp8_block_noalloc_status.argtypes = [vp, P(ctypes.c_uint32)]
         lib.moe_fp8_block_last_path.argtypes = []
         lib.moe_fp8_block_last_launches.argtypes = []
         lib.moe_fp8_block_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]

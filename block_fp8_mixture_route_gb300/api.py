@@ -244,6 +244,13 @@ def moe_fp8_block_device_status(stream=None) -> int:
     return v.value
 
 
+def moe_fp8_block_noalloc_status(stream=None) -> int:
+    """Read and clear the status word of the allocation-free entry point."""
+    v = ctypes.c_uint32(0)
+    check(_lib.load().moe_fp8_block_noalloc_status(_stream(stream), ctypes.byref(v)), "moe_fp8_block_noalloc_status")
+    return v.value
+
+
 def moe_fp8_block_last_path() -> int:
     return _lib.load().moe_fp8_block_last_path()
 

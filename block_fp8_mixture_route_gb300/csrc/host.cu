@@ -569,6 +569,11 @@ void clear_smem_attributes() {
 
 void set_error_detail(const char* text) { snprintf(g_err_detail, sizeof(g_err_detail), "%s", text); }
 
+void record_call(int path, int launches) {
+  g_last_path = path;
+  g_last_launches = launches;
+}
+
 int num_sms(int device) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_sms.find(device);

@@ -99,6 +99,9 @@ int validate_forward(const moe_tensor* hidden, const moe_tensor* topk_ids, const
                      const moe_tensor* out, LayerArgs* args, int* device);
 // Text returned by moe_fp8_block_last_error_detail on this thread.
 void set_error_detail(const char* text);
+// What moe_fp8_block_last_path / moe_fp8_block_last_launches report for the
+// last successful call on this thread.
+void record_call(int path, int launches);
 
 // Stage events of moe_fp8_block_set_stage_events (per host thread).
 struct StageEvents {

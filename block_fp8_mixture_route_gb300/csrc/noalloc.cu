@@ -97,7 +97,10 @@ extern "C" int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, co
   int rc = validate_forward(hidden, topk_ids, topk_weights, w13, w13_scale, w13_scale_stride, w2, w2_scale,
                             w2_scale_stride, out, &a, &dev);
   if (rc) return rc;
-  if (a.T == 0) return MOE_OK;
+  if (a.T == 0) {
+    record_call(MOE_PATH_NONE, 0);
+    return MOE_OK;
+  }
   if (!decode_supported(a.H, a.I)) return MOE_ERR_SHAPE;
   const NaLayout L = na_layout(a.T, a.k, a.H, a.I, a.E);
   if (L.total > kNoAllocBytes) {
@@ -135,5 +138,31 @@ extern "C" int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, co
     cudaGetLastError();
     return e == cudaErrorNotSupported ? MOE_ERR_SHAPE : MOE_ERR_CUDA;
   }
+  record_call(MOE_PATH_DECODE, launches);
+  return MOE_OK;
+}
+
+extern "C" int moe_fp8_block_noalloc_status(void* stream, uint32_t* status) {
+  if (!status) return MOE_ERR_NULL;
+  *status = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  void* base = nullptr;
+  if (note_error(scratch_address(dev, &base), "noalloc scratch address") != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  // the status word sits at the start of the array (na_layout's first field)
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, base, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(base, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  *status = v;
   return MOE_OK;
 }

@@ -289,22 +289,42 @@ int moe_fp8_block_forward_host_experts(const moe_tensor* hidden, const moe_tenso
  * until the process exits.  A call needs about
  * 4*T*k*(H + I) + 2*T*H + 16*(E + T*k) bytes of it; a larger call returns
  * MOE_ERR_ARG and moe_fp8_block_last_error_detail says how many bytes it
- * needed.  Nothing is allocated: no cudaMalloc or cudaFree, no allocating
- * library routine.
+ * needed.  The entry point itself calls no cudaMalloc or cudaFree and no
+ * allocating library routine.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before capturing the stream into a CUDA graph.  Every call on every stream
- * of a device uses the same array: calls whose kernels overlap on the GPU
- * race and give wrong results, so serialise them (one stream, or events).
- * Each call clears the array's status word first; the status bits of this
- * entry point are not reported by moe_fp8_block_device_status.
+ * (cudaGetSymbolAddress, with that device current).  CUDA loads modules
+ * lazily by default, so that first lookup may load the library's module and
+ * commit the array's memory on the device, with the implicit synchronisation
+ * a module load brings: make the first call (a warm-up call, or
+ * moe_fp8_block_noalloc_status) before the serving loop starts and before
+ * capturing the stream into a CUDA graph.  Later calls allocate nothing.
+ * Every call on every stream of a device uses the same array: calls whose
+ * kernels overlap on the GPU race and give wrong results, so serialise them
+ * (one stream, or events).  Each call clears the array's status word first;
+ * read it with moe_fp8_block_noalloc_status (moe_fp8_block_device_status
+ * reads the per-stream workspaces of the other entry points, not this
+ * array).  moe_fp8_block_last_path reports MOE_PATH_DECODE and
+ * moe_fp8_block_last_launches the kernels launched, as for the regular
+ * forward.
  */
 int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, const moe_tensor* topk_ids,
                                          const moe_tensor* topk_weights, const moe_tensor* w13,
                                          const moe_tensor* w13_scale, int64_t w13_scale_stride,
                                          const moe_tensor* w2, const moe_tensor* w2_scale,
                                          int64_t w2_scale_stride, moe_tensor* out, void* stream);
+
+/*
+ * moe_fp8_block_noalloc_status -- waits for `stream`, then returns in
+ * *status and clears the status word of moe_fp8_block_forward_decode_noalloc's
+ * array on the current device (the MOE_STATUS_* bits the kernels of the last
+ * such call raised: out-of-range expert ids, a wait that ran out).  Reading
+ * and clearing are ordered on `stream`; a call on another stream that still
+ * runs may set bits afterwards.  Allocates nothing.
+ *  status   host uint32, written (0 on any error)
+ * Returns MOE_OK, MOE_ERR_NULL (status NULL) or MOE_ERR_CUDA.
+ */
+int moe_fp8_block_noalloc_status(void* stream, uint32_t* status);
 
 /*
  * moe_fp8_block_forward_act_codes -- moe_fp8_block_forward_ex, plus a copy
