@@ -67,7 +67,7 @@ def test_padded_skewed_decode(cuda_lib, T):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("T,tokens", [(1, None), (4, None), (16, [0, 7, 15]), (64, [0, 31, 63])])
+@pytest.mark.parametrize("T,tokens", [(1, None), (4, None), (16, [0, 5, 10, 15]), (64, [0, 21, 42, 63])])
 def test_decode_wide_experts(cuda_lib, T, tokens):
     r, _ = run_and_check(problem(syn.DECODE_WIDE, T), "decode", tokens=tokens)
     assert r < TOL
@@ -226,13 +226,54 @@ def test_prefill_padded_skewed(cuda_lib, T):
     assert r < TOL
 
 
-@pytest.mark.parametrize("T,routing,tokens", [
-    (1024, "softmax", None), (1024, "zipf", None),
-    (4096, "softmax", [0, 1, 2047, 4095]), (4096, "zipf", [3, 100, 4000]),
-    (16384, "zipf", [0, 8191, 16383]),
-])
-def test_prefill_grouped_gemm(cuda_lib, T, routing, tokens):
-    r, _ = run_and_check(problem(syn.PREFILL, T, routing=routing), "prefill", tokens=tokens)
+def tile_probe_tokens(ids: np.ndarray, E: int, n: int = 64, seed: int = 0):
+    """Tokens that land on every form of the grouped GEMM's 128-row M tiles
+    (rows in the routing lists' order, expert ascending, stable in the slot
+    index): rows 0, 127, 128 and 255 of experts with two or more tiles (the
+    form where the two CTAs of a pair take M tiles 2i and 2i+1), the first
+    and last rows of the last tile of experts with an odd tile count (the
+    form where both CTAs take that one tile), the last row of every expert
+    (the ragged tail), then random tokens up to `n`, plus tokens 0 and T-1.
+    Every checked token covers all column blocks, the last one included."""
+    T, k = ids.shape
+    rl = mo.route_lists(ids, E)
+    off, perm = rl["offsets"], rl["perm"]
+    pick = {0, T - 1}
+    tiles = -(-rl["counts"].astype(np.int64) // 128)
+    two = [e for e in range(E) if tiles[e] >= 2]
+    odd = [e for e in range(E) if tiles[e] % 2 == 1]
+    rng = np.random.default_rng(seed)
+    for e in rng.permutation(two)[:6]:
+        c = off[e + 1] - off[e]
+        pick.update(int(perm[off[e] + r]) // k for r in (0, 127, 128, min(255, c - 1)))
+    for e in rng.permutation(odd)[:6]:
+        c = off[e + 1] - off[e]
+        first = (tiles[e] - 1) * 128
+        pick.update(int(perm[off[e] + r]) // k for r in (first, c - 1))
+    for e in rng.permutation(E)[:8]:
+        if off[e + 1] > off[e]:
+            pick.add(int(perm[off[e + 1] - 1]) // k)
+    rest = [t for t in rng.permutation(T) if t not in pick]
+    pick.update(int(t) for t in rest[:max(0, n - len(pick))])
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("T,routing", [(1024, "softmax"), (1024, "zipf")])
+def test_prefill_grouped_gemm(cuda_lib, T, routing):
+    r, _ = run_and_check(problem(syn.PREFILL, T, routing=routing), "prefill")
+    assert r < TOL
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,routing", [(4096, "softmax"), (4096, "zipf"), (16384, "softmax"), (16384, "zipf")])
+def test_prefill_grouped_gemm_full_size(cuda_lib, T, routing):
+    """The prefill workload at full size (the bench's T = 4096 and 16384),
+    checked on at least 64 tokens chosen to hit both pair-tile forms and
+    the ragged tail of several experts."""
+    prob = problem(syn.PREFILL, T, routing=routing)
+    tokens = tile_probe_tokens(prob["topk_ids"].cpu().numpy(), syn.PREFILL.E, n=64, seed=T)
+    assert len(tokens) >= 64
+    r, _ = run_and_check(prob, "prefill", tokens=tokens)
     assert r < TOL
 
 
