@@ -180,8 +180,6 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
   if (threadIdx.x == 0) p.db.xexp[t] = s;
 }
 
-__device__ __forceinline__ int4 ld_meta(const DecodeArgs& p, int d) { return __ldg(p.rb.meta + d); }
-
 // Shared-memory layout common to both streaming kernels.
 struct Smem {
   uint64_t* full;     // [kMaxNS] ring stage landed (tx)
@@ -234,31 +232,45 @@ __device__ __forceinline__ void smem_init(const Smem& s, int NS) {
   fence_mbar_init();
 }
 
-// The CTA's units, walked expert segment by expert segment and, within a
-// segment, pass by pass (a pass covers up to SPP of the expert's slots), so
+// The CTA's units, walked entry by entry of a work list and, within an
+// entry, pass by pass (a pass covers up to SPP of the entry's slots), so
 // that each (expert, pass) activation load is shared by all units of the
-// segment.  Producer and consumers walk the same sequence; ring stage m goes
-// to consumer group m % 2.
+// segment.  The gate/up projection walks one entry per routed expert; the
+// down projection a per-pass list (one entry per pass), so that an expert
+// with many slots weighs in its split as its passes over the weights do.
+// Producer and consumers walk the same sequence; ring stage m goes to
+// consumer group m % 2.
 struct Walk {
   long u, ue;          // next segment start, range end
-  int upe;             // units per expert
-  int d, e, off, ne;   // current expert
+  int upe;             // units per list entry
+  const int4* list;    // the work list
+  int d, e, off, ne;   // current entry: expert, first routed position, slots
+  int ep;              // passes over this expert's weights in the whole list
   long seg_b, seg_e;   // current segment [seg_b, seg_e)
   int passes;
 };
 
 __device__ __forceinline__ bool walk_next_segment(const DecodeArgs& p, Walk& w, int SPP) {
+  (void)p;   // the list is the walk's own
   if (w.u >= w.ue) return false;
   w.d = (int)(w.u / w.upe);
   w.seg_b = w.u;
   w.seg_e = min(w.ue, (long)(w.d + 1) * w.upe);
-  const int4 m = ld_meta(p, w.d);
+  const int4 m = __ldg(w.list + w.d);
   w.e = m.x;
   w.off = m.y;
   w.ne = m.z;
+  w.ep = m.w;
   w.passes = (w.ne + SPP - 1) / SPP;
   w.u = w.seg_e;
   return true;
+}
+
+// Weight copies: evict-first for an expert read once; the default policy
+// where the list reads it again (later passes, often on a neighbouring SM
+// shortly after), so that the repeat can find it in L2.
+__device__ __forceinline__ uint64_t weight_policy(const Walk& w, uint64_t once, uint64_t again) {
+  return w.ep > 1 ? again : once;
 }
 
 // Rows per unit: halved only while there are fewer units than SMs (the
@@ -396,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
   wk.u = U * blockIdx.x / gridDim.x;
   wk.ue = U * (blockIdx.x + 1) / gridDim.x;
   wk.upe = upe;
+  wk.list = p.rb.meta;   // one entry per routed expert, its passes inside
   const int NS = cfg.NS, SPP = cfg.SPP;
   const int rowb = R * a.H;   // bytes of R whole rows
 
@@ -910,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
   // the kernel this one follows (GEMM1) released its dependents, so they can
   // be read before waiting for GEMM1; only h needs the wait.
   const LayerArgs& a = p.a;
-  const int D = *p.rb.nd;
+  const int D = p.rb.nd[1];
   const int R2 = balanced_rows(cfg.R, 16, a.H, D, gridDim.x);
   const int upe = a.H / R2;
   const long U = (long)D * upe;
@@ -918,11 +931,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
   wk.u = U * blockIdx.x / gridDim.x;
   wk.ue = U * (blockIdx.x + 1) / gridDim.x;
   wk.upe = upe;
+  wk.list = p.rb.vmeta;
   const int NS = cfg.NS, SPP = cfg.SPP;
   const int tileb = R2 * a.I;
 
   if (warp == kNWC) {
-    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_once = l2_policy_evict_first();
+    const uint64_t pol_again = l2_policy_evict_normal();
     const uint64_t pol_h = l2_policy_evict_last();
     int m = 0, gen = 0;
     bool ok = true;
@@ -932,6 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     {
       Walk w0 = wk;
       if (walk_next_segment(p, w0, SPP)) {
+        const uint64_t pol_w = weight_policy(w0, pol_once, pol_again);
         const long n = min((long)kPreIssue, w0.seg_e - w0.seg_b);
         if (lane == 0)
           for (long i = 0; i < n; ++i) {
@@ -944,6 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
     }
     pdl_wait();
     while (ok && walk_next_segment(p, wk, SPP)) {
+      const uint64_t pol_w = weight_policy(wk, pol_once, pol_again);
       for (int pass = 0; pass < wk.passes && ok; ++pass, ++gen) {
         const int nh = min(SPP, wk.ne - pass * SPP);
         // the raw h buffer is single: wait until every consumer has converted the previous pass
@@ -1151,6 +1168,10 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
     return launch_decode_fused(a, db.h, db.ybuf, db.counters, status, device, st, launches);
   DecodeArgs p{a, rb, db, status, {}, {}};
   if (!config_gemm1(a.H, p.c1) || !config_gemm2(a.H, a.I, p.c2)) return cudaErrorNotSupported;
+  if (!db.vmeta) return cudaErrorInvalidValue;
+  // the prep kernel's route also writes the down projection's per-pass work list
+  p.rb.vmeta = db.vmeta;
+  p.rb.spp = p.c2.SPP;
   const int sms = num_sms(device);
   cudaError_t err;
   // few slots: a smaller CTA keeps the route's block-wide scans short; the

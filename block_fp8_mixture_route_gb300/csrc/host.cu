@@ -37,7 +37,7 @@ const size_t kCountersEnd = align_up(16) + align_up(4 * (size_t)kFusedCounterWor
 // Byte layout of one workspace.
 struct Layout {
   size_t status, fctr, counts, offsets, perm, inv, glist, nd, meta, mtp, mtp2, rcnt;
-  size_t xh, xexp, xsd, h, ybuf;                  // decode
+  size_t xh, xexp, xsd, h, ybuf, vmeta;           // decode
   size_t xq, xs, hq, hs, ys, pinv, wsc13, wsc2;  // prefill
   int64_t prows;
   size_t hid, tids, twts, outb;                   // host-io staging
@@ -72,6 +72,7 @@ Layout make_layout(int64_t T, int k, int64_t H, int64_t I, int E, int path, bool
     L.h = take(4 * (size_t)(S * I));
     L.ybuf = take(4 * (size_t)(S * H));
     L.xsd = take(4 * (size_t)T * (size_t)((H + 127) / 128));
+    L.vmeta = take(16 * (size_t)(S > 0 ? S : 1));
   } else if (path == MOE_PATH_PREFILL) {
     const int64_t R = prefill_rows(S, E);
     L.prows = R;
@@ -346,6 +347,7 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
     db.h = reinterpret_cast<float*>(w + L.h);
     db.ybuf = reinterpret_cast<float*>(w + L.ybuf);
     db.counters = reinterpret_cast<uint32_t*>(w + L.fctr);
+    db.vmeta = reinterpret_cast<int4*>(w + L.vmeta);
     err = launch_decode(a, rb, db, status, dev, st, &launches);
   } else {
     PrefillBufs pb;

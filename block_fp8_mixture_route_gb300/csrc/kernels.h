@@ -53,6 +53,13 @@ struct RouteBufs {
   int32_t* mtp = nullptr;   // [E+1]: exclusive prefix of ceil(count/128) per expert (optional)
   int32_t* mtp2 = nullptr;  // [E+1]: exclusive prefix of ceil(ceil(count/128)/2), the pairs of
                             // 128-row tiles per expert (optional)
+  // Per-pass work list of the decode down projection (optional; then nd
+  // must have room for 2 ints and mtp/mtp2 are not written): the routed
+  // experts split into passes of at most spp consecutive slots, one entry
+  // {expert, first routed position, slot count, passes of that expert} per
+  // pass, in ascending (expert, pass) order; nd[1] receives the entry count.
+  int4* vmeta = nullptr;    // [S]
+  int spp = 0;
 };
 
 // Scratch of the decode path.
@@ -63,6 +70,7 @@ struct DecodeBufs {
   float* h;           // [S, I] in routed (perm) order
   float* ybuf;        // [S, H] in slot order, times the slot's top-k weight
   uint32_t* counters = nullptr;   // fused kernel: kFusedCounterWords words, zero between forwards
+  int4* vmeta = nullptr;          // [S]: the down projection's per-pass work list (RouteBufs::vmeta)
 };
 
 // Scratch of the prefill path.  Per-row buffers hold `rows` rows in the

@@ -51,7 +51,7 @@ cudaError_t scratch_address(int device, void** out) {
 inline size_t al(size_t x) { return (x + 255) / 256 * 256; }
 
 struct NaLayout {
-  size_t status, fctr, counts, offsets, perm, inv, glist, nd, meta, xh, xexp, xs, h, ybuf, total;
+  size_t status, fctr, counts, offsets, perm, inv, glist, nd, meta, vmeta, xh, xexp, xs, h, ybuf, total;
 };
 
 NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
@@ -73,6 +73,7 @@ NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
   L.glist = take(4 * (size_t)(g > 0 ? g : 1));
   L.nd = take(16);
   L.meta = take(16 * (size_t)(g > 0 ? g : 1));
+  L.vmeta = take(16 * (size_t)(S > 0 ? S : 1));
   L.xh = take(2 * (size_t)(T * H));
   L.xexp = take(4 * (size_t)T);
   L.h = take(4 * (size_t)(S * I));
@@ -130,7 +131,8 @@ extern "C" int moe_fp8_block_forward_decode_noalloc(const moe_tensor* hidden, co
                reinterpret_cast<int4*>(w + L.meta),       nullptr};
   DecodeBufs db{reinterpret_cast<uint16_t*>(w + L.xh), reinterpret_cast<int32_t*>(w + L.xexp),
                 reinterpret_cast<float*>(w + L.xs), reinterpret_cast<float*>(w + L.h),
-                reinterpret_cast<float*>(w + L.ybuf), reinterpret_cast<uint32_t*>(w + L.fctr)};
+                reinterpret_cast<float*>(w + L.ybuf), reinterpret_cast<uint32_t*>(w + L.fctr),
+                reinterpret_cast<int4*>(w + L.vmeta)};
   int launches = 0;
   const cudaError_t e = launch_decode(a, rb, db, status, dev, st, &launches);
   if (e != cudaSuccess) {

@@ -155,20 +155,26 @@ static __device__ void route_warp_place(const int32_t* __restrict__ ids, int s0,
 }
 
 // Expert-level lists from per-expert counts in eoff[E] (shared memory):
-// writes counts, offsets, glist (padded to min(E, S)), meta, mtp, mtp2, n_distinct
-// and fills perm[offsets[E] .. S) with -1.  On return eoff[e] holds the
-// offset of expert e.  Ends with __syncthreads.
+// writes counts, offsets, glist (padded to min(E, S)), meta, n_distinct,
+// and either mtp, mtp2 or (decode) the per-pass work list, and fills
+// perm[offsets[E] .. S) with -1.  On return eoff[e] holds the offset of
+// expert e.  Ends with __syncthreads.
 static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) {
   __shared__ int4 red[33];
   const int nt = blockDim.x, tid = threadIdx.x;
   const int per = (E + nt - 1) / nt;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  // the third scanned quantity: 128-row tiles (prefill) or passes of spp
+  // slots (decode work list); the fourth: pairs of 128-row tiles (prefill)
+  const bool vl = rb.vmeta != nullptr;
+  auto q3 = [&](int c) { return vl ? (c + rb.spp - 1) / rb.spp : (c + 127) >> 7; };
+  auto q4 = [&](int c) { return vl ? 0 : (((c + 127) >> 7) + 1) >> 1; };
   int lc = 0, ld = 0, lm = 0, lp = 0;
   for (int e = e0; e < e1; ++e) {
     lc += eoff[e];
     ld += eoff[e] > 0;
-    lm += (eoff[e] + 127) >> 7;
-    lp += (((eoff[e] + 127) >> 7) + 1) >> 1;
+    lm += q3(eoff[e]);
+    lp += q4(eoff[e]);
   }
   int4 tot;
   const int4 ex = block_exclusive_scan4(make_int4(lc, ld, lm, lp), red, &tot);
@@ -178,10 +184,15 @@ static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) 
     const int c = eoff[e];
     rb.counts[e] = c;
     rb.offsets[e] = oc;
-    if (rb.mtp) rb.mtp[e] = om;
-    if (rb.mtp2) rb.mtp2[e] = op;
-    om += (c + 127) >> 7;
-    op += (((c + 127) >> 7) + 1) >> 1;
+    if (vl) {
+      const int n = q3(c);
+      for (int q = 0; q < n; ++q) rb.vmeta[om + q] = make_int4(e, oc + q * rb.spp, min(rb.spp, c - q * rb.spp), n);
+    } else {
+      if (rb.mtp) rb.mtp[e] = om;
+      if (rb.mtp2) rb.mtp2[e] = op;
+    }
+    om += q3(c);
+    op += q4(c);
     eoff[e] = oc;
     if (c > 0) {
       if (rb.meta) rb.meta[od] = make_int4(e, oc, c, 0);
@@ -193,9 +204,13 @@ static __device__ void route_expert_scan(int* eoff, int E, int S, RouteBufs rb) 
   for (int d = tot_d + tid; d < g; d += nt) rb.glist[d] = -1;
   if (tid == 0) {
     rb.offsets[E] = tot_c;
-    *rb.nd = tot_d;
-    if (rb.mtp) rb.mtp[E] = tot_m;
-    if (rb.mtp2) rb.mtp2[E] = tot_p;
+    rb.nd[0] = tot_d;
+    if (vl) {
+      rb.nd[1] = tot_m;
+    } else {
+      if (rb.mtp) rb.mtp[E] = tot_m;
+      if (rb.mtp2) rb.mtp2[E] = tot_p;
+    }
   }
   for (int q = tot_c + tid; q < S; q += nt) rb.perm[q] = -1;
   __syncthreads();

@@ -287,7 +287,7 @@ int moe_fp8_block_forward_host_experts(const moe_tensor* hidden, const moe_tenso
  * outputs) lives in one statically allocated device array of
  * MOE_FP8_BLOCK_NOALLOC_BYTES bytes that every GPU using the library keeps
  * until the process exits.  A call needs about
- * 4*T*k*(H + I) + 2*T*H + 16*(E + T*k) bytes of it; a larger call returns
+ * 4*T*k*(H + I) + 2*T*H + 16*E + 32*T*k bytes of it; a larger call returns
  * MOE_ERR_ARG and moe_fp8_block_last_error_detail says how many bytes it
  * needed.  The entry point itself calls no cudaMalloc or cudaFree and no
  * allocating library routine.
