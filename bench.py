@@ -13,6 +13,12 @@ routed experts' e4m3 weights and valid bf16 block scales, divided by the
 device time of the forwards (CUDA events on the launching stream).  The
 headline `value` aggregates every forward of up to 16 tokens (the range the
 decode target is stated for); each layer's numbers, per T, are beside it.
+Each forward takes the path the library's gate chooses for it (--path auto):
+the W8A16 decode kernels for the small and skewed layers, the tcgen05 W8A8
+grouped GEMMs for the wide layer, whose 14 KiB activation rows leave the
+decode weight ring too few stages.  `value_decode_path` is the same
+aggregate with every forward forced onto the decode kernels, and --path
+decode makes that the headline.
 
 No forward finds its weights in L2.  Two ways to ensure it (--l2), for the
 small and skewed layers:
@@ -62,6 +68,7 @@ WORKLOAD = ("decode, batches of up to 16 tokens of three layers: E=128 H=2048 I=
             "E=256 H=2560 I=640 skewed (T=1,8); E=256 H=7168 I=2048 (T=1,4,16); top_k=8")
 METRIC = "decode routed-weight HBM GB/s"
 DECODE_KERNEL = "chain"   # --decode-kernel: the chained decode kernels or the single persistent one
+FORCE = None              # --path: None = the library's own gate per call; "decode" = the W8A16 decode path
 
 
 def routed_bytes(shape: syn.MoeShape, ids: torch.Tensor) -> tuple[int, int]:
@@ -129,18 +136,21 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def profile_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
-    the kernel source has not changed since it was taken (else None)."""
+def profile_traffic(kernel: str):
+    """(DRAM bytes of one launch, captured workload, its algorithmic bytes)
+    of `kernel` from the committed ncu summary profiles/traffic.txt, if the
+    source file it was captured from has not changed since (else None).
+    Line format: kernel workload dram_bytes algorithmic_bytes source sha256[:16]."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = open(os.path.join(ROOT, "block_fp8_mixture_route_gb300", "csrc", "decode.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
     for line in open(path):
         f = line.split()
-        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[3] == sha:
-            return float(f[2])
+        if len(f) < 6 or line.startswith("#") or f[0] != kernel:
+            continue
+        src = os.path.join(ROOT, "block_fp8_mixture_route_gb300", "csrc", f[4])
+        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == f[5]:
+            return float(f[2]), f[1], float(f[3])
     return None
 
 
@@ -324,7 +334,7 @@ def hold_stream(s, ms: float):
         torch.cuda._sleep(int(ms * 2.0e6))
 
 
-def capture_forwards(wl, feed, s, outs):
+def capture_forwards(wl, feed, s, outs, force):
     """One CUDA graph per (T, weight bank) of the library's forward, captured
     on stream s (the library is capture-safe once its workspace is sized):
     replays launch the forward's kernels without host work in between."""
@@ -333,7 +343,7 @@ def capture_forwards(wl, feed, s, outs):
         for bank in range(feed.n_banks()):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
-                api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode",
+                api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path=force,
                                     decode_kernel=DECODE_KERNEL)
             graphs[(T, bank)] = g
     with torch.cuda.stream(s):
@@ -343,7 +353,7 @@ def capture_forwards(wl, feed, s, outs):
     return graphs
 
 
-def timed_forwards(wl, feed, s, outs, steps, graphs=None, decode_act=None):
+def timed_forwards(wl, feed, s, outs, steps, graphs=None, decode_act=None, force=None):
     """Device time of every forward of `steps` steps: {T: [ms per forward]}.
     With `graphs`, each forward is a replay of its captured graph."""
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.ts]
@@ -357,7 +367,7 @@ def timed_forwards(wl, feed, s, outs, steps, graphs=None, decode_act=None):
                 if graphs is not None:
                     graphs[(T, bank)].replay()
                 else:
-                    api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path="decode",
+                    api.forward_problem(feed.problem(T, bank), out=outs[T], stream=s, force_path=force,
                                         decode_act=decode_act, decode_kernel=DECODE_KERNEL)
                 ev[k][i][1].record(s)
     s.synchronize()
@@ -395,6 +405,59 @@ WORKLOADS = [
 HEADLINE_T_MAX = 16
 
 
+DECODE_KERNELS = ["decode_prep_kernel", "decode_gemm1_kernel", "decode_gemm2_kernel", "decode_combine_kernel"]
+PREFILL_KERNELS = ["route", "act_quant_permute_kernel", "prefill_gemm_kernel<1>", "prefill_gemm_kernel<2>",
+                   "prefill_combine_kernel"]
+
+
+def kernel_names(path: str, n: int) -> list:
+    """Names of the stage-timed kernels of one forward (the route of the
+    prefill path is one stage whatever its launch count)."""
+    if path == "decode":
+        return DECODE_KERNELS[:n] if n == 4 else ["decode_fused_kernel"][:n]
+    return PREFILL_KERNELS[:n]
+
+
+def kernel_bytes(name: str, shape, T: int, D: int) -> int:
+    """Algorithmic bytes of one launch: what the kernel must read and write
+    at least (weights and valid scales of the D routed experts it streams,
+    its activation inputs once, its outputs once)."""
+    E, H, I, k = shape.E, shape.H, shape.I, shape.k
+    S = T * k
+    w13 = D * (2 * I * H + 2 * ((2 * I // 128) * (H // 128)))
+    w2 = D * (H * I + 2 * ((H // 128) * (I // 128)))
+    return {
+        "decode_prep_kernel": 4 * S + 2 * T * H + 2 * T * H,
+        "decode_gemm1_kernel": w13 + 2 * T * H + 4 * S * I,
+        "decode_gemm2_kernel": w2 + 4 * S * I + 4 * S * H,
+        "decode_combine_kernel": 4 * S * H + 2 * T * H,
+        "decode_fused_kernel": w13 + w2 + 2 * T * H + 2 * T * H,
+        "route": 4 * S + 4 * S,
+        "act_quant_permute_kernel": 2 * T * H + S * H + 4 * S * (H // 128),
+        "prefill_gemm_kernel<1>": w13 + S * H + S * I + 4 * S * ((H // 128) + (I // 128)),
+        "prefill_gemm_kernel<2>": w2 + S * I + 2 * S * H + 4 * S * (I // 128),
+        "prefill_combine_kernel": 2 * S * H + 2 * T * H,
+    }[name]
+
+
+def roofline_entry(name, nbytes, ms, n, steps, hbm, src, share):
+    """The `roofline` object for the dominant kernel: its algorithmic bytes
+    per launch over its average stage-timed launch duration, against the
+    measured copy bandwidth; traffic = ncu DRAM bytes of one captured launch
+    (committed summary) while the kernel's source is unchanged."""
+    achieved = nbytes / (ms / 1e3) / 1e9
+    tr = profile_traffic(name)
+    return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": tr[0] if tr else None,
+            "traffic_case": ({"workload": tr[1], "algorithmic_bytes": tr[2]} if tr else None),
+            "launches_timed": n, "share_of_kernel_time": share,
+            "algorithmic_bytes": "per launch: the routed experts' e4m3 weights and valid bf16 scales the kernel "
+                                 "streams, its activation inputs read once and its outputs written once; "
+                                 "summed over the headline forwards' launches, over their summed stage-timed "
+                                 "durations",
+            "peak_source": f"{src} hbm_gbs (copy, burst)"}
+
+
 def algorithmic_bytes(shape, T, D) -> int:
     """Least bytes a decode forward moves: the routed experts' weights and
     valid block scales, the activations read and the output written."""
@@ -419,31 +482,41 @@ def measure_workload(wl, dev, s, steps, warmup, l2="rotate", graphs_on=True, ext
     with torch.cuda.stream(s):
         for _ in range(warmup):
             for T in wl.ts:
-                api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode",
-                                    decode_kernel=DECODE_KERNEL)
+                for force in {FORCE, "decode"}:
+                    api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path=force,
+                                        decode_kernel=DECODE_KERNEL)
     s.synchronize()
-    launches = {}
+    launches, paths = {}, {}
     for T in wl.ts:
         with torch.cuda.stream(s):
-            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+            api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path=FORCE, decode_kernel=DECODE_KERNEL)
         launches[T] = api.moe_fp8_block_last_launches()
+        paths[T] = "decode" if api.moe_fp8_block_last_path() == 1 else "prefill"
     s.synchronize()
-    graphs = capture_forwards(wl, feed, s, outs) if graphs_on else None
-    per_T = timed_forwards(wl, feed, s, outs, steps, graphs)
+    graphs = capture_forwards(wl, feed, s, outs, FORCE) if graphs_on else None
+    per_T = timed_forwards(wl, feed, s, outs, steps, graphs, force=FORCE)
     kern = kernel_durations(wl, feed, s, max(3, steps // 2))
+    # where the library's gate takes the prefill path, the forced decode path too
+    per_T_decode = {T: per_T[T] for T in wl.ts if paths[T] == "decode"}
+    other = [T for T in wl.ts if paths[T] != "decode"]
+    if other:
+        sub_wl = Workload(wl.name, wl.shape, other, wl.routing, wl.banks, wl.desc, wl.hold_scale)
+        dgraphs = capture_forwards(sub_wl, feed, s, outs, "decode") if graphs_on else None
+        per_T_decode.update(timed_forwards(sub_wl, feed, s, outs, steps, dgraphs, force="decode"))
+        del dgraphs
     res = {"workload": wl.desc, "l2": feed.describe(), "per_T": per_T, "info": info, "kern": kern,
-           "launches": launches}
+           "launches": launches, "paths": paths, "per_T_decode": per_T_decode}
     if extras:
         alt = Feed(wl, probs, "flush" if mode == "rotate" else "rotate", dev, wl.banks)
-        alt_graphs = capture_forwards(wl, alt, s, outs) if graphs_on else None
-        alt_T = timed_forwards(wl, alt, s, outs, steps, alt_graphs)
+        alt_graphs = capture_forwards(wl, alt, s, outs, FORCE) if graphs_on else None
+        alt_T = timed_forwards(wl, alt, s, outs, steps, alt_graphs, force=FORCE)
         res["alt"] = (alt.describe(), alt_T)
-        res["eager"] = timed_forwards(wl, feed, s, outs, steps)
+        res["eager"] = timed_forwards(wl, feed, s, outs, steps, force=FORCE)
         with torch.cuda.stream(s):
             for T in wl.ts:
                 api.forward_problem(feed.next(T), out=outs[T], stream=s, force_path="decode", decode_act="e4m3",
                                     decode_kernel=DECODE_KERNEL)
-        res["w8a8"] = timed_forwards(wl, feed, s, outs, steps, decode_act="e4m3")
+        res["w8a8"] = timed_forwards(wl, feed, s, outs, steps, decode_act="e4m3", force="decode")
         res["feed"] = feed
     else:
         del feed, probs, graphs
@@ -461,8 +534,10 @@ def kernel_durations(wl, feed, s, reps):
     res = {}
     for T in wl.ts:
         with torch.cuda.stream(s):
-            api.forward_problem(feed.next(T), stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+            api.forward_problem(feed.next(T), stream=s, force_path=FORCE, decode_kernel=DECODE_KERNEL)
         n = api.moe_fp8_block_last_launches()
+        if api.moe_fp8_block_last_path() == 2:
+            n = len(PREFILL_KERNELS)   # the route is one stage whatever its launch count
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         for e in evs:          # torch creates the event handle on first record
             e.record(s)
@@ -474,7 +549,7 @@ def kernel_durations(wl, feed, s, reps):
             with torch.cuda.stream(s):
                 prob = feed.next(T)
                 _lib.check(lib.moe_fp8_block_set_stage_events(arr, n + 1), "set_stage_events")
-                api.forward_problem(prob, stream=s, force_path="decode", decode_kernel=DECODE_KERNEL)
+                api.forward_problem(prob, stream=s, force_path=FORCE, decode_kernel=DECODE_KERNEL)
             s.synchronize()
             times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(n)])
         res[T] = [statistics.median(t[i] for t in times) for i in range(n)]
@@ -502,10 +577,11 @@ def run_ours(args, world, rank, local):
     wall = time.perf_counter() - t_wall
     ck = clocks.stop()
 
-    # headline: all decode forwards of up to 16 tokens
+    # headline: all decode-size forwards (up to 16 tokens), each on the path
+    # the library's gate takes (or the forced one)
     step_bytes = step_tokens = 0
-    dev_ms = 0.0
-    kern_bytes, kern_ms = 0, 0.0
+    dev_ms = dec_ms = 0.0
+    kern_tot = {}   # kernel name -> [algorithmic bytes, summed median ms, launches per step]
     gpu_launches = 0
     per_wl = {}
     for wl in WORKLOADS:
@@ -514,17 +590,26 @@ def run_ours(args, world, rank, local):
         for T in wl.ts:
             D, nbytes = r["info"][T]
             med = statistics.median(r["per_T"][T])
-            kms = sum(r["kern"][T])
-            rows[str(T)] = {"distinct_experts": D, "routed_MB": nbytes / 1e6, "us": 1e3 * med,
+            path = r["paths"][T]
+            names = kernel_names(path, len(r["kern"][T]))
+            rows[str(T)] = {"distinct_experts": D, "routed_MB": nbytes / 1e6, "path": path, "us": 1e3 * med,
                             "GB_s": nbytes / (med / 1e3) / 1e9, "frac_of_hbm_peak": nbytes / (med / 1e3) / 1e9 / hbm,
-                            "kernels_us": [round(1e3 * x, 2) for x in r["kern"][T]],
+                            "kernels_us": {n: round(1e3 * x, 2) for n, x in zip(names, r["kern"][T])},
                             "launches": r["launches"][T]}
+            dmed = statistics.median(r["per_T_decode"][T])
+            if path != "decode":
+                rows[str(T)]["decode_path_us"] = 1e3 * dmed
+                rows[str(T)]["decode_path_GB_s"] = nbytes / (dmed / 1e3) / 1e9
             if T <= HEADLINE_T_MAX:
                 step_bytes += nbytes
                 step_tokens += T
                 dev_ms += sum(r["per_T"][T])
-                kern_bytes += algorithmic_bytes(wl.shape, T, D)
-                kern_ms += kms
+                dec_ms += sum(r["per_T_decode"][T])
+                for n, x in zip(names, r["kern"][T]):
+                    kt = kern_tot.setdefault(n, [0, 0.0, 0])
+                    kt[0] += kernel_bytes(n, wl.shape, T, D)
+                    kt[1] += x
+                    kt[2] += 1
                 gpu_launches += r["launches"][T] * args.steps
         head = [T for T in wl.ts if T <= HEADLINE_T_MAX]
         wb = sum(r["info"][T][1] for T in head)
@@ -532,7 +617,12 @@ def run_ours(args, world, rank, local):
         per_wl[wl.name] = {"workload": wl.desc, "l2": r["l2"], "GB_s_T_le_16": wb / (wms / 1e3) / 1e9,
                            "frac_of_hbm_peak_T_le_16": wb / (wms / 1e3) / 1e9 / hbm, "per_T": rows}
     value, tok_s, dev_ms_max = aggregate(step_bytes, step_tokens, args.steps, dev_ms, world)
-    kern_achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+    dec_value, _, _ = aggregate(step_bytes, step_tokens, args.steps, dec_ms, world)
+    # the dominant kernel: most summed device time over the headline forwards
+    dom = max(kern_tot, key=lambda n: kern_tot[n][1])
+    dom_bytes, dom_ms, dom_n = kern_tot[dom]
+    dom_achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    kern_all_ms = sum(v[1] for v in kern_tot.values())
 
     small = results["small"]
     sb = sum(small["info"][T][1] for T in WORKLOADS[0].ts)
@@ -562,8 +652,12 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "decode_kernel": DECODE_KERNEL,
                    "l2": {n: v["l2"] for n, v in per_wl.items()},
                    "launch": "CUDA graph replay per forward" if not args.no_graph else "eager",
-                   "path": "decode (forced)", "replicas": world},
+                   "path": "decode (forced)" if FORCE == "decode" else
+                   "the library's gate per call (W8A16 decode kernels, or the tcgen05 W8A8 grouped GEMMs)",
+                   "replicas": world},
         "frac_of_hbm_peak": value / hbm, "peak_source": src,
+        "value_decode_path": {"path": "the W8A16 decode kernels for every forward (forced)", "value": dec_value,
+                              "frac_of_hbm_peak": dec_value / hbm},
         "tok_per_s": tok_s,
         "workloads": per_wl,
         "value_small_other_l2": {"l2": alt_desc, "value": alt_value, "frac_of_hbm_peak": alt_value / hbm},
@@ -572,15 +666,8 @@ def run_ours(args, world, rank, local):
         "value_small_w8a8": {"decode_act": "e4m3 (W8A8), eager", "value": w8a8_value,
                              "frac_of_hbm_peak": w8a8_value / hbm,
                              "us": {str(T): 1e3 * statistics.median(small["w8a8"][T]) for T in WORKLOADS[0].ts}},
-        "roofline": {"kernel": "decode forward (all its kernels)" if DECODE_KERNEL == "chain" else "decode_fused",
-                     "bound": "hbm", "achieved": kern_achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": kern_achieved / hbm,
-                     "traffic": profile_traffic("decode_gemm1_kernel" if DECODE_KERNEL == "chain"
-                                                else "decode_fused_kernel", "decode_small_T16"),
-                     "algorithmic_bytes": "per forward: routed experts' e4m3 weights + valid bf16 scales + "
-                                          "activations read (2TH) + output written (2TH), over the summed device "
-                                          "time of the forward's kernels; summed over every headline forward",
-                     "peak_source": f"{src} hbm_gbs (copy, burst)"},
+        "roofline": roofline_entry(dom, dom_bytes, dom_ms, dom_n, args.steps, hbm, src,
+                                   share=dom_ms / kern_all_ms),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "moe_fp8_block_forward_hostio through the C ABI on the small-expert workload; page-locked "
@@ -707,7 +794,7 @@ def prefill_leg(dev, s, reps):
     return res
 
 
-PROFILE_CASES = ("decode_T16", "decode_T1", "prefill_T4096", "prefill_T16384")
+PROFILE_CASES = ("decode_T16", "decode_T1", "prefill_T4096", "prefill_T16384", "wide_T16", "wide_T1", "wide32_T4")
 # gate sweeps: layer -> token counts.  wide: T = round(32 r), r = T*k/E = 0.1 .. 1.0;
 # small: r = T*k/E = 0.0625 .. 1.0
 SWEEPS = {
@@ -773,6 +860,17 @@ def profile_case(name: str, reps: int = 3):
         T = int(name.split("_T")[1])
         prob = make_problems(dev)[T]
         path, H = "decode", SHAPE.H
+    elif name.startswith("wide"):
+        # the wide layer at a decode batch size, on the path the library's gate
+        # takes; wide32: the same expert shape with 32 experts (1.4 GB of
+        # weights, a case small enough for a full ncu capture)
+        T = int(name.split("_T")[1])
+        shp = syn.DECODE_WIDE if name.startswith("wide_") else syn.MoeShape(E=32, H=7168, I=2048, k=8)
+        w13, w13s, w2, w2s = syn.make_weights(shp, 0, dev)
+        ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, "softmax", step=T)
+        prob = dict(hidden=syn.make_hidden(T, shp.H, 0, dev, step=T), topk_ids=ids, topk_weights=w, w13=w13,
+                    w13_scale=w13s, w2=w2, w2_scale=w2s)
+        path, H = None, shp.H
     else:
         T = int(name.split("_T")[1])
         shp = syn.PREFILL
@@ -802,13 +900,17 @@ def main():
                     help="how forwards are kept from finding their weights in L2 (see the module docstring)")
     ap.add_argument("--gate-sweep", choices=tuple(SWEEPS), default=None,
                     help="time decode against prefill for r = T*k/E up to 1.0 on one layer (one JSON object)")
+    ap.add_argument("--path", choices=("auto", "decode"), default="auto",
+                    help="auto (default): each forward takes the path the library's gate chooses; decode: force "
+                         "the W8A16 decode kernels")
     ap.add_argument("--decode-kernel", choices=("chain", "fused"), default="chain",
                     help="decode kernels: four chained launches (default) or one persistent launch")
     ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
                     help="only run 3 forwards of one case (for ncu captures); prints no bench line")
     args = ap.parse_args()
-    global DECODE_KERNEL
+    global DECODE_KERNEL, FORCE
     DECODE_KERNEL = args.decode_kernel
+    FORCE = None if args.path == "auto" else "decode"
     if args.profile_case:
         profile_case(args.profile_case)
         return
