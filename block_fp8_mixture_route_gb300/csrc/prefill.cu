@@ -249,7 +249,7 @@ constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 // offsets from a 1024-aligned base; the same function on host and device).
 // Every tensor-copy destination or source is 128-byte aligned.
 struct PfLayout {
-  uint32_t out, ring_a, ring_w, xch, bars, mtp, total;
+  uint32_t out, ring_a, ring_w, xch, bars, mtp, cnt, total;
 };
 
 __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
@@ -268,13 +268,17 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   o = (o + 15u) & ~15u;
   L.mtp = o;
   o += 4u * (uint32_t)(E + 1);
+  L.cnt = o;   // GEMM2: the experts' slot counts (rows of each expert's last tile)
+  if (mode == 2) o += 4u * (uint32_t)E;
   L.total = o + 1024;   // slack for aligning the dynamic shared memory base
   return L;
 }
 
 // The tensor maps one GEMM uses: A rows, B rows (GEMM1: 3-D view of w13 so
 // one load brings a gate block and the matching up block), A scales (K-block
-// major), B scale records, and the output(s).
+// major), B scale records, and the output(s): GEMM1 h codes (o) and scales
+// (os); GEMM2 y rows as whole 128-row tiles (o) and as 8-row boxes of one
+// 64-column quarter (os), for tiles with few valid rows.
 struct PfMaps {
   CUtensorMap a, b, sa, sw, o, os;
 };
@@ -425,6 +429,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   float* ring_w = reinterpret_cast<float*>(base + L.ring_w);
   float* xch = reinterpret_cast<float*>(base + L.xch);
   int* mtp_s = reinterpret_cast<int*>(base + L.mtp);
+  int* cnt_s = reinterpret_cast<int*>(base + L.cnt);
   const uint32_t rank = blockIdx.x & 1u;
   uint8_t* outs = base + L.out;
   __shared__ int abort_flag;
@@ -458,6 +463,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // the tile tables, read once before any tensor-map traffic starts
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     mtp_s[i] = __ldg(p.rb.mtp + i);
+    if (MODE == 2 && i < E) cnt_s[i] = __ldg(p.rb.counts + i);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -703,7 +709,18 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         tc::fence_proxy_async_smem();
         stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
         if (issuer && !stop && tl.real) {
-          tc::tma_store_3d(&m.o, outs, 0, p0, nb * 4);
+          // rows past the expert's slots are padding no combine reads: a
+          // tile with at most 8 valid rows (the decode-size batches) stores
+          // one 8-row box per quarter, 4 KB instead of 64 KB.  More boxes
+          // would cost the issuing thread more than the bytes they save
+          // (a box takes about 135 cycles to issue, plus 1 per 128-B row).
+          const int valid = cnt_s[tl.e] - (tl.mi - mtp_s[tl.e]) * BM;
+          if (valid > 8) {
+            tc::tma_store_3d(&m.o, outs, 0, p0, nb * 4);
+          } else {
+            for (int q = 0; q < 4 && (nb * 4 + q) * 64 < a.H; ++q)
+              tc::tma_store_3d(&m.os, outs + q * (OUT2 / 4), 0, p0, nb * 4 + q);
+          }
           tc::bulk_commit();
         }
       }
@@ -859,13 +876,16 @@ static bool make_map_w13(CUtensorMap* m, const void* base, int E, int I, int H) 
 
 // ys [rows, H] bf16 viewed as [H/64][rows][64] (x = column within a 64-column
 // quarter, y = row, z = quarter): a box of 64 x 128 x 4 is 128 rows x 256
-// columns, stored from four 128-byte-swizzled 16 KB quarters.
-static bool make_map_ys(CUtensorMap* m, const void* base, uint64_t rows, int H) {
+// columns, stored from four 128-byte-swizzled 16 KB quarters; a box of
+// 64 x 8 x 1 is 8 rows of one quarter (one 1 KB swizzle atom of the staging
+// tile).
+static bool make_map_ys(CUtensorMap* m, const void* base, uint64_t rows, int H, uint32_t box_rows = 128,
+                        uint32_t box_quarters = 4) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {64, rows, (cuuint64_t)(H / 64)};
   const cuuint64_t strides[2] = {2 * (cuuint64_t)H, 128};
-  const cuuint32_t box[3] = {64, 128, 4};
+  const cuuint32_t box[3] = {64, box_rows, box_quarters};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -954,10 +974,9 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN / 2, true) &&
        make_map(&g2.sa, F32, 4, pb.hsT, nk2, R, 4 * R, 128, pf::KG, false) &&
        make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
-       make_map_ys(&g2.o, pb.ys, R, a.H);
+       make_map_ys(&g2.o, pb.ys, R, a.H) && make_map_ys(&g2.os, pb.ys, R, a.H, 8, 1);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   g2.a = g1.o;
-  g2.os = g2.o;
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
   const int sm1 = (int)pf_layout(1, ns1, a.E).total, sm2 = (int)pf_layout(2, ns2, a.E).total;
