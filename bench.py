@@ -642,6 +642,7 @@ def run_ours(args, world, rank, local):
     small.pop("feed")
     torch.cuda.empty_cache()
     prefill = prefill_leg(dev, s, max(5, args.steps)) if not args.no_prefill and world == 1 else None
+    host_exp = host_experts_leg(dev, s, 5) if not args.no_prefill and world == 1 else None
 
     if rank != 0:
         return
@@ -679,6 +680,7 @@ def run_ours(args, world, rank, local):
                 "call": "moe_fp8_block_forward_hostio through the C ABI on the small-expert workload; page-locked "
                         "host inputs read and the output written in place by the kernels"},
         "prefill": prefill,
+        "host_experts": host_exp,
         "gpu_launches": gpu_launches,
         "clocks": ck,
         "wall_s": wall,
@@ -731,6 +733,61 @@ def e2e_hostio(feed, s, steps, warmup):
 
 
 PREFILL_CASES = [(1024, "softmax"), (4096, "softmax"), (4096, "zipf"), (16384, "softmax"), (16384, "zipf")]
+HOST_EXPERT_TS = [1, 4, 16]
+
+
+def host_experts_leg(dev, s, reps):
+    """The small-expert layer with its expert banks in page-locked host
+    memory (moe_fp8_block_forward_host_experts): routed-weight GB/s per T,
+    against the host link's read rate measured here as a 1 GiB page-locked
+    host-to-device copy."""
+    shp = syn.DECODE_SMALL
+    dw = syn.make_weights(shp, 0, dev)
+    hw = []
+    for t in dw:
+        h = torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        hw.append(h)
+    del dw
+    torch.cuda.empty_cache()
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    link = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            dst.copy_(src, non_blocking=True)
+            e1.record(s)
+        s.synchronize()
+        link.append(src.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del src, dst
+    link_gbs = max(link)
+    rows, tb, tms = {}, 0, 0.0
+    for T in HOST_EXPERT_TS:
+        ids, w = syn.make_routing(T, shp.E, shp.k, 0, dev, "softmax", step=T)
+        x = syn.make_hidden(T, shp.H, 0, dev, step=T)
+        out = torch.empty(T, shp.H, dtype=torch.bfloat16, device=dev)
+        D, nbytes = routed_bytes(shp, ids)
+        times = []
+        for r in range(reps + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                api.moe_fp8_block_forward_host_experts(x, ids, w, hw[0], hw[1], hw[1].stride(1), hw[2], hw[3],
+                                                       hw[3].stride(1), out=out, stream=s)
+                e1.record(s)
+            s.synchronize()
+            if r >= 2:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        rows[str(T)] = {"distinct_experts": D, "us": 1e3 * ms, "GB_s": nbytes / (ms / 1e3) / 1e9}
+        tb += nbytes
+        tms += ms
+    value = tb / (tms / 1e3) / 1e9
+    return {"layer": "E=128 H=2048 I=512 top_k=8, expert banks in page-locked host memory", "value": value,
+            "unit": "GB/s", "link_GB_s": link_gbs, "frac_of_link": value / link_gbs,
+            "link": "1 GiB page-locked host-to-device copy, best of 3", "per_T": rows}
 
 
 def prefill_leg(dev, s, reps):
