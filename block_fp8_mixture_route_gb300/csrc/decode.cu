@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(DecodeArgs p) {
           q4[j >> 1] |= (uint32_t)q << (16 * (j & 1));
         }
         *reinterpret_cast<uint4*>(p.db.xh + (int64_t)t * a.H + i0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-        if ((threadIdx.x & 15) == 0) p.db.xs[(int64_t)t * (a.H / 128) + i0 / 128] = sc;
+        if ((threadIdx.x & 15) == 0) p.db.xs[(int64_t)t * ((a.H + 127) / 128) + i0 / 128] = sc;
         if (a.dbg_codes) {   // moe_fp8_block_forward_act_codes: the codes and scales as quantised here
           *reinterpret_cast<uint2*>(a.dbg_codes + (int64_t)t * a.H + i0) = make_uint2(q4[0], q4[1]);
-          if ((threadIdx.x & 15) == 0) a.dbg_scales[(int64_t)t * (a.H / 128) + i0 / 128] = sc;
+          if ((threadIdx.x & 15) == 0) a.dbg_scales[(int64_t)t * ((a.H + 127) / 128) + i0 / 128] = sc;
         }
       }
     }
@@ -322,17 +322,18 @@ __device__ __forceinline__ bool group_reduce(const Smem& S, int gr, int wq, int 
 // stage is held only for those loads, not for the MMAs.  The arrive has
 // release semantics and so orders the shared-memory reads before the
 // producer's next copy into the stage.
-template <int KW>
+template <int KW, bool RAG>
 __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8_t* brow, const uint8_t* xrow,
-                                                int kb0, bool has_w, bool has_x, float sgl, float sul,
+                                                int kb0, int K, bool has_w, bool has_x, float sgl, float sul,
                                                 const float (&sa)[2][4], uint64_t* empty_bar, int lane,
                                                 float (&acc)[4]) {
   uint4 wa[2 * KW], wb[2 * KW];
 #pragma unroll
   for (int i = 0; i < 2 * KW; ++i) {
     const int kk = (kb0 + (i >> 1)) * 128 + (i & 1) * 64;
-    wa[i] = has_w ? lds128(arow + kk) : make_uint4(0, 0, 0, 0);
-    wb[i] = has_w ? lds128(brow + kk) : make_uint4(0, 0, 0, 0);
+    const bool in = has_w && (!RAG || kk < K);   // RAG: a 64-wide chunk past K is zero
+    wa[i] = in ? lds128(arow + kk) : make_uint4(0, 0, 0, 0);
+    wb[i] = in ? lds128(brow + kk) : make_uint4(0, 0, 0, 0);
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
@@ -343,7 +344,7 @@ __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8
     for (int ch = 0; ch < 2; ++ch) {
       const int kk = (kb0 + j) * 128 + ch * 64;
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-      if (has_x) {
+      if (has_x && (!RAG || kk < K)) {
         x0 = lds128(xrow + 2 * kk);
         x1 = lds128(xrow + 2 * kk + 16);
       }
@@ -374,7 +375,7 @@ __device__ __forceinline__ void gemm1_unit_regs(const uint8_t* arow, const uint8
 // group's leader sums the partials and applies silu(gate)*up.
 // ACT8: W8A8 (the activation rows are e4m3 code values with per-group
 // scales); W8A16 otherwise.
-template <bool ACT8, bool BIAS>
+template <bool ACT8, bool BIAS, bool RAG>
 __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamCfg& cfg = p.c1;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
   // -------------------------------------------------- consumer warps
   const int gr = warp / kGW, wq = warp % kGW;
   const int g = lane >> 2, c = lane & 3;
-  const int nkb = a.H >> 7;
+  const int nkb = (a.H + 127) >> 7;   // RAG: the last K block is a single 64-wide chunk
   const int kb0 = wq * nkb / kGW, kb1 = (wq + 1) * nkb / kGW;
   const bool has_w = g < R;
   int m = 0, gen = 0;
@@ -567,10 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
         const int kw = kb1 - kb0;
         if (kw >= 1 && kw <= 4) {
           switch (kw) {
-            case 1: gemm1_unit_regs<1>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
-            case 2: gemm1_unit_regs<2>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
-            case 3: gemm1_unit_regs<3>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
-            default: gemm1_unit_regs<4>(arow, brow, xrow, kb0, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            case 1: gemm1_unit_regs<1, RAG>(arow, brow, xrow, kb0, a.H, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            case 2: gemm1_unit_regs<2, RAG>(arow, brow, xrow, kb0, a.H, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            case 3: gemm1_unit_regs<3, RAG>(arow, brow, xrow, kb0, a.H, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
+            default: gemm1_unit_regs<4, RAG>(arow, brow, xrow, kb0, a.H, has_w, has_x, sgl, sul, sa, &S.empty[slot], lane, acc); break;
           }
         } else {
 #pragma unroll 1
@@ -580,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
           for (int ch = 0; ch < 2; ++ch) {
             const int kk = kb * 128 + ch * 64;
             uint4 wa = make_uint4(0, 0, 0, 0), wb = wa, x0 = wa, x1 = wa;
-            if (has_w) {
+            const bool in = !RAG || kk < a.H;
+            if (has_w && in) {
               wa = lds128(arow + kk);
               wb = lds128(brow + kk);
             }
-            if (has_x) {
+            if (has_x && in) {
               x0 = lds128(xrow + 2 * kk);
               x1 = lds128(xrow + 2 * kk + 16);
             }
@@ -644,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm1_kernel(DecodeArgs p)
 // lo_0..lo_3]; y_slot = (C[:, slot] + C[:, 4 + slot]) * 2^s.  The four warps
 // of a group split K; the leader sums the partials and writes y times the
 // slot's top-k weight.
-template <int MT>
+template <int MT, bool RAG>
 __device__ void gemm2_unit_compute(const uint8_t* st, const uint8_t* hbrow, int I, int kb0, int kb1, int lane,
                                    bool has_b, float sl, float (&acc)[MT][4]) {
   const int g = lane >> 2, c = lane & 3;
@@ -660,6 +662,7 @@ __device__ void gemm2_unit_compute(const uint8_t* st, const uint8_t* hbrow, int 
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       const int kk = kb * 128 + ch * 64;
+      if (RAG && kk >= I) break;   // the last K block is a single 64-wide chunk
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
       if (has_b) {
         x0 = lds128(hbrow + 2 * kk);
@@ -683,7 +686,7 @@ __device__ void gemm2_unit_compute(const uint8_t* st, const uint8_t* hbrow, int 
 
 // The same with the warp's weight bytes first copied into registers and the
 // ring stage released before the MMAs (KW K blocks per warp, MT * KW <= 4).
-template <int MT, int KW>
+template <int MT, int KW, bool RAG>
 __device__ __forceinline__ void gemm2_unit_regs(const uint8_t* st, const uint8_t* hbrow, int I, int kb0, int lane,
                                                 bool has_b, float sl, uint64_t* empty_bar, float (&acc)[MT][4]) {
   const int g = lane >> 2, c = lane & 3;
@@ -692,9 +695,11 @@ __device__ __forceinline__ void gemm2_unit_regs(const uint8_t* st, const uint8_t
   for (int t = 0; t < MT; ++t)
 #pragma unroll
     for (int i = 0; i < 2 * KW; ++i) {
-      const uint8_t* ra = st + (t * 16 + g) * I + (kb0 + (i >> 1)) * 128 + (i & 1) * 64 + c * 16;
-      wa[t][i] = lds128(ra);
-      wb[t][i] = lds128(ra + 8 * I);
+      const int kk = (kb0 + (i >> 1)) * 128 + (i & 1) * 64;
+      const bool in = !RAG || kk < I;   // RAG: a 64-wide chunk past K is zero
+      const uint8_t* ra = st + (t * 16 + g) * I + kk + c * 16;
+      wa[t][i] = in ? lds128(ra) : make_uint4(0, 0, 0, 0);
+      wb[t][i] = in ? lds128(ra + 8 * I) : make_uint4(0, 0, 0, 0);
     }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
@@ -711,7 +716,7 @@ __device__ __forceinline__ void gemm2_unit_regs(const uint8_t* st, const uint8_t
     for (int ch = 0; ch < 2; ++ch) {
       const int kk = (kb0 + j) * 128 + ch * 64;
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-      if (has_b) {
+      if (has_b && (!RAG || kk < I)) {
         x0 = lds128(hbrow + 2 * kk);
         x1 = lds128(hbrow + 2 * kk + 16);
       }
@@ -730,7 +735,7 @@ __device__ __forceinline__ void gemm2_unit_regs(const uint8_t* st, const uint8_t
 // rows wq*16 ..) over the whole K, so there is no cross-warp sum and every
 // warp writes its own rows (used when a unit of 64 rows fits a stage).
 // Otherwise the warps split K and the group's first warp sums and writes.
-template <int MT, bool ROWS>
+template <int MT, bool ROWS, bool RAG>
 __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, int R2, int upe, int warp, int lane,
                                 int* abort_flag) {
   const LayerArgs& a = p.a;
@@ -738,7 +743,7 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
   const int NS = cfg.NS, SPP = cfg.SPP;
   const int gr = warp / kGW, wq = warp % kGW;
   const int g = lane >> 2, c = lane & 3;
-  const int nkb = a.I >> 7;
+  const int nkb = (a.I + 127) >> 7;   // RAG: the last K block is a single 64-wide chunk
   const int kb0 = ROWS ? 0 : wq * nkb / kGW, kb1 = ROWS ? nkb : (wq + 1) * nkb / kGW;
   const bool lead = ROWS || wq == 0;   // writes outputs
   // this warp's share of the h conversion
@@ -848,24 +853,24 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
         bool done = true;
         if constexpr (MT == 1) {
           switch (kw) {
-            case 1: gemm2_unit_regs<1, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
-            case 2: gemm2_unit_regs<1, 2>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
-            case 3: gemm2_unit_regs<1, 3>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
-            case 4: gemm2_unit_regs<1, 4>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 1: gemm2_unit_regs<1, 1, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 2: gemm2_unit_regs<1, 2, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 3: gemm2_unit_regs<1, 3, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 4: gemm2_unit_regs<1, 4, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
             default: done = false;
           }
         } else if constexpr (MT == 2) {
           switch (kw) {
-            case 1: gemm2_unit_regs<2, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
-            case 2: gemm2_unit_regs<2, 2>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 1: gemm2_unit_regs<2, 1, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
+            case 2: gemm2_unit_regs<2, 2, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc); break;
             default: done = false;
           }
         } else {
-          if (kw == 1) gemm2_unit_regs<MT, 1>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc);
+          if (kw == 1) gemm2_unit_regs<MT, 1, RAG>(st, hbrow, a.I, kb0, lane, has_b, sl, &S.empty[slot], acc);
           else done = false;
         }
         if (!done) {
-          gemm2_unit_compute<MT>(st, hbrow, a.I, kb0, kb1, lane, has_b, sl, acc);
+          gemm2_unit_compute<MT, RAG>(st, hbrow, a.I, kb0, kb1, lane, has_b, sl, acc);
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.empty[slot]);
         }
@@ -906,6 +911,7 @@ __device__ void gemm2_consumers(const DecodeArgs& p, const Smem& S, Walk& wk, in
   }
 }
 
+template <bool RAG>
 __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamCfg& cfg = p.c2;
@@ -998,12 +1004,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm2_kernel(DecodeArgs p)
   }
   pdl_wait();
   if (cfg.V == 0) {
-    gemm2_consumers<1, true>(p, S, wk, R2, upe, warp, lane, &abort_flag);
+    gemm2_consumers<1, true, RAG>(p, S, wk, R2, upe, warp, lane, &abort_flag);
   } else {
     switch (R2 / 16) {
-      case 1: gemm2_consumers<1, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
-      case 2: gemm2_consumers<2, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
-      default: gemm2_consumers<4, false>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+      case 1: gemm2_consumers<1, false, RAG>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+      case 2: gemm2_consumers<2, false, RAG>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
+      default: gemm2_consumers<4, false, RAG>(p, S, wk, R2, upe, warp, lane, &abort_flag); break;
     }
   }
 }
@@ -1151,15 +1157,19 @@ static bool config_gemm2(int H, int I, StreamCfg& c) {
   return false;
 }
 
+// Decode layer shapes: H and I multiples of 64 (a K dimension that is not a
+// multiple of 128 ends in one 64-wide chunk) and at least 128.
+static bool decode_shape(int H, int I) { return H % 64 == 0 && I % 64 == 0 && H >= 128 && I >= 128; }
+
 int decode_ring_stages(int H, int I) {
   StreamCfg c1, c2;
-  if (H % 128 || I % 128 || !config_gemm1(H, c1) || !config_gemm2(H, I, c2)) return 0;
+  if (!decode_shape(H, I) || !config_gemm1(H, c1) || !config_gemm2(H, I, c2)) return 0;
   return c1.NS;
 }
 
 bool decode_supported(int H, int I) {
   StreamCfg c1, c2;
-  return H % 128 == 0 && I % 128 == 0 && config_gemm1(H, c1) && config_gemm2(H, I, c2);
+  return decode_shape(H, I) && config_gemm1(H, c1) && config_gemm2(H, I, c2);
 }
 
 cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeBufs& db, uint32_t* status,
@@ -1184,11 +1194,18 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
   if ((err = set_max_smem((const void*)prep, (int)rsm))) return err;
   // the gate/up projection for the activation format, with the optional
   // MLP bias compiled in or out
-  auto gemm1 = a.act8 ? (a.b13 ? decode_gemm1_kernel<true, true> : decode_gemm1_kernel<true, false>)
-                      : (a.b13 ? decode_gemm1_kernel<false, true> : decode_gemm1_kernel<false, false>);
+  // H or I not a multiple of 128 (both multiples of 64): the kernels' last
+  // K block is one 64-wide chunk
+  const bool rag = a.H % 128 != 0 || a.I % 128 != 0;
+  auto gemm1 = rag ? (a.act8 ? (a.b13 ? decode_gemm1_kernel<true, true, true> : decode_gemm1_kernel<true, false, true>)
+                             : (a.b13 ? decode_gemm1_kernel<false, true, true> : decode_gemm1_kernel<false, false, true>))
+                   : (a.act8 ? (a.b13 ? decode_gemm1_kernel<true, true, false> : decode_gemm1_kernel<true, false, false>)
+                             : (a.b13 ? decode_gemm1_kernel<false, true, false>
+                                      : decode_gemm1_kernel<false, false, false>));
+  auto gemm2 = rag ? decode_gemm2_kernel<true> : decode_gemm2_kernel<false>;
   auto combine = a.b2 ? decode_combine_kernel<true> : decode_combine_kernel<false>;
   if ((err = set_max_smem((const void*)gemm1, p.c1.smem))) return err;
-  if ((err = set_max_smem((const void*)decode_gemm2_kernel, p.c2.smem)))
+  if ((err = set_max_smem((const void*)gemm2, p.c2.smem)))
     return err;
   // a shortened wait limit for this call (failure-detection test aid)
   if (a.dbg_wait_ns) {
@@ -1208,7 +1225,7 @@ cudaError_t launch_decode(const LayerArgs& a, const RouteBufs& rb, const DecodeB
                           "decode_gemm1")))
     return err;
   stage_mark(st, 2);
-  if ((err = launch_check(launch_pdl(decode_gemm2_kernel, dim3(sms), dim3(kThreads), p.c2.smem, st, pdl, p), st,
+  if ((err = launch_check(launch_pdl(gemm2, dim3(sms), dim3(kThreads), p.c2.smem, st, pdl, p), st,
                           "decode_gemm2")))
     return err;
   stage_mark(st, 3);

@@ -799,7 +799,7 @@ const char* moe_fp8_block_error_string(int code) {
     case MOE_OK: return "ok";
     case MOE_ERR_NULL: return "a required pointer or descriptor is NULL";
     case MOE_ERR_DTYPE: return "wrong element type";
-    case MOE_ERR_SHAPE: return "inconsistent shapes, or H / I not a multiple of 128";
+    case MOE_ERR_SHAPE: return "inconsistent shapes, or H / I not supported by the requested path";
     case MOE_ERR_ALIGN: return "a base pointer or row stride is not 16-byte aligned";
     case MOE_ERR_STRIDE: return "unsupported stride";
     case MOE_ERR_ALIAS: return "out overlaps an input";

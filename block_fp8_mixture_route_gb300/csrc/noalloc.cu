@@ -78,7 +78,7 @@ NaLayout na_layout(int64_t T, int k, int64_t H, int64_t I, int E) {
   L.xexp = take(4 * (size_t)T);
   L.h = take(4 * (size_t)(S * I));
   L.ybuf = take(4 * (size_t)(S * H));
-  L.xs = take(4 * (size_t)T * (size_t)(H / 128));
+  L.xs = take(4 * (size_t)T * (size_t)((H + 127) / 128));
   L.total = o;
   return L;
 }

@@ -179,8 +179,11 @@ typedef struct {
  *  stream        cudaStream_t.
  * H and I in [128, 8192], H a multiple of 64 and I of 16.  A layer whose
  * H or I is not a multiple of 128 ("ragged K", FreeToken PR #662, Tests:
- * the last 128-wide K block of a projection is partial) runs on the prefill
- * path; forcing the decode path on it returns MOE_ERR_SHAPE.  k in [1, 64];
+ * the last 128-wide K block of a projection is partial) runs on the decode
+ * path when both are multiples of 64 (its last K block is one 64-wide
+ * chunk), else on the prefill path, and forcing decode on it returns
+ * MOE_ERR_SHAPE; the single-kernel decode option and the host-resident
+ * entry point take multiples of 128 only.  k in [1, 64];
  * E in [1, 4096]; T*k <= 2^24.  Every
  * base pointer must be 16-byte aligned.  T == 0 is a no-op returning MOE_OK.
  */
