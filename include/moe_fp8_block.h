@@ -181,7 +181,9 @@ typedef struct {
  * H or I is not a multiple of 128 ("ragged K", FreeToken PR #662, Tests:
  * the last 128-wide K block of a projection is partial) runs on the decode
  * path when both are multiples of 64 (its last K block is one 64-wide
- * chunk), else on the prefill path, and forcing decode on it returns
+ * chunk), else on the prefill path.  Forcing decode on a layer the decode
+ * kernels do not take (such a ragged layer, or an I whose down-projection
+ * staging outgrows their shared memory, above about 2560) returns
  * MOE_ERR_SHAPE; the single-kernel decode option and the host-resident
  * entry point take multiples of 128 only.  k in [1, 64];
  * E in [1, 4096]; T*k <= 2^24.  Every
