@@ -604,23 +604,39 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       uint64_t acc0[32], acc1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc0[i] = acc1[i] = 0ull;
+      // promotion factors of the scale group's K blocks (g: gate / first 128
+      // columns, u: up / next 128, ub: up past `split`), element 0 = the
+      // current K block.  A group's factors are read together at its first K
+      // block and its ring entry released at once: between two K blocks a
+      // warp then touches shared memory only for the accumulator barrier,
+      // each access there waiting behind the copies and MMA operand reads.
+      float fg[KG], fu[KG], fub[KG];
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        if (*(volatile int*)&abort_flag) ok = false;
         const int sub = kb % KG;
         const int buf = it & 1;
-        if (sub == 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[gp.i], gp.ph));
-        float f0 = 0.f, f1 = 0.f, f1b = 0.f;
-        if (ok) {
-          const float sa = ring_a[gp.i * (SA_BYTES / 4) + sub * BM + row];
-          f0 = sa * ring_w[gp.i * 32 + sub * 4];
-          f1 = sa * ring_w[gp.i * 32 + sub * 4 + 1];
-          if (SPLIT) f1b = sa * ring_w[gp.i * 32 + sub * 4 + 2];
-        }
-        if (sub == KG - 1 || kb == nkb - 1) {
+        if (sub == 0) {
+          if (*(volatile int*)&abort_flag) ok = false;
+          ok = __all_sync(0xffffffffu, ok && mbar_wait(&sfull[gp.i], gp.ph));
+#pragma unroll
+          for (int j = 0; j < KG; ++j) {
+            const float sa = ok ? ring_a[gp.i * (SA_BYTES / 4) + j * BM + row] : 0.f;
+            const float4 w = ok ? reinterpret_cast<const float4*>(ring_w + gp.i * 32)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            fg[j] = sa * w.x;
+            fu[j] = sa * w.y;
+            fub[j] = SPLIT ? sa * w.z : 0.f;
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sempty[gp.i]);
           gp.next(NSG);
+        } else {
+#pragma unroll
+          for (int j = 0; j + 1 < KG; ++j) {
+            fg[j] = fg[j + 1];
+            fu[j] = fu[j + 1];
+            fub[j] = fub[j + 1];
+          }
         }
+        const float f0 = fg[0], f1 = fu[0], f1b = fub[0];
         ok = __all_sync(0xffffffffu, ok && mbar_wait(&tfull[buf], (uint32_t)(it >> 1) & 1));
         if (ok) {
           tc::fence_after_sync();
