@@ -294,6 +294,23 @@ __device__ __forceinline__ int expert_of_tile(const int* mtp, int E, int mi) {
   return lo;
 }
 
+// Barrier of the two epilogue warps of TMEM lane quarter q (warps ew and
+// ew ^ 4: named barrier 2 + q, 64 threads), and the same returning the OR
+// of `v` over those 64 threads.
+__device__ __forceinline__ void pair_sync(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
+__device__ __forceinline__ bool pair_sync_or(int q, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.u32 t, %2, 0;\n\t"
+      "bar.red.or.pred p, %1, 64, t;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(2 + q), "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 // Barrier among the 8 epilogue warps (named barrier 1).
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier, returning the OR of `v` over the 256 threads: every
@@ -581,6 +598,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int row = eq * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(eq * 32) << 16);
     const bool issuer = ew == 0 && lane == 0;
+    const bool pair_issuer = hf == 0 && lane == 0;   // GEMM1: one per lane quarter
     // first up column (within a tile) of the stacked bank's next scale block
     const int split = SPLIT ? 128 - a.I % 128 : 128;
     int it = 0;
@@ -684,10 +702,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           acc0[i] = f2pack(h0, h1);
           amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
         }
-        // the other half of the row's 128-group is held by warp ew ^ 4
+        // the other half of the row's 128-group is held by warp ew ^ 4: the
+        // two warps of lane quarter eq exchange, stage and store their 32
+        // rows by themselves (no barrier among all eight epilogue warps)
         xch[row * 2 + hf] = amax;
-        if (issuer) tc::bulk_wait_read0();   // the previous tile's store has left the staging tile
-        epi_sync();
+        if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
+        pair_sync(eq);
         amax = fmaxf(amax, xch[row * 2 + (1 - hf)]);
         const float sc = __fdiv_rn(amax, 448.0f);
         // code = e4m3(h * (1 / scale)): one IEEE reciprocal per group instead
@@ -709,10 +729,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
         if (hf == 0) reinterpret_cast<float*>(outs + OUT1)[row] = sc;
         tc::fence_proxy_async_smem();
-        stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
-        if (issuer && !stop && tl.real) {
-          tc::tma_store_2d(&m.o, outs, nb * 128, p0);
-          tc::tma_store_2d(&m.os, outs + OUT1, p0, nb);
+        stop = pair_sync_or(eq, !ok || *(volatile int*)&abort_flag);
+        if (pair_issuer && !stop && tl.real) {
+          tc::tma_store_2d(&m.o, outs + eq * 32 * 128, nb * 128, p0 + eq * 32);
+          tc::tma_store_2d(&m.os, outs + OUT1 + eq * 32 * 4, p0 + eq * 32, nb);
           tc::bulk_commit();
         }
       } else {
@@ -748,7 +768,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         break;
       }
     }
-    if (issuer) tc::bulk_wait0();
+    if (MODE == 1 ? pair_issuer : issuer) tc::bulk_wait0();
   }
   // ---------------------------------------------------------- teardown
   tc::fence_before_sync();
@@ -985,14 +1005,17 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
             make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
             make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, pf::KG, false) &&
             make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
-            make_map(&g1.o, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true) &&
-            make_map(&g1.os, F32, 4, pb.hsT, nk2, R, 4 * R, 128, 1, false);
+            make_map(&g1.o, U8, 1, pb.hq, R, a.I, a.I, 128, 32, true) &&
+            make_map(&g1.os, F32, 4, pb.hsT, nk2, R, 4 * R, 32, 1, false);
   ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN / 2, true) &&
        make_map(&g2.sa, F32, 4, pb.hsT, nk2, R, 4 * R, 128, pf::KG, false) &&
        make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
        make_map_ys(&g2.o, pb.ys, R, a.H) && make_map_ys(&g2.os, pb.ys, R, a.H, 8, 1);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
-  g2.a = g1.o;
+  // GEMM2 reads the h codes in whole 128-row tiles (GEMM1 stores them in
+  // 32-row boxes, one per pair of epilogue warps)
+  if (!make_map(&g2.a, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true))
+    return note_error(cudaErrorInvalidValue, "tensor map encode");
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
   const int sm1 = (int)pf_layout(1, ns1, a.E).total, sm2 = (int)pf_layout(2, ns2, a.E).total;
