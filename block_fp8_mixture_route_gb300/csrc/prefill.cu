@@ -240,7 +240,7 @@ constexpr int SW_BYTES = KG * 16;       // weight scale records of one group: [K
 constexpr int NEPI = 8;            // epilogue warps (two per TMEM lane quarter)
 constexpr int THREADS = 32 * (2 + NEPI);
 constexpr int OUT1 = BM * 128;     // GEMM1 staging: 128 rows x 128 h codes (+ 128 fp32 scales)
-constexpr int OUT2 = BM * 256 * 2; // GEMM2 staging: 128 rows x 256 bf16, four 64-column quarters
+constexpr int OUT2 = BM * 256 * 2; // GEMM2 staging: 128 rows x 256 bf16, pair-major (32 rows x four 64-column quarters)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 }  // namespace pf
@@ -277,8 +277,9 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
 // The tensor maps one GEMM uses: A rows, B rows (GEMM1: 3-D view of w13 so
 // one load brings a gate block and the matching up block), A scales (K-block
 // major), B scale records, and the output(s): GEMM1 h codes (o) and scales
-// (os); GEMM2 y rows as whole 128-row tiles (o) and as 8-row boxes of one
-// 64-column quarter (os), for tiles with few valid rows.
+// (os); GEMM2 y rows as 32-row boxes of four 64-column quarters (o: one
+// pair of epilogue warps' rows) and as 8-row boxes of one quarter (os), for
+// pairs with few valid rows.
 struct PfMaps {
   CUtensorMap a, b, sa, sw, o, os;
 };
@@ -307,23 +308,6 @@ __device__ __forceinline__ bool pair_sync_or(int q, bool v) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
       : "r"(2 + q), "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-
-// Barrier among the 8 epilogue warps (named barrier 1).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// The same barrier, returning the OR of `v` over the 256 threads: every
-// epilogue thread gets the same answer, so all leave the tile loop together.
-__device__ __forceinline__ bool epi_sync_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, 256, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
       : "memory");
   return r != 0;
 }
@@ -597,8 +581,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int hf = ew >> 2;                  // which 64-column half of each 128-column block
     const int row = eq * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(eq * 32) << 16);
-    const bool issuer = ew == 0 && lane == 0;
-    const bool pair_issuer = hf == 0 && lane == 0;   // GEMM1: one per lane quarter
+    const bool pair_issuer = hf == 0 && lane == 0;   // one per lane quarter
     // first up column (within a tile) of the stacked bank's next scale block
     const int split = SPLIT ? 128 - a.I % 128 : 128;
     int it = 0;
@@ -736,28 +719,31 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           tc::bulk_commit();
         }
       } else {
-        // quarter q of the staging tile = output columns nb*256 + 64 q ..,
-        // 16 KB each; one store writes all four (quarters past H are clipped)
-        if (issuer) tc::bulk_wait_read0();   // the previous tile's store has left the staging tile
-        epi_sync();
-        stage_bf16_row64(outs + hf * (OUT2 / 4), row, acc0);
-        if (has1) stage_bf16_row64(outs + (2 + hf) * (OUT2 / 4), row, acc1);
+        // staging tile pair-major: the 32 rows of lane quarter eq, then
+        // column quarter q (output columns nb*256 + 64 q ..), 4 KB each, so
+        // that the two warps of the quarter stage and store their rows by
+        // themselves, one box of 32 rows x 256 columns (quarters past H are
+        // clipped by the tensor map)
+        uint8_t* pst = outs + eq * (OUT2 / 4);
+        if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
+        pair_sync(eq);
+        stage_bf16_row64(pst + hf * (OUT2 / 16), row & 31, acc0);
+        if (has1) stage_bf16_row64(pst + (2 + hf) * (OUT2 / 16), row & 31, acc1);
         tc::fence_proxy_async_smem();
-        stop = epi_sync_or(!ok || *(volatile int*)&abort_flag);
-        if (issuer && !stop && tl.real) {
+        stop = pair_sync_or(eq, !ok || *(volatile int*)&abort_flag);
+        if (pair_issuer && !stop && tl.real) {
           // rows past the expert's slots are padding no combine reads: a
-          // tile with at most 8 valid rows (the decode-size batches) stores
-          // one 8-row box per quarter, 4 KB instead of 64 KB.  More boxes
-          // would cost the issuing thread more than the bytes they save
-          // (a box takes about 135 cycles to issue, plus 1 per 128-B row).
-          const int valid = cnt_s[tl.e] - (tl.mi - mtp_s[tl.e]) * BM;
+          // pair whose rows are all padding stores nothing, one with at most
+          // 8 valid rows (the decode-size batches) one 8-row box per quarter
+          const int valid = cnt_s[tl.e] - (tl.mi - mtp_s[tl.e]) * BM - eq * 32;
           if (valid > 8) {
-            tc::tma_store_3d(&m.o, outs, 0, p0, nb * 4);
-          } else {
+            tc::tma_store_3d(&m.o, pst, 0, p0 + eq * 32, nb * 4);
+            tc::bulk_commit();
+          } else if (valid > 0) {
             for (int q = 0; q < 4 && (nb * 4 + q) * 64 < a.H; ++q)
-              tc::tma_store_3d(&m.os, outs + q * (OUT2 / 4), 0, p0, nb * 4 + q);
+              tc::tma_store_3d(&m.os, pst + q * (OUT2 / 16), 0, p0 + eq * 32, nb * 4 + q);
+            tc::bulk_commit();
           }
-          tc::bulk_commit();
         }
       }
       if (stop) {
@@ -768,7 +754,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         break;
       }
     }
-    if (MODE == 1 ? pair_issuer : issuer) tc::bulk_wait0();
+    if (pair_issuer) tc::bulk_wait0();
   }
   // ---------------------------------------------------------- teardown
   tc::fence_before_sync();
@@ -911,10 +897,10 @@ static bool make_map_w13(CUtensorMap* m, const void* base, int E, int I, int H) 
 }
 
 // ys [rows, H] bf16 viewed as [H/64][rows][64] (x = column within a 64-column
-// quarter, y = row, z = quarter): a box of 64 x 128 x 4 is 128 rows x 256
-// columns, stored from four 128-byte-swizzled 16 KB quarters; a box of
-// 64 x 8 x 1 is 8 rows of one quarter (one 1 KB swizzle atom of the staging
-// tile).
+// quarter, y = row, z = quarter), stored from 128-byte-swizzled staging
+// quarters of 32 rows: a box of 64 x 32 x 4 is 32 rows x 256 columns (four
+// 4 KB quarters); a box of 64 x 8 x 1 is 8 rows of one quarter (one 1 KB
+// swizzle atom).
 static bool make_map_ys(CUtensorMap* m, const void* base, uint64_t rows, int H, uint32_t box_rows = 128,
                         uint32_t box_quarters = 4) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -1010,7 +996,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   ok = ok && make_map(&g2.b, U8, 1, a.w2, (uint64_t)a.E * a.H, a.I, a.I, 128, pf::BN / 2, true) &&
        make_map(&g2.sa, F32, 4, pb.hsT, nk2, R, 4 * R, 128, pf::KG, false) &&
        make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
-       make_map_ys(&g2.o, pb.ys, R, a.H) && make_map_ys(&g2.os, pb.ys, R, a.H, 8, 1);
+       make_map_ys(&g2.o, pb.ys, R, a.H, 32, 4) && make_map_ys(&g2.os, pb.ys, R, a.H, 8, 1);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
   // GEMM2 reads the h codes in whole 128-row tiles (GEMM1 stores them in
   // 32-row boxes, one per pair of epilogue warps)
