@@ -1161,6 +1161,11 @@ static bool config_gemm2(int H, int I, StreamCfg& c) {
 // multiple of 128 ends in one 64-wide chunk) and at least 128.
 static bool decode_shape(int H, int I) { return H % 64 == 0 && I % 64 == 0 && H >= 128 && I >= 128; }
 
+int decode_unit_rows(int H) {
+  StreamCfg c;
+  return config_gemm1(H, c) ? c.R : 0;
+}
+
 int decode_ring_stages(int H, int I) {
   StreamCfg c1, c2;
   if (!decode_shape(H, I) || !config_gemm1(H, c1) || !config_gemm2(H, I, c2)) return 0;

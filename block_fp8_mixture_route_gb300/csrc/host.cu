@@ -382,10 +382,15 @@ int run_forward(const LayerArgs& a, float ratio, int force, cudaStream_t st, boo
 
 // Gate.  With a caller ratio: decode while T*k <= E*ratio (the rule of the
 // fp8-moe-gather page, environment-variable table).  Default, from sweeps of
-// both paths on GB300: decode while T*k <= E and the decode gate/up stream
-// gets at least 4 ring stages.  With H = 2048 (5 stages) decode was faster
-// at every T*k/E up to 1; with H = 7168 (3 stages: the 14 KB activation
-// rows crowd the ring) prefill was faster from T*k/E = 0.1 up.
+// both paths on GB300 (median forward us, decode / prefill): decode while
+// T*k <= E, the decode gate/up stream gets at least 4 ring stages, and its
+// units are the full 8 row pairs (H <= 2048) or the batch routes at most 8
+// slots.  E128 H2048 I512 (8 row pairs, 5 stages): decode faster at every
+// T*k/E up to 1 (T=8 61 / 69, T=16 86 / 93).  E256 H2560 I640 with hot
+// experts (4 row pairs, 8 stages): decode faster only at T=1 (37 / 42),
+// prefill from T=2 on (T=8 94 / 76, T=32 441 / 105).  E256 H7168 I2048
+// (3 stages: the 14 KB activation rows crowd the ring): prefill from
+// T*k/E = 0.03 on.
 int choose_path(const LayerArgs& a, float ratio, int force) {
   if (force != MOE_PATH_NONE) return force;
   if (ratio > 0.f) {
@@ -393,7 +398,8 @@ int choose_path(const LayerArgs& a, float ratio, int force) {
     return gathered && decode_supported(a.H, a.I) ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
   }
   const bool gathered = (double)a.T * a.k <= (double)a.E;
-  return gathered && decode_ring_stages(a.H, a.I) >= 4 ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  const bool units = decode_unit_rows(a.H) >= 8 || (int64_t)a.T * a.k <= 8;
+  return gathered && units && decode_ring_stages(a.H, a.I) >= 4 ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
 // Device address of page-locked host memory that kernels can read and write

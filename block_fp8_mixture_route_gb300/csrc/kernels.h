@@ -141,6 +141,9 @@ cudaError_t launch_widen(const uint8_t* codes, int64_t n, float* out, cudaStream
 bool decode_supported(int H, int I);
 // Ring stages the decode gate/up stream gets for this shape (0 if unsupported).
 int decode_ring_stages(int H, int I);
+// Row pairs of one decode gate/up unit (ring stage) for hidden width H: 8
+// while 8 whole rows of gate and of up fit 16 KiB each (H <= 2048).
+int decode_unit_rows(int H);
 
 // The fused decode kernel (one launch per forward) handles up to this many
 // slots, when its shared-memory layout fits; larger slot counts take the

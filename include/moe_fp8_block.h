@@ -25,10 +25,13 @@
  *   decode  (W8A16): with a caller gate ratio, taken while T*k <= E*ratio
  *     (fp8-moe-gather page, environment-variable table, where the ratio is
  *     0.4).  By default, from measurements of both paths on GB300: taken
- *     while T*k <= E and the layer's hidden rows leave the decode weight
+ *     while T*k <= E, the layer's hidden rows leave the decode weight
  *     stream at least 4 shared-memory ring stages (H = 2048: yes; H = 7168:
- *     no, where the prefill path streams faster).  bf16 activations, e4m3
- *     weights widened in registers, fp32 accumulation and fp32 h.
+ *     no, where the prefill path streams faster), and its units are whole
+ *     8-row-pair blocks (H <= 2048) or the batch routes at most 8 slots
+ *     (H = 2560 with hot experts: decode only at T*k = 8).  bf16
+ *     activations, e4m3 weights widened in registers, fp32 accumulation and
+ *     fp32 h.
  *   prefill (W8A8): activations quantised per token per 128 columns with a
  *     dynamic scale amax/448 (fp8-moe-gather page, "Affects": dynamic
  *     activation scales), grouped FP8 tensor-core GEMMs, h quantised the same

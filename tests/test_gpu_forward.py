@@ -124,6 +124,16 @@ def test_default_gate(cuda_lib):
         assert api.moe_fp8_block_last_path() == 1
 
 
+def test_default_gate_unit_rows(cuda_lib):
+    """Default gate on a layer whose decode gate/up units hold 4 row pairs
+    (H = 2560, hot experts): decode only while the batch routes at most 8
+    slots, the grouped GEMMs from there on (measured faster from T = 2)."""
+    api.forward_problem(problem(syn.PADDED_SKEWED, 1, routing="hot"))
+    assert api.moe_fp8_block_last_path() == 1
+    api.forward_problem(problem(syn.PADDED_SKEWED, 8, routing="hot"))
+    assert api.moe_fp8_block_last_path() == 2
+
+
 def test_gate_ratio_option(cuda_lib):
     """A caller ratio applies the page's rule: decode while T*k <= E*ratio."""
     prob = problem(syn.DECODE_SMALL, 7)   # 56 slots > 128 * 0.4
