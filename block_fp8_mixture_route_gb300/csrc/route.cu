@@ -117,7 +117,11 @@ cudaError_t launch_route(const int32_t* ids, int S, int E, const RouteBufs& rb, 
   const int G = scratch ? route_chunks(S) : 1;
   cudaError_t err;
   if (G <= 1) {
-    const int nt = route_threads(E);
+    // few slots: a CTA of about one warp per 32 slots keeps the per-warp
+    // counters and the block-wide scans short
+    int nt = route_threads(E);
+    const int want = (S + 31) / 32 * 32;
+    if (want < nt) nt = want < 128 ? 128 : want;
     const size_t sm = route_smem_bytes(E, nt);
     if ((err = set_max_smem((const void*)route_kernel, (int)sm)))
       return err;
