@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     moe_fp8_block_abi_version,
     moe_fp8_block_act_quant,
     moe_fp8_block_device_status,
+    moe_fp8_block_default_path,
     moe_fp8_block_forward,
     moe_fp8_block_forward_act_codes,
     moe_fp8_block_forward_bias,

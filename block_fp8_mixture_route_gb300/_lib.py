@@ -31,7 +31,7 @@ EXPORTS = [
     "moe_fp8_block_forward_decode_noalloc", "moe_fp8_block_noalloc_status", "moe_fp8_block_forward_act_codes",
     "moe_fp8_block_forward_host_experts",
     "moe_fp8_block_route", "moe_fp8_block_act_quant", "moe_fp8_block_widen_e4m3",
-    "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path",
+    "moe_fp8_block_reserve", "moe_fp8_block_device_status", "moe_fp8_block_last_path", "moe_fp8_block_default_path",
     "moe_fp8_block_last_launches", "moe_fp8_block_set_stage_events", "moe_fp8_block_abi_version", "moe_fp8_block_last_error_detail", "moe_fp8_block_error_string",
     "moe_fp8_block_release",
 ]
@@ -97,6 +97,7 @@ def load(path: str = LIB_PATH):
         lib.moe_fp8_block_device_status.argtypes = [vp, P(ctypes.c_uint32)]
         lib.moe_fp8_block_noalloc_status.argtypes = [vp, P(ctypes.c_uint32)]
         lib.moe_fp8_block_last_path.argtypes = []
+        lib.moe_fp8_block_default_path.argtypes = [i64, i32, i32, i64, i64]
         lib.moe_fp8_block_last_launches.argtypes = []
         lib.moe_fp8_block_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.moe_fp8_block_abi_version.argtypes = []

@@ -255,6 +255,15 @@ def moe_fp8_block_last_path() -> int:
     return _lib.load().moe_fp8_block_last_path()
 
 
+def moe_fp8_block_default_path(T: int, k: int, E: int, H: int, I: int) -> int:
+    """The path (1 decode, 2 prefill) the default gate takes for a call of
+    this shape; raises on arguments no path takes.  Host only."""
+    rc = _lib.load().moe_fp8_block_default_path(T, k, E, H, I)
+    if rc < 0:
+        check(rc, "moe_fp8_block_default_path")
+    return rc
+
+
 def moe_fp8_block_last_launches() -> int:
     return _lib.load().moe_fp8_block_last_launches()
 

@@ -783,6 +783,18 @@ int moe_fp8_block_device_status(void* stream, uint32_t* status) {
 
 int moe_fp8_block_last_path(void) { return g_last_path; }
 
+int moe_fp8_block_default_path(int64_t T, int32_t k, int32_t E, int64_t H, int64_t I) {
+  if (T < 0 || k < 1 || k > 64 || E < 1 || E > 4096) return MOE_ERR_ARG;
+  if (!layer_shape_ok(H, I) || H > 8192 || I > 8192) return MOE_ERR_SHAPE;
+  LayerArgs a{};
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.H = (int)H;
+  a.I = (int)I;
+  return choose_path(a, 0.f, MOE_PATH_NONE);
+}
+
 int moe_fp8_block_last_launches(void) { return g_last_launches; }
 
 int moe_fp8_block_set_stage_events(void* const* events, int n) {

@@ -416,6 +416,14 @@ int moe_fp8_block_last_path(void);
  * thread enqueued. */
 int moe_fp8_block_last_launches(void);
 
+/* The path the default gate (no caller ratio, no forced path) takes for a
+ * forward call of T tokens, top_k = k, E experts, hidden width H and
+ * intermediate width I: MOE_PATH_DECODE or MOE_PATH_PREFILL; the rule is
+ * the one in "Paths" above.  Host only, needs no device.  Returns
+ * MOE_ERR_ARG for T < 0, k outside 1..64 or E outside 1..4096, and
+ * MOE_ERR_SHAPE for H, I that no path takes. */
+int moe_fp8_block_default_path(int64_t T, int32_t k, int32_t E, int64_t H, int64_t I);
+
 /* Profiling aid.  The next forward call on this host thread records
  * events[i] (cudaEvent_t, created by the caller) on its stream before its
  * i-th kernel launch and one more event after its last launch, for as many

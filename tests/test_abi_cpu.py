@@ -220,3 +220,32 @@ def test_ragged_shape_rules(lib, H, I, ok):
         assert rc in (-8, -10)          # past every argument check, then no device
     else:
         assert rc == -3
+
+
+@pytest.mark.parametrize("T,k,E,H,I,path", [
+    (16, 8, 128, 2048, 512, 1),    # small layer: decode up to T*k = E
+    (17, 8, 128, 2048, 512, 2),
+    (1, 8, 256, 2560, 640, 1),     # 4-row-pair decode units: decode only up to 8 slots
+    (2, 8, 256, 2560, 640, 2),
+    (8, 8, 256, 2560, 640, 2),
+    (1, 8, 256, 7168, 2048, 2),    # 3 decode ring stages: always the grouped GEMMs
+    (1, 4, 16, 320, 192, 1),       # ragged, multiples of 64: decode
+    (1, 4, 16, 320, 176, 2),       # I not a multiple of 64: prefill only
+    (0, 8, 128, 2048, 512, 1),
+])
+def test_default_path_rule(lib, T, k, E, H, I, path):
+    """The default gate as a host-only query: decode while T*k <= E, the
+    decode gate/up ring keeps at least 4 stages and its units are whole
+    8-row-pair blocks (H <= 2048) or the batch routes at most 8 slots."""
+    assert lib.moe_fp8_block_default_path(T, k, E, H, I) == path
+    assert api.moe_fp8_block_default_path(T, k, E, H, I) == path
+
+
+def test_default_path_argument_errors(lib):
+    err_arg, err_shape = -9, -3   # MOE_ERR_ARG, MOE_ERR_SHAPE
+    assert lib.moe_fp8_block_default_path(-1, 8, 128, 2048, 512) == err_arg
+    assert lib.moe_fp8_block_default_path(1, 0, 128, 2048, 512) == err_arg
+    assert lib.moe_fp8_block_default_path(1, 8, 0, 2048, 512) == err_arg
+    assert lib.moe_fp8_block_default_path(1, 8, 128, 160, 512) == err_shape
+    with pytest.raises(RuntimeError):
+        api.moe_fp8_block_default_path(1, 8, 128, 160, 512)
