@@ -136,17 +136,18 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def profile_traffic(kernel: str):
+def profile_traffic(kernel: str, workload: str = None):
     """(DRAM bytes of one launch, captured workload, its algorithmic bytes)
-    of `kernel` from the committed ncu summary profiles/traffic.txt, if the
-    source file it was captured from has not changed since (else None).
+    of `kernel` (on `workload` if given, else its first line) from the
+    committed ncu summary profiles/traffic.txt, if the source file it was
+    captured from has not changed since (else None).
     Line format: kernel workload dram_bytes algorithmic_bytes source sha256[:16]."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     for line in open(path):
         f = line.split()
-        if len(f) < 6 or line.startswith("#") or f[0] != kernel:
+        if len(f) < 6 or line.startswith("#") or f[0] != kernel or (workload and f[1] != workload):
             continue
         src = os.path.join(ROOT, "block_fp8_mixture_route_gb300", "csrc", f[4])
         if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == f[5]:
@@ -852,6 +853,17 @@ def prefill_leg(dev, s, reps):
                          zip(("route", "act_quant_permute", "gemm1", "gemm2", "combine"), stage)},
             "gemm1_tflops": g1f / (stage[2] / 1e3) / 1e12, "gemm2_tflops": g2f / (stage[3] / 1e3) / 1e12,
         }
+        if (T, routing) == (4096, "softmax"):
+            # DRAM bytes of one launch of each GEMM from the committed ncu
+            # capture of this case, beside the launch's algorithmic bytes
+            # (null once the kernel source has changed since the capture)
+            tr = {}
+            for name, key in (("prefill_gemm_kernel<1>", "gemm1"), ("prefill_gemm_kernel<2>", "gemm2")):
+                t = profile_traffic(name, "prefill_T4096")
+                alg = kernel_bytes(name, shp, T, shp.E)
+                tr[key] = {"dram_bytes": t[0] if t else None, "algorithmic_bytes": alg,
+                           "ratio": t[0] / alg if t else None}
+            res[f"T{T}_{routing}"]["traffic"] = tr
     res["fp8_peak_tflops"] = fp8_peak
     res["peak_source"] = f"2 x {src} bf16_tflops (burst)"
     return res
