@@ -43,7 +43,7 @@ __device__ __forceinline__ float4 lds_f4(const void* p) {
 }
 
 
-// Bounded wait by lane 0 of a warp; the verdict is returned on all lanes.
+// Bounded wait by lane 0 of a warp; its outcome is returned on all lanes.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
   int ok = 1;
   if (lane == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
