@@ -601,6 +601,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         bg2 = __ldg(reinterpret_cast<const float2*>(br));
         bu2 = __ldg(reinterpret_cast<const float2*>(br + a.I));
       }
+      // GEMM1: the expert's slot count (which of the tile's rows are not
+      // padding), read now so that the load completes during the K loop
+      const int cnt_e = MODE == 1 ? __ldg(p.rb.counts + tl.e) : cnt_s[tl.e];
+      // rows of this pair of warps (lane quarter eq) before the expert's
+      // padding: a pair with none skips its tile end (decode-size batches
+      // have at most 8 valid rows per tile, all in quarter 0)
+      const int pvalid = cnt_e - (tl.mi - mtp_s[tl.e]) * BM - eq * 32;
+      const bool pany = tl.real && pvalid > 0;
       // this thread's 64 columns of each 128-column block, as 32 pairs
       uint64_t acc0[32], acc1[32];
 #pragma unroll
@@ -662,58 +670,60 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       bool stop;
       if (MODE == 1) {
-        // h = silu(gate) * up for this thread's 64 columns of the 128-block.
-        // silu(g) = g / (1 + e^-g) with the fast exponential and division:
-        // an IEEE division here takes its slow path whenever e^-g overflows
-        // (every strongly negative gate value), which made this loop cost
-        // more than the whole K loop of a tile.  h feeds a quantiser, and
-        // both approximations are within a few fp32 ulps (a denominator
-        // past 2^126 gives 0, the limit silu takes there anyway).
-        float amax = 0.f;
+        if (pany) {
+          // h = silu(gate) * up for this thread's 64 columns of the 128-block.
+          // silu(g) = g / (1 + e^-g) with the fast exponential and division:
+          // an IEEE division here takes its slow path whenever e^-g overflows
+          // (every strongly negative gate value), which made this loop cost
+          // more than the whole K loop of a tile.  h feeds a quantiser, and
+          // both approximations are within a few fp32 ulps (a denominator
+          // past 2^126 gives 0, the limit silu takes there anyway).
+          float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float g0 = f2lo(acc0[i]), g1 = f2hi(acc0[i]);
-          float u0 = f2lo(acc1[i]), u1 = f2hi(acc1[i]);
-          if (BIAS) {
-            g0 += __shfl_sync(0xffffffffu, bg2.x, i);
-            g1 += __shfl_sync(0xffffffffu, bg2.y, i);
-            u0 += __shfl_sync(0xffffffffu, bu2.x, i);
-            u1 += __shfl_sync(0xffffffffu, bu2.y, i);
+          for (int i = 0; i < 32; ++i) {
+            float g0 = f2lo(acc0[i]), g1 = f2hi(acc0[i]);
+            float u0 = f2lo(acc1[i]), u1 = f2hi(acc1[i]);
+            if (BIAS) {
+              g0 += __shfl_sync(0xffffffffu, bg2.x, i);
+              g1 += __shfl_sync(0xffffffffu, bg2.y, i);
+              u0 += __shfl_sync(0xffffffffu, bu2.x, i);
+              u1 += __shfl_sync(0xffffffffu, bu2.y, i);
+            }
+            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+            acc0[i] = f2pack(h0, h1);
+            amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
           }
-          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-          acc0[i] = f2pack(h0, h1);
-          amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
-        }
-        // the other half of the row's 128-group is held by warp ew ^ 4: the
-        // two warps of lane quarter eq exchange, stage and store their 32
-        // rows by themselves (no barrier among all eight epilogue warps)
-        xch[row * 2 + hf] = amax;
-        if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
-        pair_sync(eq);
-        amax = fmaxf(amax, xch[row * 2 + (1 - hf)]);
-        const float sc = __fdiv_rn(amax, 448.0f);
-        // code = e4m3(h * (1 / scale)): one IEEE reciprocal per group instead
-        // of a division per value
-        const float inv = sc != 0.f ? __frcp_rn(sc) : 0.f;
-        uint8_t* orow = outs + row * 128;
+          // the other half of the row's 128-group is held by warp ew ^ 4: the
+          // two warps of lane quarter eq exchange, stage and store their 32
+          // rows by themselves (no barrier among all eight epilogue warps)
+          xch[row * 2 + hf] = amax;
+          if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
+          pair_sync(eq);
+          amax = fmaxf(amax, xch[row * 2 + (1 - hf)]);
+          const float sc = __fdiv_rn(amax, 448.0f);
+          // code = e4m3(h * (1 / scale)): one IEEE reciprocal per group instead
+          // of a division per value
+          const float inv = sc != 0.f ? __frcp_rn(sc) : 0.f;
+          uint8_t* orow = outs + row * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t w[4];
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int b = 8 * i + 2 * u;   // pairs b, b + 1 = values 16 i + 4 u .. + 3
-            const uint32_t c01 = f32x2_to_e4m3x2(f2lo(acc0[b]) * inv, f2hi(acc0[b]) * inv);
-            const uint32_t c23 = f32x2_to_e4m3x2(f2lo(acc0[b + 1]) * inv, f2hi(acc0[b + 1]) * inv);
-            w[u] = c01 | (c23 << 16);
+            for (int u = 0; u < 4; ++u) {
+              const int b = 8 * i + 2 * u;   // pairs b, b + 1 = values 16 i + 4 u .. + 3
+              const uint32_t c01 = f32x2_to_e4m3x2(f2lo(acc0[b]) * inv, f2hi(acc0[b]) * inv);
+              const uint32_t c23 = f32x2_to_e4m3x2(f2lo(acc0[b + 1]) * inv, f2hi(acc0[b + 1]) * inv);
+              w[u] = c01 | (c23 << 16);
+            }
+            const int c = hf * 4 + i;
+            *reinterpret_cast<uint4*>(orow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          const int c = hf * 4 + i;
-          *reinterpret_cast<uint4*>(orow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (hf == 0) reinterpret_cast<float*>(outs + OUT1)[row] = sc;
+          tc::fence_proxy_async_smem();
         }
-        if (hf == 0) reinterpret_cast<float*>(outs + OUT1)[row] = sc;
-        tc::fence_proxy_async_smem();
         stop = pair_sync_or(eq, !ok || *(volatile int*)&abort_flag);
-        if (pair_issuer && !stop && tl.real) {
+        if (pair_issuer && !stop && pany) {
           tc::tma_store_2d(&m.o, outs + eq * 32 * 128, nb * 128, p0 + eq * 32);
           tc::tma_store_2d(&m.os, outs + OUT1 + eq * 32 * 4, p0 + eq * 32, nb);
           tc::bulk_commit();
@@ -725,17 +735,20 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         // themselves, one box of 32 rows x 256 columns (quarters past H are
         // clipped by the tensor map)
         uint8_t* pst = outs + eq * (OUT2 / 4);
-        if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
-        pair_sync(eq);
-        stage_bf16_row64(pst + hf * (OUT2 / 16), row & 31, acc0);
-        if (has1) stage_bf16_row64(pst + (2 + hf) * (OUT2 / 16), row & 31, acc1);
-        tc::fence_proxy_async_smem();
+        if (pany) {
+          if (pair_issuer) tc::bulk_wait_read0();   // the pair's previous stores have left its staging rows
+          pair_sync(eq);
+          stage_bf16_row64(pst + hf * (OUT2 / 16), row & 31, acc0);
+          if (has1) stage_bf16_row64(pst + (2 + hf) * (OUT2 / 16), row & 31, acc1);
+          tc::fence_proxy_async_smem();
+        }
         stop = pair_sync_or(eq, !ok || *(volatile int*)&abort_flag);
-        if (pair_issuer && !stop && tl.real) {
+        if (pair_issuer && !stop && pany) {
           // rows past the expert's slots are padding no combine reads: a
-          // pair whose rows are all padding stores nothing, one with at most
-          // 8 valid rows (the decode-size batches) one 8-row box per quarter
-          const int valid = cnt_s[tl.e] - (tl.mi - mtp_s[tl.e]) * BM - eq * 32;
+          // pair whose rows are all padding stages and stores nothing, one
+          // with at most 8 valid rows (the decode-size batches) stores one
+          // 8-row box per quarter
+          const int valid = pvalid;
           if (valid > 8) {
             tc::tma_store_3d(&m.o, pst, 0, p0 + eq * 32, nb * 4);
             tc::bulk_commit();
