@@ -264,7 +264,7 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   L.xch = o;
   o += pf::BM * 2 * 4;
   L.bars = o;
-  o += (2 * ns + 2 * pf::NSG + 4) * 8 + 16;
+  o += (2 * (ns + (mode == 2)) + 2 * pf::NSG + 4) * 8 + 16;   // GEMM2: one spare stage's barriers
   o = (o + 15u) & ~15u;
   L.mtp = o;
   o += 4u * (uint32_t)(E + 1);
@@ -419,9 +419,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const LayerArgs& a = p.a;
   const int E = a.E;
   const PfLayout L = pf_layout(MODE, ns, E);
+  // GEMM2 lays out one more stage's barriers: when no expert has more than
+  // 32 slots (every decode-size batch), only the first pair of epilogue
+  // warps ever stages output rows, and the other 48 KB of the staging tile
+  // serve as one more ring stage
+  const int nsb = ns + (MODE == 2 ? 1 : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);
-  uint64_t* empty = full + ns;
-  uint64_t* sfull = empty + ns;
+  uint64_t* empty = full + nsb;
+  uint64_t* sfull = empty + nsb;
   uint64_t* sempty = sfull + NSG;
   uint64_t* tfull = sempty + NSG;
   uint64_t* tempty = tfull + 2;
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < ns; ++i) {
+    for (int i = 0; i < nsb; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -462,15 +467,23 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   }
   pdl_wait();
   // the tile tables, read once before any tensor-map traffic starts
+  int over32 = 0;   // some expert has more than 32 slots
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     mtp_s[i] = __ldg(p.rb.mtp + i);
-    if (MODE == 2 && i < E) cnt_s[i] = __ldg(p.rb.counts + i);
+    if (MODE == 2 && i < E) {
+      cnt_s[i] = __ldg(p.rb.counts + i);
+      over32 |= cnt_s[i] > 32;
+    }
   }
   tc::fence_before_sync();
-  __syncthreads();
+  over32 = __syncthreads_or(over32);
   tc::fence_after_sync();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
+  // ring stages of this launch (the same in every CTA: all read the same
+  // counts) and the shared memory of stage i
+  const int nse = MODE == 2 && !over32 ? nsb : ns;
+  auto stage_at = [&](int i) -> uint8_t* { return i < ns ? base + i * STAGE : outs + OUT2 / 4; };
 
   const int K = MODE == 1 ? a.H : a.I;
   const int nkb = (int)(((unsigned)K + BK - 1) / BK);   // a partial last K block reads zeros past K
@@ -506,16 +519,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       for (int t = bx; t < total && ok; t += gx, ++ti) {
         const PairTile tl = pair_tile(mtp_s, E, NBT, t, rank);
         const int p0 = tl.mi * BM;
-        for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(ns)) {
+        for (int kb = 0; kb < nkb; ++kb, ++n_main, sp.next(nse)) {
           if (!issue_groups(ti * ngpt + kb / KG + 1 + LEAD_G)) {
             ok = false;
             break;
           }
-          if (n_main >= ns && !mbar_wait(&empty[sp.i], sp.ph ^ 1u)) {
+          if (n_main >= nse && !mbar_wait(&empty[sp.i], sp.ph ^ 1u)) {
             ok = false;
             break;
           }
-          uint8_t* st = base + sp.i * STAGE;
+          uint8_t* st = stage_at(sp.i);
           // A: the tile's 128 rows, 16 KB; B: the column block's 256 rows, 32 KB
           mbar_arrive_expect_tx(&full[sp.i], STAGE);
           tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
@@ -535,8 +548,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         abort_flag = 1;
         raise_status(p.status, MOE_STATUS_TIMEOUT);
         // let the copies already issued land before the CTA goes away
-        for (int i = n_main > ns ? n_main - ns : 0; i < n_main; ++i)
-          mbar_wait(&full[i % ns], (uint32_t)(i / ns) & 1);
+        for (int i = n_main > nse ? n_main - nse : 0; i < n_main; ++i)
+          mbar_wait(&full[i % nse], (uint32_t)(i / nse) & 1);
         for (int i = n_g > NSG ? n_g - NSG : 0; i < n_g; ++i) mbar_wait(&sfull[i % NSG], (uint32_t)(i / NSG) & 1);
       }
     }
@@ -548,7 +561,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       RingPos sp;
       bool ok = true;
       for (int t = bx; t < total && ok; t += gx) {
-        for (int kb = 0; kb < nkb; ++kb, ++it, sp.next(ns)) {
+        for (int kb = 0; kb < nkb; ++kb, ++it, sp.next(nse)) {
           const int buf = it & 1;
           if (!mbar_wait(&full[sp.i], sp.ph) ||
               (it >= 2 && !mbar_wait(&tempty[buf], (uint32_t)((it >> 1) - 1) & 1))) {
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint8_t* st = base + sp.i * STAGE;
+          const uint8_t* st = stage_at(sp.i);
           const uint32_t d = tmem + buf * BN;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
@@ -572,7 +585,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       // the last commits must land before TMEM is released and the CTA goes away
       if (it > 0) mbar_wait(&tfull[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1);
-      for (int i = it > ns ? it - ns : 0; i < it; ++i) mbar_wait(&empty[i % ns], (uint32_t)(i / ns) & 1);
+      for (int i = it > nse ? it - nse : 0; i < it; ++i) mbar_wait(&empty[i % nse], (uint32_t)(i / nse) & 1);
     }
   } else {
     // -------------------------------------------------- epilogue warps
