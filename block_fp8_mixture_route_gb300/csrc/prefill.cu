@@ -473,6 +473,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     if (MODE == 2 && i < E) {
       cnt_s[i] = __ldg(p.rb.counts + i);
       over32 |= cnt_s[i] > 32;
+    } else if (i < E) {
+      over32 |= __ldg(p.rb.counts + i) > 32;
     }
   }
   tc::fence_before_sync();
@@ -496,6 +498,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     // -------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
+      // weights: evict-first when the batch routes at most 32 slots to every
+      // expert and at most 64 experts (each weight block is then read by one
+      // CTA, once) so that L2 keeps the activation codes and outputs; wide
+      // layer T = 1 / 4: 95 -> 90 / 260 -> 256 us.  With more experts
+      // (T = 16 of the wide layer) evict-first measured no better.
+      const uint64_t polb = over32 || mtp_s[E] > 64 ? pol : l2_policy_evict_first();
       const int my_tiles = total > bx ? (total - bx + gx - 1) / gx : 0;
       const int n_groups = my_tiles * ngpt;
       int n_main = 0, n_g = 0;          // operand stages / scale groups issued
@@ -533,13 +541,13 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           mbar_arrive_expect_tx(&full[sp.i], STAGE);
           tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
           if (MODE == 1) {   // gate block nb, then up block nb
-            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], pol);
+            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], polb);
             tc::tma_load_3d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
-                            pol);
+                            polb);
           } else {           // rows nb * 256 .. + 255 of the expert's down projection
-            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], pol);
+            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], polb);
             tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128, &full[sp.i],
-                            pol);
+                            polb);
           }
         }
         if (*(volatile int*)&abort_flag) ok = false;
