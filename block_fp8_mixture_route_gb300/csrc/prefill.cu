@@ -499,11 +499,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
       // weights: evict-first when the batch routes at most 32 slots to every
-      // expert and at most 64 experts (each weight block is then read by one
-      // CTA, once) so that L2 keeps the activation codes and outputs; wide
-      // layer T = 1 / 4: 95 -> 90 / 260 -> 256 us.  With more experts
-      // (T = 16 of the wide layer) evict-first measured no better.
-      const uint64_t polb = over32 || mtp_s[E] > 64 ? pol : l2_policy_evict_first();
+      // expert (each weight block is then read by one CTA, once) so that L2
+      // keeps the activation codes and outputs; the gate/up projection only
+      // up to 64 experts (wide layer T = 1 / 4: 95 -> 90 / 260 -> 256 us; at
+      // T = 16, 109 experts, it was slower), the down projection always
+      // (T = 16: 781 -> 775 us)
+      const uint64_t polb = over32 || (MODE == 1 && mtp_s[E] > 64) ? pol : l2_policy_evict_first();
       const int my_tiles = total > bx ? (total - bx + gx - 1) / gx : 0;
       const int n_groups = my_tiles * ngpt;
       int n_main = 0, n_g = 0;          // operand stages / scale groups issued
