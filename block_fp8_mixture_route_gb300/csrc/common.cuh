@@ -112,6 +112,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Start streaming `bytes` (a multiple of 16, 16-byte aligned) of global
+// memory into L2; no completion, no shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch --
 // Wait until the preceding kernel in the stream has completed and its
 // memory is visible (no-op when the kernel was launched without the

@@ -119,12 +119,6 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 // warps 0-7 and 9).
 __device__ __forceinline__ void finish_sync() { asm volatile("bar.sync 1, 288;" ::: "memory"); }
 
-// Start streaming `bytes` (a multiple of 16, 16-byte aligned) of global
-// memory into L2; no completion, no shared memory.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // 16 bytes of weights that are read once: not kept in L1.
 __device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
   uint4 v;

@@ -465,22 +465,28 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
     tc::tmem_relinquish();
   }
-  pdl_wait();
+  // GEMM1 waits for the activation codes before anything else.  GEMM2 can
+  // start only once every GEMM1 CTA has passed that wait, so the route
+  // kernel's tile tables are complete by then: GEMM2 reads them (through
+  // L2) and prefetches its first tile's weights before waiting for the h
+  // codes, and its CTAs placed on SMs that GEMM1 has already left stream
+  // weights during GEMM1's last wave.
+  if (MODE == 1) pdl_wait();
+  auto ld_table = [](const int* q) { return MODE == 2 ? __ldcg(q) : __ldg(q); };
   // the tile tables, read once before any tensor-map traffic starts
   int over32 = 0;   // some expert has more than 32 slots
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-    mtp_s[i] = __ldg(p.rb.mtp + i);
+    mtp_s[i] = ld_table(p.rb.mtp + i);
     if (MODE == 2 && i < E) {
-      cnt_s[i] = __ldg(p.rb.counts + i);
+      cnt_s[i] = ld_table(p.rb.counts + i);
       over32 |= cnt_s[i] > 32;
     } else if (i < E) {
-      over32 |= __ldg(p.rb.counts + i) > 32;
+      over32 |= ld_table(p.rb.counts + i) > 32;
     }
   }
   tc::fence_before_sync();
   over32 = __syncthreads_or(over32);
   tc::fence_after_sync();
-  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   // ring stages of this launch (the same in every CTA: all read the same
   // counts) and the shared memory of stage i
@@ -493,6 +499,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const int NBT = MODE == 1 ? (int)(((unsigned)a.I + 127) / 128) : (a.H + BN - 1) / BN;
   const int total = mtp_s[E] * ((NBT + 1) >> 1);   // pair tiles
   const int bx = (int)blockIdx.x >> 1, gx = (int)gridDim.x >> 1;   // pair index, pairs
+  if (MODE == 2) {
+    // the first tile's rows of the down projection, contiguous in w2 (a hint:
+    // the ring's loads read them again)
+    if (threadIdx.x == 0 && bx < total) {
+      const PairTile tl = pair_tile(mtp_s, E, NBT, bx, rank);
+      if (tl.real) {
+        const int r0 = tl.nb * BN, nr = min(BN, a.H - r0);
+        const uint8_t* src = a.w2 + ((int64_t)tl.e * a.H + r0) * a.I;
+        for (int c = 0; c < nr; c += 32)
+          prefetch_l2(src + (int64_t)c * a.I, (uint32_t)(min(32, nr - c) * a.I));
+      }
+    }
+    pdl_wait();
+  }
+  pdl_trigger();
 
   if (warp == 0) {
     // -------------------------------------------------- TMA producer
