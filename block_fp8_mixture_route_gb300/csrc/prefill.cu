@@ -230,11 +230,18 @@ constexpr int BK = 128;            // K block (bytes = e4m3 elements)
 constexpr int A_BYTES = BM * BK;   // 16 KiB
 constexpr int B_BYTES = BN * BK;   // 32 KiB
 constexpr int STAGE = A_BYTES + B_BYTES;
+// A stage of a launch whose tiles have at most 32 valid rows (no expert has
+// more than 32 slots: every decode-size batch): the A tile's first 32 rows
+// only, then B.  The MMA still reads 128 A rows; rows 32..127 come from the
+// stage's B bytes and yield accumulator rows that lie in the expert's
+// padding, which no epilogue warp finishes.
+constexpr int A_SMALL = 32 * BK;   // 4 KiB
+constexpr int STAGE_S = A_SMALL + B_BYTES;
 constexpr int KG = 4;              // K blocks per scale group (one scale-ring entry)
 constexpr int NSG = 6;             // scale-ring entries
 constexpr int LEAD_G = 3;          // groups the scale loads run ahead of the operand loads
                                    // (NSG - LEAD_G >= 3: the epilogue is never more than
-                                   // 2 accumulators + 4 stages, i.e. under 3 groups, behind)
+                                   // 2 accumulators + 5 stages, i.e. under 3 groups, behind)
 constexpr int SA_BYTES = BM * KG * 4;   // activation scales of one group: [KG][BM] fp32
 constexpr int SW_BYTES = KG * 16;       // weight scale records of one group: [KG][4] fp32
 constexpr int NEPI = 8;            // epilogue warps (two per TMEM lane quarter)
@@ -244,6 +251,9 @@ constexpr int OUT2 = BM * 256 * 2; // GEMM2 staging: 128 rows x 256 bf16, pair-m
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kSmemMax = 232448;   // opt-in shared memory per CTA
 }  // namespace pf
+
+// Stages of STAGE_S bytes that fit where ns stages of STAGE bytes lie.
+__host__ __device__ inline int pf_small_stages(int ns) { return ns * pf::STAGE / pf::STAGE_S; }
 
 // Shared-memory layout of prefill_gemm_kernel<mode> with ns stages (byte
 // offsets from a 1024-aligned base; the same function on host and device).
@@ -264,7 +274,9 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   L.xch = o;
   o += pf::BM * 2 * 4;
   L.bars = o;
-  o += (2 * (ns + (mode == 2)) + 2 * pf::NSG + 4) * 8 + 16;   // GEMM2: one spare stage's barriers
+  // barriers of the most stages a launch uses: the stages of STAGE_S bytes
+  // in the ring, and in GEMM2 one more in the staging tile
+  o += (2 * (pf_small_stages(ns) + (mode == 2)) + 2 * pf::NSG + 4) * 8 + 16;
   o = (o + 15u) & ~15u;
   L.mtp = o;
   o += 4u * (uint32_t)(E + 1);
@@ -274,14 +286,15 @@ __host__ __device__ inline PfLayout pf_layout(int mode, int ns, int E) {
   return L;
 }
 
-// The tensor maps one GEMM uses: A rows, B rows (GEMM1: 3-D view of w13 so
-// one load brings a gate block and the matching up block), A scales (K-block
-// major), B scale records, and the output(s): GEMM1 h codes (o) and scales
-// (os); GEMM2 y rows as 32-row boxes of four 64-column quarters (o: one
-// pair of epilogue warps' rows) and as 8-row boxes of one quarter (os), for
-// pairs with few valid rows.
+// The tensor maps one GEMM uses: A rows (a: 128-row boxes; a32: 32-row
+// boxes, for launches whose tiles have at most 32 valid rows), B rows
+// (GEMM1: 3-D view of w13 so one load brings a gate block and the matching
+// up block), A scales (K-block major), B scale records, and the output(s):
+// GEMM1 h codes (o) and scales (os); GEMM2 y rows as 32-row boxes of four
+// 64-column quarters (o: one pair of epilogue warps' rows) and as 8-row
+// boxes of one quarter (os), for pairs with few valid rows.
 struct PfMaps {
-  CUtensorMap a, b, sa, sw, o, os;
+  CUtensorMap a, a32, b, sa, sw, o, os;
 };
 
 // Largest expert e with mtp[e] <= mi (the expert owning 128-row tile mi).
@@ -404,9 +417,10 @@ struct RingPos {
 // 10 warps per CTA: warp 0 issues tensor-map loads, warp 1 owns TMEM and
 // issues the MMAs, warps 2..9 promote, finish and store.  CTA pair c (CTAs
 // 2c and 2c + 1) takes pair tiles c, c + pairs, ... (pair_tile).  A stage
-// holds a 128-row A tile and a 256-row B tile, both loaded by the CTA itself;
-// it is free again once this CTA's MMAs have read it (one commit arrives on
-// its empty barrier).
+// holds a 128-row A tile (its first 32 rows when no expert has more than 32
+// slots) and a 256-row B tile, both loaded by the CTA itself; it is free
+// again once this CTA's MMAs have read it (one commit arrives on its empty
+// barrier).
 // BIAS: GEMM1 adds the optional MLP gate/up bias.  SPLIT: GEMM1 of a layer
 // whose I is not a multiple of 128, where each up tile's columns take two
 // weight scales (see repack_weight_scales).
@@ -419,11 +433,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const LayerArgs& a = p.a;
   const int E = a.E;
   const PfLayout L = pf_layout(MODE, ns, E);
-  // GEMM2 lays out one more stage's barriers: when no expert has more than
-  // 32 slots (every decode-size batch), only the first pair of epilogue
-  // warps ever stages output rows, and the other 48 KB of the staging tile
-  // serve as one more ring stage
-  const int nsb = ns + (MODE == 2 ? 1 : 0);
+  // barriers of the most stages a launch can use: when no expert has more
+  // than 32 slots (every decode-size batch) the ring holds stages of
+  // STAGE_S bytes, and in GEMM2, where only the first pair of epilogue warps
+  // then ever stages output rows, the other 48 KB of the staging tile serve
+  // as one more stage
+  const int nsb = pf_small_stages(ns) + (MODE == 2 ? 1 : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);
   uint64_t* empty = full + nsb;
   uint64_t* sfull = empty + nsb;
@@ -457,6 +472,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     fence_mbar_init();
     abort_flag = 0;
     tc::prefetch_tensormap(&m.a);
+    tc::prefetch_tensormap(&m.a32);
     tc::prefetch_tensormap(&m.b);
     tc::prefetch_tensormap(&m.sa);
     tc::prefetch_tensormap(&m.sw);
@@ -489,9 +505,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // ring stages of this launch (the same in every CTA: all read the same
-  // counts) and the shared memory of stage i
-  const int nse = MODE == 2 && !over32 ? nsb : ns;
-  auto stage_at = [&](int i) -> uint8_t* { return i < ns ? base + i * STAGE : outs + OUT2 / 4; };
+  // counts), their size, B's offset in a stage, and the shared memory of
+  // stage i.  With at most 32 valid rows per tile the stages hold 32 A rows:
+  // 5 stages of 32 KB of weights instead of 4 (GEMM1; GEMM2 4 + 1 instead
+  // of 3 + 1)
+  const bool small = !over32;
+  const int nring = small ? pf_small_stages(ns) : ns;
+  const int nse = nring + (MODE == 2 && small ? 1 : 0);
+  const uint32_t sbytes = small ? STAGE_S : STAGE;
+  const int boff = small ? A_SMALL : A_BYTES;
+  auto stage_at = [&](int i) -> uint8_t* { return i < nring ? base + i * sbytes : outs + OUT2 / 4; };
 
   const int K = MODE == 1 ? a.H : a.I;
   const int nkb = (int)(((unsigned)K + BK - 1) / BK);   // a partial last K block reads zeros past K
@@ -559,16 +582,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             break;
           }
           uint8_t* st = stage_at(sp.i);
-          // A: the tile's 128 rows, 16 KB; B: the column block's 256 rows, 32 KB
-          mbar_arrive_expect_tx(&full[sp.i], STAGE);
-          tc::tma_load_2d(st, &m.a, kb * BK, p0, &full[sp.i], pol);
+          // A: the tile's 128 rows, 16 KB (or its first 32, 4 KB); B: the
+          // column block's 256 rows, 32 KB
+          mbar_arrive_expect_tx(&full[sp.i], sbytes);
+          tc::tma_load_2d(st, small ? &m.a32 : &m.a, kb * BK, p0, &full[sp.i], pol);
           if (MODE == 1) {   // gate block nb, then up block nb
-            tc::tma_load_3d(st + A_BYTES, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], polb);
-            tc::tma_load_3d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
+            tc::tma_load_3d(st + boff, &m.b, kb * BK, tl.nb * 128, 2 * tl.e, &full[sp.i], polb);
+            tc::tma_load_3d(st + boff + B_BYTES / 2, &m.b, kb * BK, tl.nb * 128, 2 * tl.e + 1, &full[sp.i],
                             polb);
           } else {           // rows nb * 256 .. + 255 of the expert's down projection
-            tc::tma_load_2d(st + A_BYTES, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], polb);
-            tc::tma_load_2d(st + A_BYTES + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128, &full[sp.i],
+            tc::tma_load_2d(st + boff, &m.b, kb * BK, tl.e * a.H + tl.nb * BN, &full[sp.i], polb);
+            tc::tma_load_2d(st + boff + B_BYTES / 2, &m.b, kb * BK, tl.e * a.H + tl.nb * BN + 128, &full[sp.i],
                             polb);
           }
         }
@@ -603,7 +627,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           const uint32_t d = tmem + buf * BN;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            tc::mma_f8(d, tc::sw128_desc(st + k * 32), tc::sw128_desc(st + A_BYTES + k * 32), idesc, k > 0);
+            tc::mma_f8(d, tc::sw128_desc(st + k * 32), tc::sw128_desc(st + boff + k * 32), idesc, k > 0);
           tc::commit(&empty[sp.i]);
           tc::commit(&tfull[buf]);
         }
@@ -1044,6 +1068,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   PfMaps g1, g2;
   bool ok = make_map(&g1.a, U8, 1, pb.xq, R, a.H, a.H, 128, 128, true) &&
+            make_map(&g1.a32, U8, 1, pb.xq, R, a.H, a.H, 128, 32, true) &&
             make_map_w13(&g1.b, a.w13, a.E, a.I, a.H) &&
             make_map(&g1.sa, F32, 4, pb.xsT, nk1, R, 4 * R, 128, pf::KG, false) &&
             make_map(&g1.sw, F32, 4, pb.wsc13, (uint64_t)a.E * nk1, 4 * np1, 16 * np1, 4, pf::KG, false) &&
@@ -1054,9 +1079,11 @@ cudaError_t launch_prefill(const LayerArgs& a, const RouteBufs& rb, const Prefil
        make_map(&g2.sw, F32, 4, pb.wsc2, (uint64_t)a.E * nk2, 4 * np2, 16 * np2, 4, pf::KG, false) &&
        make_map_ys(&g2.o, pb.ys, R, a.H, 32, 4) && make_map_ys(&g2.os, pb.ys, R, a.H, 8, 1);
   if (!ok) return note_error(cudaErrorInvalidValue, "tensor map encode");
-  // GEMM2 reads the h codes in whole 128-row tiles (GEMM1 stores them in
-  // 32-row boxes, one per pair of epilogue warps)
-  if (!make_map(&g2.a, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true))
+  // GEMM2 reads the h codes in 128-row tiles, or 32-row ones when no tile
+  // has more valid rows (GEMM1 stores them in 32-row boxes, one per pair of
+  // epilogue warps)
+  if (!make_map(&g2.a, U8, 1, pb.hq, R, a.I, a.I, 128, 128, true) ||
+      !make_map(&g2.a32, U8, 1, pb.hq, R, a.I, a.I, 128, 32, true))
     return note_error(cudaErrorInvalidValue, "tensor map encode");
   const int ns1 = pick_stages(1, a.E), ns2 = pick_stages(2, a.E);
   if (!ns1 || !ns2) return note_error(cudaErrorNotSupported, "prefill shared memory");
