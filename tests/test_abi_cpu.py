@@ -249,3 +249,66 @@ def test_default_path_argument_errors(lib):
     assert lib.moe_fp8_block_default_path(1, 8, 128, 160, 512) == err_shape
     with pytest.raises(RuntimeError):
         api.moe_fp8_block_default_path(1, 8, 128, 160, 512)
+
+
+C_CHECK = r"""
+#include "moe_fp8_block.h"
+#include <stddef.h>
+#include <stdio.h>
+#include <string.h>
+
+#define CHECK(c) do { if (!(c)) { printf("failed: %s\n", #c); return 1; } } while (0)
+
+int main(void) {
+  static const int codes[] = {MOE_OK, MOE_ERR_NULL, MOE_ERR_DTYPE, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_STRIDE,
+                              MOE_ERR_ALIAS, MOE_ERR_CAPTURE_GROW, MOE_ERR_CUDA, MOE_ERR_ARG, MOE_ERR_DEVICE};
+  static uint16_t host[4 * 256];
+  moe_tensor t;
+  size_t i;
+  CHECK(moe_fp8_block_abi_version() == MOE_FP8_BLOCK_ABI_VERSION);
+  for (i = 0; i < sizeof(codes) / sizeof(codes[0]); ++i) {
+    const char* s = moe_fp8_block_error_string(codes[i]);
+    CHECK(s != NULL && strlen(s) > 0);
+  }
+  CHECK(moe_fp8_block_default_path(1, 8, 128, 2048, 512) == MOE_PATH_DECODE);
+  CHECK(moe_fp8_block_default_path(1, 8, 256, 7168, 2048) == MOE_PATH_PREFILL);
+  CHECK(moe_fp8_block_default_path(-1, 8, 128, 2048, 512) == MOE_ERR_ARG);
+  memset(&t, 0, sizeof(t));
+  t.data = host;
+  t.ndim = 2;
+  t.dtype = MOE_BF16;
+  t.shape[0] = 4;
+  t.shape[1] = 256;
+  t.stride[0] = 256;
+  t.stride[1] = 1;
+  CHECK(moe_fp8_block_forward(NULL, &t, &t, &t, &t, 2, &t, &t, 1, &t, NULL) == MOE_ERR_NULL);
+  CHECK(moe_fp8_block_last_path() == MOE_PATH_NONE);
+  moe_fp8_block_release();
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c(lib):
+    """The header compiles as strict C99 (and as C++), and a C program links
+    the library and calls it without Python: the boundary is a C ABI."""
+    import shutil
+    import subprocess
+    from block_fp8_mixture_route_gb300 import build
+    gcc, gxx = shutil.which("gcc"), shutil.which("g++")
+    if not gcc:
+        pytest.skip("no C compiler")
+    out_dir = os.path.join(build.BUILD, "abi_c_check")
+    os.makedirs(out_dir, exist_ok=True)
+    src, exe = os.path.join(out_dir, "check.c"), os.path.join(out_dir, "check")
+    with open(src, "w") as f:
+        f.write(C_CHECK)
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER), src,
+                    "-L", libdir, "-lmoe_fp8_block", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+    if gxx:
+        subprocess.run([gxx, "-std=c++11", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", "c++",
+                        "-I", os.path.dirname(HEADER), src], check=True)
