@@ -285,6 +285,16 @@ int main(void) {
   CHECK(moe_fp8_block_last_path() == MOE_PATH_NONE);
   moe_fp8_block_release();
   printf("ok\n");
+  printf("moe_tensor %u data %u ndim %u dtype %u shape %u stride %u\n", (unsigned)sizeof(moe_tensor),
+         (unsigned)offsetof(moe_tensor, data), (unsigned)offsetof(moe_tensor, ndim),
+         (unsigned)offsetof(moe_tensor, dtype), (unsigned)offsetof(moe_tensor, shape),
+         (unsigned)offsetof(moe_tensor, stride));
+  printf("moe_options %u gate_ratio %u force_path %u decode_act %u decode_kernel %u debug_wait_timeout_us %u "
+         "debug_drop_stage %u reserved %u\n", (unsigned)sizeof(moe_options),
+         (unsigned)offsetof(moe_options, gate_ratio), (unsigned)offsetof(moe_options, force_path),
+         (unsigned)offsetof(moe_options, decode_act), (unsigned)offsetof(moe_options, decode_kernel),
+         (unsigned)offsetof(moe_options, debug_wait_timeout_us), (unsigned)offsetof(moe_options, debug_drop_stage),
+         (unsigned)offsetof(moe_options, reserved));
   return 0;
 }
 """
@@ -308,7 +318,52 @@ def test_header_is_plain_c(lib):
     subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER), src,
                     "-L", libdir, "-lmoe_fp8_block", "-Wl,-rpath," + libdir, "-o", exe], check=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
-    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+    lines = r.stdout.strip().splitlines()
+    assert r.returncode == 0 and lines and lines[0] == "ok", r.stdout + r.stderr
+    # the binding's structures have the layout a C compiler gives the header's
+    for line, cls in zip(lines[1:], (_lib.MoeTensor, _lib.MoeOptions)):
+        f = line.split()
+        assert int(f[1]) == ctypes.sizeof(cls), line
+        layout = {f[i]: int(f[i + 1]) for i in range(2, len(f), 2)}
+        assert layout == {name: getattr(cls, name).offset for name, _ in cls._fields_}, line
     if gxx:
         subprocess.run([gxx, "-std=c++11", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", "c++",
                         "-I", os.path.dirname(HEADER), src], check=True)
+
+
+def _header_signatures():
+    """{function: (return type, [parameter types])} from the header's text."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    sigs = {}
+    for ret, name, params in re.findall(r"((?:const\s+)?\w+\s*\*?)\s*(moe_fp8_block_\w+)\s*\(([^)]*)\)\s*;", src):
+        types = []
+        for prm in params.split(","):
+            prm = " ".join(prm.split())
+            if prm in ("", "void"):
+                continue
+            types.append(re.sub(r"\s*\b\w+$", "", prm).replace(" *", "*"))
+        sigs[name] = (" ".join(ret.split()).replace(" *", "*"), types)
+    return sigs
+
+
+def test_binding_signatures_match_header(lib):
+    """Every ctypes argtype/restype of the binding is the C type the header
+    declares (a mismatched width would pass garbage through the ABI)."""
+    P = ctypes.POINTER
+    vp = ctypes.c_void_p
+    ctype = {
+        "const moe_tensor*": P(_lib.MoeTensor), "moe_tensor*": P(_lib.MoeTensor),
+        "const moe_options*": P(_lib.MoeOptions),
+        "int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "int": ctypes.c_int,
+        "uint32_t*": P(ctypes.c_uint32), "void* const*": P(ctypes.c_void_p),
+        "void*": vp, "const void*": vp, "uint8_t*": vp, "const uint8_t*": vp, "float*": vp, "int32_t*": vp,
+    }
+    rtype = {"int": ctypes.c_int, "const char*": ctypes.c_char_p, "void": None}
+    sigs = _header_signatures()
+    assert sorted(sigs) == sorted(_lib.EXPORTS)
+    for name, (ret, params) in sigs.items():
+        fn = getattr(lib, name)
+        assert fn.restype == rtype[ret], name
+        assert len(fn.argtypes) == len(params), name
+        for i, (have, want) in enumerate(zip(fn.argtypes, params)):
+            assert have == ctype[want], f"{name} argument {i}: {want}"
